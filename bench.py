@@ -1,0 +1,373 @@
+"""Benchmark: masked attention forward on GB300, in TFLOPS of unmasked work.
+
+One step = one pass of the hot path over the workload: build the block mask
+for the batch, then the fused forward (O and LSE). The workload is the bf16
+causal + ALiBi problem (B=4, Hq=Hkv=16, S=2048, D=64) with seeded synthetic
+inputs. FLOPs counted = 4 * D * (kept (q, kv) pairs summed over batch and
+heads): neither the pairs the mask removes nor the masked pairs inside
+partial tiles are counted.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+path has no exchange step), so scaling is weak; rank 0 prints one JSON line.
+``--impl reference`` times the fp64 CPU oracle on the host's cores instead,
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = 2
+METRIC = "attention fwd TFLOPS (unmasked FLOPs) and % of GB300 bf16 dense peak"
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+
+
+def kept_pairs(w) -> int:
+    """Kept (q, kv) pairs of one head, summed over the batch (mask evaluated
+    row-slab by row-slab; the count defines the FLOPs of the metric)."""
+    import numpy as np
+    total = 0
+    j = np.arange(w.Skv)[None, :]
+    for b in range(w.B):
+        for s in range(0, w.Sq, 1024):
+            i = np.arange(s, min(s + 1024, w.Sq))[:, None]
+            keep = np.ones((i.shape[0], w.Skv), bool)
+            if w.causal:
+                keep &= j <= i
+            if w.window is not None:
+                keep &= (i - j) < w.window
+            if w.document:
+                keep &= w.doc_id[b][i] == w.doc_id[b][j]
+            if w.prefix:
+                keep |= j < int(w.prefix_len[b])
+            total += int(keep.sum())
+    return total
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    for name in ("fwd_tc.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "masked_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_digest: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "fwd_tc_causal_alibi_b4h16s2048d64.md")
+    try:
+        with open(path) as f:
+            text = f.read()
+    except OSError:
+        return None
+    digest = traffic = None
+    for line in text.splitlines():
+        if line.startswith("source_digest:"):
+            digest = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    return traffic if digest == kernel_digest else None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4)
+                          if r[5 + k].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def oracle_leg(w, seconds_target: float, cores: int):
+    """Times the CPU oracle on whole heads of the workload (a bounded sample),
+    one head per worker process; returns (TFLOPS, sample description, cores)."""
+    import multiprocessing as mp
+    per_head_pairs = kept_pairs(w) // w.B
+    heads = [(b, h) for b in range(w.B) for h in range(w.Hq)]
+    ctx = mp.get_context("spawn")
+    done = 0
+    t0 = time.perf_counter()
+    with ctx.Pool(processes=cores, initializer=_oracle_worker_init,
+                  initargs=(WORKLOAD,)) as pool:
+        # one warm round loads the inputs in every worker, then the timed rounds
+        pool.map(_oracle_head, heads[:cores])
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds_target and done < len(heads):
+            batch = heads[done:done + cores]
+            pool.map(_oracle_head, batch)
+            done += len(batch)
+    dt = time.perf_counter() - t0
+    flops = 4.0 * w.D * per_head_pairs * done
+    return flops / dt / 1e12, f"{done} of {len(heads)} (b, h) heads, whole rows", cores
+
+
+_W = None
+
+
+def _oracle_worker_init(number):
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    global _W
+    from synth import make_workload
+    _W = make_workload(number)
+
+
+def _oracle_head(bh):
+    from oracle import attention_forward
+    from tests.helpers import oracle_spec
+    attention_forward(_W.q, _W.k, _W.v, oracle_spec(_W), heads=[bh])
+    return bh
+
+
+def run_reference(args, rank: int, world: int) -> None:
+    if rank != 0:
+        return
+    from synth import make_workload
+    w = make_workload(WORKLOAD, with_tensors=False)
+    cores = os.cpu_count() or 1
+    steps = []
+    for _ in range(args.warmup):
+        oracle_leg(w, 2.0, cores)
+    for _ in range(args.steps):
+        steps.append(oracle_leg(w, 8.0, cores))
+    value = statistics.median(s[0] for s in steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_dict(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": steps[0][1] + " per step"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w):
+    return {"workload": f"bf16 causal + ALiBi attention forward, B={w.B} Hq={w.Hq} Hkv={w.Hkv} "
+                        f"S={w.Sq} D={w.D}",
+            "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.Sq, "D": w.D,
+            "variant": "causal + alibi (slope_h = 2^(-8(h+1)/H))", "seed": w.seed,
+            "l2": "flushed between timed steps (512 MiB write)",
+            "step": "build_block_mask + attn_fwd"}
+
+
+def run_ours(args, rank: int, world: int) -> None:
+    import torch
+    import torch.distributed as dist
+
+    import masked_attention_gb300 as M
+    from synth import make_workload
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = make_workload(WORKLOAD)
+    variant = M.MASK_CAUSAL | M.SCORE_ALIBI  # the workload's mask and score terms
+    assert w.causal and w.alibi and not (w.document or w.prefix or w.window or w.softcap)
+    pairs = kept_pairs(w)
+    flops = 4.0 * w.D * pairs * w.Hq  # per step, whole batch
+    stream = torch.cuda.current_stream()
+
+    q, k, v = (t.to(dev) for t in (w.q, w.k, w.v))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device=dev)
+    bm_buf = torch.empty(M.attn_block_mask_bytes(w.B, w.Sq, w.Skv), dtype=torch.uint8,
+                         device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        bm = M.build_block_mask(variant & 0xF, w.B, w.Sq, w.Skv, buf=bm_buf, stream=stream)
+        M.attn_fwd(q, k, v, o, lse, variant, block_mask=bm, stream=stream)
+        return bm
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        step()
+    if M.attn_check_status() != M.ATTN_OK:
+        raise RuntimeError("device status error during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for s in range(args.steps):
+            flush.fill_(s & 0xFF)
+            ev[s][0].record(stream)
+            bm = M.build_block_mask(variant & 0xF, w.B, w.Sq, w.Skv, buf=bm_buf, stream=stream)
+            ev[s][1].record(stream)
+            M.attn_fwd(q, k, v, o, lse, variant, block_mask=bm, stream=stream)
+            ev[s][2].record(stream)
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    if M.attn_check_status() != M.ATTN_OK:
+        raise RuntimeError("device status error during the timed steps")
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    fwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    total_s = sum(step_ms) / 1e3
+    fwd_s = sum(fwd_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s, fwd_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_s, fwd_s = float(t[0]), float(t[1])
+
+    # end to end through the public API: pinned host inputs in, O and LSE out
+    hq, hk, hv = (t.pin_memory() for t in (w.q, w.k, w.v))
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        flush.fill_(2)
+        e2e_step()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    barrier()
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)
+        e2e_ev[s][0].record(stream)
+        e2e_step()
+        e2e_ev[s][1].record(stream)
+    barrier()
+    e2e_s = sum(a.elapsed_time(b) for a, b in e2e_ev) / 1e3
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t[0])
+
+    if rank != 0:
+        return
+    peaks, peak_kind = read_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    value = world * flops * args.steps / total_s / 1e12
+    fwd_tflops = flops * args.steps / fwd_s / 1e12
+    digest = source_digest()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_dict(w),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak,
+                     "unit": "TFLOP/s", "frac": fwd_tflops / peak,
+                     "traffic": profiled_traffic(digest),
+                     "kernel": "fwd_tc_kernel<64, alibi>",
+                     "peak_source": f"{peak_kind} bf16 dense (burst), MEASURED_PEAKS.json"
+                                    if peak_kind == "measured" else "fallback 1.9 PFLOP/s"},
+        "e2e": {"value": world * flops * args.steps / e2e_s / 1e12, "unit": "TFLOPS",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+        "flops_per_step": flops,
+        "fwd_ms_per_launch": fwd_s / args.steps * 1e3,
+        "source_digest": digest,
+    }
+    if not args.no_cpu_baseline:
+        tf, sample, cores = oracle_leg(w, args.cpu_seconds, os.cpu_count() or 1)
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOPS", "cores": cores,
+                                "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,183 @@
+/*
+ * mattn.h - C ABI of the masked-attention library (libmattn.so) for one
+ * NVIDIA GB300 GPU (sm_103a).
+ *
+ * The library computes fused scaled-dot-product attention with an element-wise
+ * score modification and a mask, in one pass over key/value tiles with an
+ * online softmax, so the Sq x Skv score matrix never reaches device memory:
+ *
+ *   s[b,h,i,j] = scale * <q[b,h,i,:], k[b,hk,j,:]>            hk = h / (Hq/Hkv)
+ *   s'         = score_mod(s, b, h, i, j)                       (before softmax)
+ *   O[b,h,i,:] = sum over kept j of softmax_j(s') * v[b,hk,j,:]
+ *   LSE[b,h,i] = ln sum over kept j of exp(s'[b,h,i,j])
+ *
+ * Sources: the FlexAttention page (section "FlexAttention": a user function
+ * score_mod(score, b, h, q_idx, kv_idx) modifies every score before the
+ * softmax; the variant list: causal, relative position, ALiBi, sliding window,
+ * PrefixLM, document masking; the item on exploiting mask sparsity; section
+ * "Performance": a deterministic backward that recomputes intermediates) and
+ * the Online-Softmax/FlashAttention page (abstract: 3-pass safe softmax,
+ * 2-pass online softmax, 1-pass FlashAttention).
+ *
+ * Conventions for every entry point:
+ *  - Buffers are caller-owned. Tensor arguments are DEVICE pointers; structs
+ *    (attn_params, attn_block_mask) live in HOST memory. The library allocates
+ *    no device memory on any call.
+ *  - Layout: contiguous [B, H, S, D], D innermost. Base pointers of q, k, v,
+ *    o, dO, dq, dk, dv must be 16-byte aligned.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream). Argument errors are returned before anything is launched. A
+ *    failed launch returns ATTN_ERR_CUDA. Device-side failures (a bounded wait
+ *    that ran out) are written to the status word and read back with
+ *    attn_check_status().
+ *  - No C++ exception crosses this boundary. The functions are thread-safe.
+ */
+#ifndef MATTN_H_
+#define MATTN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st*` */
+
+typedef enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,        /* NULL pointer, bad size, inconsistent shapes */
+  ATTN_ERR_UNSUPPORTED = 2,        /* valid but not built: D, dtype, tails, variant */
+  ATTN_ERR_MISALIGNED = 3,         /* a tensor base pointer is not 16-byte aligned */
+  ATTN_ERR_WORKSPACE_TOO_SMALL = 4,/* the caller's buffer is smaller than required */
+  ATTN_ERR_CUDA = 5,               /* a CUDA runtime call or a launch failed */
+  ATTN_ERR_TIMEOUT = 6             /* a device-side bounded wait ran out */
+} attn_status;
+
+/* Variant: OR of the bits below; 0 = full (bidirectional) attention with the
+ * identity score_mod. Mask terms combine as
+ *   keep(b,i,j) = (CAUSAL: j <= i) AND (WINDOW: i - j < window)
+ *                 AND (DOCUMENT: doc_id[b][i] == doc_id[b][j])
+ *                 OR  (PREFIX: j < prefix_len[b])
+ * with absent AND-terms true and an absent PREFIX false. i and j are absolute
+ * positions (query row i, key column j), aligned at 0.
+ * Score terms apply in this order: s <- scale * q.k; ALIBI: s <- s - slope_h
+ * * (i - j); SOFTCAP: s <- softcap * tanh(s / softcap). */
+enum {
+  ATTN_MASK_CAUSAL = 1u << 0,   /* FlexAttention page, "Causal Mask" */
+  ATTN_MASK_WINDOW = 1u << 1,   /* "Sliding Window + Causal" (1024 tokens there) */
+  ATTN_MASK_DOCUMENT = 1u << 2, /* variant list: document masking */
+  ATTN_MASK_PREFIX = 1u << 3,   /* variant list: PrefixLM (prefix is bidirectional) */
+  ATTN_SCORE_ALIBI = 1u << 8,   /* variant list: ALiBi; slope_h = 2^(-8(h+1)/Hq) */
+  ATTN_SCORE_SOFTCAP = 1u << 9  /* "Soft-capping" section (Gemma 2, Grok-1) */
+};
+#define ATTN_MASK_BITS 0x0Fu
+#define ATTN_SCORE_BITS 0x300u
+
+enum { ATTN_BF16 = 0, ATTN_F32 = 1 };
+
+/* Tile size of the block mask and of the kernels (query rows x key columns). */
+#define ATTN_TILE 128
+
+/* Block mask: per (batch, 128-row query tile) the ascending lists of
+ * 128-column key tiles that are FULL (every pair kept: no mask evaluated) or
+ * PARTIAL (some pairs kept: the mask is evaluated per element); EMPTY tiles
+ * are skipped (FlexAttention page: exploiting the sparsity of the mask). The
+ * mask does not depend on the head, so one list serves every head. All
+ * pointers below point into the caller's device buffer given to
+ * build_block_mask(); this host struct only describes it.
+ *   full_cnt, part_cnt  int32 [B][nq]
+ *   full_idx, part_idx  int32 [B][nq][nkv]  (first *_cnt entries valid)
+ *   order               int32 [B*nq]: b*nq+qt by descending full+part count
+ *                       (ties by ascending index): longest work first
+ * The t_* members hold the transposed lists (per key tile, its query tiles,
+ * [B][nkv] and [B][nkv][nq]) when built with transposed = 1, else NULL. */
+typedef struct attn_block_mask {
+  int B, Sq, Skv;
+  int nq, nkv;
+  unsigned variant;      /* mask bits it was built for */
+  int window;            /* parameters it was built for */
+  const int* doc_id;
+  const int* prefix_len;
+  const int* full_cnt;
+  const int* part_cnt;
+  const int* full_idx;
+  const int* part_idx;
+  const int* order;
+  const int* t_full_cnt;
+  const int* t_part_cnt;
+  const int* t_full_idx;
+  const int* t_part_idx;
+  const int* t_order;
+} attn_block_mask;
+
+/* Parameters of a call (host struct). */
+typedef struct attn_params {
+  int dtype;                   /* ATTN_BF16 or ATTN_F32: type of q, k, v, o, do, dq, dk, dv */
+  float scale;                 /* multiplies q.k; 0 selects 1/sqrt(D) */
+  int window;                  /* ATTN_MASK_WINDOW: keys with i - j < window; >= 1 */
+  float softcap;               /* ATTN_SCORE_SOFTCAP: cap c > 0 */
+  const float* alibi_slopes;   /* ATTN_SCORE_ALIBI: device fp32 [Hq], or NULL for 2^(-8(h+1)/Hq) */
+  const int* doc_id;           /* ATTN_MASK_DOCUMENT: device int32 [B][max(Sq,Skv)] */
+  const int* prefix_len;       /* ATTN_MASK_PREFIX: device int32 [B] */
+  const attn_block_mask* block_mask; /* from build_block_mask() for the same mask, or NULL:
+                                        then every key tile allowed by the causal bound is
+                                        visited with the mask evaluated per element */
+  int* status;                 /* device int32 status word, or NULL for the library's own */
+  unsigned long long timeout_ns; /* limit of each device-side wait; 0 = 4 s */
+} attn_params;
+
+/* Forward: O = softmax(score_mod(scale*QK^T) under the mask) V and LSE.
+ *   q [B,Hq,Sq,D], k and v [B,Hkv,Skv,D], o [B,Hq,Sq,D] (dtype p->dtype),
+ *   lse fp32 [B,Hq,Sq] (natural log; -inf for a row with no kept key, whose
+ *   O row is 0).
+ * Supported: D in {64, 128}; Hq % Hkv == 0 (GQA: query head h reads key/value
+ * head h / (Hq/Hkv)); ATTN_BF16 needs Sq and Skv multiples of 128 (tcgen05
+ * tensor-core kernel); ATTN_F32 takes any Sq, Skv >= 1 (fp32 FFMA kernel).
+ * Returns ATTN_ERR_UNSUPPORTED for anything else. */
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                     unsigned variant, const attn_params* p, struct CUstream_st* stream);
+
+/* Bytes of device buffer build_block_mask() needs (256-byte aligned pieces). */
+size_t attn_block_mask_bytes(int B, int Sq, int Skv, int transposed);
+
+/* Classifies every (query tile, key tile) pair as full, partial or empty
+ * under the mask bits of `variant` (score bits are ignored) and writes the
+ * lists into `buf` (device, `bytes` long, 256-byte aligned). Fills `*out`
+ * (host) with pointers into `buf`. The result is exact: a tile is full iff
+ * every pair in it is kept and empty iff none is. */
+attn_status build_block_mask(unsigned variant, const attn_params* p, int B, int Sq, int Skv,
+                             void* buf, size_t bytes, int transposed, attn_block_mask* out,
+                             struct CUstream_st* stream);
+
+/* Bytes of fp32 workspace attn_bwd() needs: B*Hq*Sq*4 (the row terms
+ * Delta_i = <dO_i, O_i>). */
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq);
+
+/* Backward of the forward above (FlexAttention page, "Performance": a
+ * deterministic backward that recomputes intermediates instead of storing
+ * them): from q, k, v, o, lse and dO computes
+ *   dq [B,Hq,Sq,D], dk and dv [B,Hkv,Skv,D] (dtype p->dtype; with GQA, dk and
+ *   dv sum over the query heads of their group).
+ * `workspace` is device memory of attn_bwd_workspace_bytes() bytes. No
+ * atomics: results are bitwise reproducible. Supported: ATTN_BF16, D = 128 and
+ * 64, Sq and Skv multiples of 128; a block mask built with transposed = 1 (or
+ * NULL). */
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                     void* workspace, size_t workspace_bytes,
+                     int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                     unsigned variant, const attn_params* p, struct CUstream_st* stream);
+
+/* Synchronises `stream`, reads the device status word (`status_dev`, or the
+ * library's own when NULL), resets it to 0 and returns it as an attn_status. */
+attn_status attn_check_status(int* status_dev, struct CUstream_st* stream);
+
+/* Static string naming a status code. */
+const char* attn_status_str(attn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MATTN_H_ */

@@ -1,0 +1,253 @@
+"""Masked fused attention for one GB300 GPU (sm_103a).
+
+A thin ctypes binding of ``libmattn.so`` (C ABI in ``include/mattn.h``). The
+functions here only marshal arguments: every step of the computation runs in
+the library's CUDA kernels. There is no CPU fallback: if the library has not
+been built (``python -m masked_attention_gb300._build``), loading it raises.
+
+Tensors are passed as torch CUDA tensors (or raw device addresses as ints);
+PyTorch provides device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+__all__ = [
+    "MASK_CAUSAL", "MASK_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX", "SCORE_ALIBI",
+    "SCORE_SOFTCAP", "BF16", "F32", "AttnError", "BlockMask", "attn_fwd", "attn_bwd",
+    "build_block_mask", "attn_block_mask_bytes", "attn_bwd_workspace_bytes",
+    "attn_check_status", "attn_status_str", "lib", "LIB_PATH",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmattn.so")
+
+# Mirrors of the constants in include/mattn.h (a test checks they agree).
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_MISALIGNED = 0, 1, 2, 3
+ATTN_ERR_WORKSPACE_TOO_SMALL, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = 4, 5, 6
+MASK_CAUSAL, MASK_WINDOW, MASK_DOCUMENT, MASK_PREFIX = 1 << 0, 1 << 1, 1 << 2, 1 << 3
+SCORE_ALIBI, SCORE_SOFTCAP = 1 << 8, 1 << 9
+BF16, F32 = 0, 1
+TILE = 128
+
+
+class attn_block_mask(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Sq", ctypes.c_int), ("Skv", ctypes.c_int),
+                ("nq", ctypes.c_int), ("nkv", ctypes.c_int), ("variant", ctypes.c_uint),
+                ("window", ctypes.c_int), ("doc_id", ctypes.c_void_p),
+                ("prefix_len", ctypes.c_void_p), ("full_cnt", ctypes.c_void_p),
+                ("part_cnt", ctypes.c_void_p), ("full_idx", ctypes.c_void_p),
+                ("part_idx", ctypes.c_void_p), ("order", ctypes.c_void_p),
+                ("t_full_cnt", ctypes.c_void_p), ("t_part_cnt", ctypes.c_void_p),
+                ("t_full_idx", ctypes.c_void_p), ("t_part_idx", ctypes.c_void_p),
+                ("t_order", ctypes.c_void_p)]
+
+
+class attn_params(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int), ("scale", ctypes.c_float), ("window", ctypes.c_int),
+                ("softcap", ctypes.c_float), ("alibi_slopes", ctypes.c_void_p),
+                ("doc_id", ctypes.c_void_p), ("prefix_len", ctypes.c_void_p),
+                ("block_mask", ctypes.POINTER(attn_block_mask)), ("status", ctypes.c_void_p),
+                ("timeout_ns", ctypes.c_ulonglong)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m masked_attention_gb300._build` (no CPU fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, u, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
+        P = ctypes.POINTER(attn_params)
+        BM = ctypes.POINTER(attn_block_mask)
+        L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, u, P, vp]
+        L.attn_fwd.restype = i
+        L.attn_block_mask_bytes.argtypes = [i, i, i, i]
+        L.attn_block_mask_bytes.restype = sz
+        L.build_block_mask.argtypes = [u, P, i, i, i, vp, sz, i, BM, vp]
+        L.build_block_mask.restype = i
+        L.attn_bwd_workspace_bytes.argtypes = [i, i, i]
+        L.attn_bwd_workspace_bytes.restype = sz
+        L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, u, P,
+                               vp]
+        L.attn_bwd.restype = i
+        L.attn_check_status.argtypes = [vp, vp]
+        L.attn_check_status.restype = i
+        L.attn_status_str.argtypes = [i]
+        L.attn_status_str.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_status_str(status)} (status {status})")
+
+
+def attn_status_str(status: int) -> str:
+    return lib().attn_status_str(int(status)).decode()
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != ATTN_OK:
+        raise AttnError(status, where)
+
+
+class BlockMask:
+    """A block mask built on the device. Holds the device buffer (a torch
+    uint8 tensor) and the host struct that describes it."""
+
+    def __init__(self, buf, struct: attn_block_mask, keep_alive: tuple):
+        self.buf = buf
+        self.struct = struct
+        self._keep = keep_alive
+
+    @property
+    def nq(self) -> int:
+        return self.struct.nq
+
+    @property
+    def nkv(self) -> int:
+        return self.struct.nkv
+
+    def to_host(self) -> dict:
+        """Copies the lists to the host (for tests and inspection)."""
+        import torch
+        s = self.struct
+        base = self.buf.data_ptr()
+
+        def view(addr, n):
+            off = addr - base
+            return self.buf[off:off + 4 * n].view(torch.int32).cpu().numpy()
+
+        B, nq, nkv = s.B, s.nq, s.nkv
+        out = dict(full_cnt=view(s.full_cnt, B * nq).reshape(B, nq),
+                   part_cnt=view(s.part_cnt, B * nq).reshape(B, nq),
+                   full_idx=view(s.full_idx, B * nq * nkv).reshape(B, nq, nkv),
+                   part_idx=view(s.part_idx, B * nq * nkv).reshape(B, nq, nkv),
+                   order=view(s.order, B * nq))
+        if s.t_full_cnt:
+            out.update(t_full_cnt=view(s.t_full_cnt, B * nkv).reshape(B, nkv),
+                       t_part_cnt=view(s.t_part_cnt, B * nkv).reshape(B, nkv),
+                       t_full_idx=view(s.t_full_idx, B * nkv * nq).reshape(B, nkv, nq),
+                       t_part_idx=view(s.t_part_idx, B * nkv * nq).reshape(B, nkv, nq),
+                       t_order=view(s.t_order, B * nkv))
+        return out
+
+
+def _params(dtype: int, scale: float, window: int, softcap: float, alibi_slopes, doc_id,
+            prefix_len, block_mask: Optional[BlockMask], status, timeout_ns: int) -> attn_params:
+    p = attn_params()
+    p.dtype = dtype
+    p.scale = scale
+    p.window = window
+    p.softcap = softcap
+    p.alibi_slopes = _ptr(alibi_slopes)
+    p.doc_id = _ptr(doc_id)
+    p.prefix_len = _ptr(prefix_len)
+    p.block_mask = ctypes.pointer(block_mask.struct) if block_mask is not None else None
+    p.status = _ptr(status)
+    p.timeout_ns = timeout_ns
+    return p
+
+
+def attn_block_mask_bytes(B: int, Sq: int, Skv: int, transposed: bool = False) -> int:
+    return int(lib().attn_block_mask_bytes(B, Sq, Skv, int(transposed)))
+
+
+def attn_bwd_workspace_bytes(B: int, Hq: int, Sq: int) -> int:
+    return int(lib().attn_bwd_workspace_bytes(B, Hq, Sq))
+
+
+def build_block_mask(variant: int, B: int, Sq: int, Skv: int, *, window: int = 0, doc_id=None,
+                     prefix_len=None, transposed: bool = False, device="cuda",
+                     buf=None, stream=None) -> BlockMask:
+    """Builds the block mask on the device (``buf``: optional caller buffer,
+    a uint8 CUDA tensor of at least ``attn_block_mask_bytes`` bytes)."""
+    import torch
+    nbytes = attn_block_mask_bytes(B, Sq, Skv, transposed)
+    if buf is None:
+        buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    p = _params(BF16, 0.0, window, 0.0, None, doc_id, prefix_len, None, None, 0)
+    out = attn_block_mask()
+    st = lib().build_block_mask(variant, ctypes.byref(p), B, Sq, Skv, _ptr(buf),
+                                buf.numel() if hasattr(buf, "numel") else nbytes,
+                                int(transposed), ctypes.byref(out), _stream(stream))
+    _check(st, "build_block_mask")
+    return BlockMask(buf, out, (doc_id, prefix_len))
+
+
+def attn_fwd(q, k, v, o, lse, variant: int = 0, *, B=None, Hq=None, Hkv=None, Sq=None,
+             Skv=None, D=None, dtype: Optional[int] = None, scale: float = 0.0, window: int = 0,
+             softcap: float = 0.0, alibi_slopes=None, doc_id=None, prefix_len=None,
+             block_mask: Optional[BlockMask] = None, status=None, timeout_ns: int = 0,
+             stream=None) -> None:
+    """O and LSE of masked attention; writes ``o`` and ``lse`` in place.
+
+    ``q`` [B,Hq,Sq,D], ``k``/``v`` [B,Hkv,Skv,D], ``o`` like ``q``, ``lse`` fp32
+    [B,Hq,Sq]. Shapes come from the tensors unless given explicitly (needed
+    when raw addresses are passed)."""
+    if B is None:
+        B, Hq, Sq, D = q.shape
+        Hkv, Skv = k.shape[1], k.shape[2]
+    if dtype is None:
+        import torch
+        dtype = F32 if q.dtype == torch.float32 else BF16
+    p = _params(dtype, scale, window, softcap, alibi_slopes, doc_id, prefix_len, block_mask,
+                status, timeout_ns)
+    st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
+                        variant, ctypes.byref(p), _stream(stream))
+    _check(st, "attn_fwd")
+
+
+def attn_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, variant: int = 0, *,
+             scale: float = 0.0, window: int = 0, softcap: float = 0.0, alibi_slopes=None,
+             doc_id=None, prefix_len=None, block_mask: Optional[BlockMask] = None, status=None,
+             timeout_ns: int = 0, stream=None) -> None:
+    """dQ, dK, dV of ``sum(dO * O)``; writes ``dq``, ``dk``, ``dv`` in place.
+    ``workspace``: a CUDA tensor of at least ``attn_bwd_workspace_bytes`` bytes."""
+    import torch
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    dtype = F32 if q.dtype == torch.float32 else BF16
+    p = _params(dtype, scale, window, softcap, alibi_slopes, doc_id, prefix_len, block_mask,
+                status, timeout_ns)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
+                        _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, B, Hq, Hkv, Sq, Skv, D,
+                        variant, ctypes.byref(p), _stream(stream))
+    _check(st, "attn_bwd")
+
+
+def attn_check_status(status=None, stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status word."""
+    return int(lib().attn_check_status(_ptr(status), _stream(stream)))
+
+
+def default_scale(D: int) -> float:
+    return 1.0 / math.sqrt(D)

@@ -1,0 +1,317 @@
+// The exported C ABI (include/mattn.h): argument checks, block-mask buffer
+// layout, and dispatch to the kernels. Every check returns before anything
+// is launched; nothing here allocates device memory.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "launch.h"
+
+#define MATTN_API extern "C" __attribute__((visibility("default")))
+
+namespace mattn {
+namespace {
+
+__device__ int g_status;  // status word used when the caller passes none
+
+int* default_status() {
+  // one address per device (a module variable has a separate copy per device)
+  static int* addr[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int*>(p);
+  }
+  return addr[dev];
+}
+
+__global__ void fill_empty_rows(void* o, float* lse, size_t rows, int D, int elem_bytes) {
+  const size_t n = rows * (size_t)D;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n;
+       e += (size_t)gridDim.x * blockDim.x) {
+    if (elem_bytes == 4) static_cast<float*>(o)[e] = 0.0f;
+    else static_cast<uint16_t*>(o)[e] = 0;
+    if (e % D == 0) lse[e / D] = -INFINITY;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr unsigned kKnownBits = ATTN_MASK_BITS | ATTN_SCORE_BITS;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct MaskLayout {
+  size_t full_cnt, part_cnt, full_idx, part_idx, order;
+  size_t t_full_cnt, t_part_cnt, t_full_idx, t_part_idx, t_order;
+  size_t total;
+};
+
+MaskLayout mask_layout(int B, int Sq, int Skv, int transposed) {
+  const size_t nq = (size_t)(Sq + kTile - 1) / kTile, nkv = (size_t)(Skv + kTile - 1) / kTile;
+  const size_t I = sizeof(int);
+  MaskLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align256(bytes);
+    return at;
+  };
+  L.full_cnt = take(I * B * nq);
+  L.part_cnt = take(I * B * nq);
+  L.full_idx = take(I * B * nq * nkv);
+  L.part_idx = take(I * B * nq * nkv);
+  L.order = take(I * B * nq);
+  if (transposed) {
+    L.t_full_cnt = take(I * B * nkv);
+    L.t_part_cnt = take(I * B * nkv);
+    L.t_full_idx = take(I * B * nkv * nq);
+    L.t_part_idx = take(I * B * nkv * nq);
+    L.t_order = take(I * B * nkv);
+  }
+  L.total = off;
+  return L;
+}
+
+attn_status check_mask_params(unsigned variant, const attn_params* p, int B) {
+  if (variant & ~kKnownBits) return ATTN_ERR_INVALID_ARG;
+  if ((variant & ATTN_MASK_WINDOW) && p->window < 1) return ATTN_ERR_INVALID_ARG;
+  if ((variant & ATTN_MASK_DOCUMENT) && !p->doc_id) return ATTN_ERR_INVALID_ARG;
+  if ((variant & ATTN_MASK_PREFIX) && !p->prefix_len) return ATTN_ERR_INVALID_ARG;
+  if ((variant & ATTN_SCORE_SOFTCAP) && !(p->softcap > 0.0f)) return ATTN_ERR_INVALID_ARG;
+  (void)B;
+  return ATTN_OK;
+}
+
+MaskArgs mask_args(unsigned variant, const attn_params* p, int Sq, int Skv) {
+  MaskArgs m;
+  m.variant = variant & ATTN_MASK_BITS;
+  m.window = p->window;
+  m.doc_id = p->doc_id;
+  m.doc_len = Sq > Skv ? Sq : Skv;
+  m.prefix_len = p->prefix_len;
+  return m;
+}
+
+// The block mask must describe the same mask and shape as the call.
+attn_status check_block_mask(const attn_block_mask* bm, unsigned variant, const attn_params* p,
+                             int B, int Sq, int Skv, bool need_transposed) {
+  if (!bm) return ATTN_OK;
+  const unsigned mbits = variant & ATTN_MASK_BITS;
+  if (bm->B != B || bm->Sq != Sq || bm->Skv != Skv || bm->variant != mbits)
+    return ATTN_ERR_INVALID_ARG;
+  if ((mbits & ATTN_MASK_WINDOW) && bm->window != p->window) return ATTN_ERR_INVALID_ARG;
+  if ((mbits & ATTN_MASK_DOCUMENT) && bm->doc_id != p->doc_id) return ATTN_ERR_INVALID_ARG;
+  if ((mbits & ATTN_MASK_PREFIX) && bm->prefix_len != p->prefix_len) return ATTN_ERR_INVALID_ARG;
+  if (!bm->full_cnt || !bm->part_cnt || !bm->full_idx || !bm->part_idx || !bm->order)
+    return ATTN_ERR_INVALID_ARG;
+  if (need_transposed && (!bm->t_full_cnt || !bm->t_part_cnt || !bm->t_full_idx ||
+                          !bm->t_part_idx || !bm->t_order))
+    return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+attn_status fill_problem(FwdProblem& f, const void* q, const void* k, const void* v, void* o,
+                         float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                         unsigned variant, const attn_params* p) {
+  if (!p) return ATTN_ERR_INVALID_ARG;
+  if (B < 0 || Hq < 1 || Hkv < 1 || Sq < 0 || Skv < 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (p->dtype != ATTN_BF16 && p->dtype != ATTN_F32) return ATTN_ERR_UNSUPPORTED;
+  attn_status st = check_mask_params(variant, p, B);
+  if (st != ATTN_OK) return st;
+  if (!std::isfinite(p->scale)) return ATTN_ERR_INVALID_ARG;
+  f = FwdProblem{};
+  f.q = q;
+  f.k = k;
+  f.v = v;
+  f.o = o;
+  f.lse = lse;
+  f.B = B;
+  f.Hq = Hq;
+  f.Hkv = Hkv;
+  f.Sq = Sq;
+  f.Skv = Skv;
+  f.D = D;
+  f.variant = variant;
+  f.mask = mask_args(variant, p, Sq, Skv);
+  f.score.scale = p->scale != 0.0f ? p->scale : 1.0f / std::sqrt((float)D);
+  f.score.softcap = p->softcap;
+  f.score.slopes = p->alibi_slopes;
+  f.score.Hq = Hq;
+  if (p->block_mask) {
+    const attn_block_mask* bm = p->block_mask;
+    f.lists = BlockLists{bm->full_cnt, bm->part_cnt, bm->full_idx, bm->part_idx, bm->order,
+                         bm->nq, bm->nkv};
+  } else {
+    f.lists = BlockLists{nullptr, nullptr, nullptr, nullptr, nullptr, 0, 0};
+  }
+  f.status = p->status;  // resolved by resolve_status() once every check has passed
+  f.timeout_ns = p->timeout_ns ? p->timeout_ns : 4000000000ull;
+  return ATTN_OK;
+}
+
+attn_status resolve_status(FwdProblem& f) {
+  if (!f.status) f.status = default_status();
+  return f.status ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace mattn
+
+using namespace mattn;
+
+MATTN_API const char* attn_status_str(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_MISALIGNED: return "tensor base pointer not 16-byte aligned";
+    case ATTN_ERR_WORKSPACE_TOO_SMALL: return "buffer too small";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+MATTN_API size_t attn_block_mask_bytes(int B, int Sq, int Skv, int transposed) {
+  if (B < 0 || Sq < 0 || Skv < 0) return 0;
+  return mask_layout(B, Sq, Skv, transposed).total;
+}
+
+MATTN_API attn_status build_block_mask(unsigned variant, const attn_params* p, int B, int Sq,
+                                       int Skv, void* buf, size_t bytes, int transposed,
+                                       attn_block_mask* out, struct CUstream_st* stream) {
+  if (!p || !out || B < 1 || Sq < 1 || Skv < 1) return ATTN_ERR_INVALID_ARG;
+  attn_status st = check_mask_params(variant, p, B);
+  if (st != ATTN_OK) return st;
+  if (!buf) return ATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(buf) & 255u) return ATTN_ERR_MISALIGNED;
+  const MaskLayout L = mask_layout(B, Sq, Skv, transposed);
+  if (bytes < L.total) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+  const MaskArgs m = mask_args(variant, p, Sq, Skv);
+  char* base = static_cast<char*>(buf);
+  auto at = [&](size_t off) { return reinterpret_cast<int*>(base + off); };
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_block_mask(m, B, Sq, Skv, 0, at(L.full_cnt), at(L.part_cnt), at(L.full_idx),
+                        at(L.part_idx), at(L.order), s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  attn_block_mask r{};
+  r.B = B;
+  r.Sq = Sq;
+  r.Skv = Skv;
+  r.nq = (Sq + kTile - 1) / kTile;
+  r.nkv = (Skv + kTile - 1) / kTile;
+  r.variant = variant & ATTN_MASK_BITS;
+  r.window = p->window;
+  r.doc_id = (variant & ATTN_MASK_DOCUMENT) ? p->doc_id : nullptr;
+  r.prefix_len = (variant & ATTN_MASK_PREFIX) ? p->prefix_len : nullptr;
+  r.full_cnt = at(L.full_cnt);
+  r.part_cnt = at(L.part_cnt);
+  r.full_idx = at(L.full_idx);
+  r.part_idx = at(L.part_idx);
+  r.order = at(L.order);
+  if (transposed) {
+    if (launch_block_mask(m, B, Sq, Skv, 1, at(L.t_full_cnt), at(L.t_part_cnt),
+                          at(L.t_full_idx), at(L.t_part_idx), at(L.t_order), s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    r.t_full_cnt = at(L.t_full_cnt);
+    r.t_part_cnt = at(L.t_part_cnt);
+    r.t_full_idx = at(L.t_full_idx);
+    r.t_part_idx = at(L.t_part_idx);
+    r.t_order = at(L.t_order);
+  }
+  *out = r;
+  return ATTN_OK;
+}
+
+MATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int Hq, int Hkv, int Sq, int Skv, int D, unsigned variant,
+                               const attn_params* p, struct CUstream_st* stream) {
+  FwdProblem f;
+  attn_status st = fill_problem(f, q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, variant, p);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || Sq == 0) return ATTN_OK;
+  if (!q || !o || !lse || (Skv > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return ATTN_ERR_MISALIGNED;
+  st = check_block_mask(p->block_mask, variant, p, B, Sq, Skv, false);
+  if (st != ATTN_OK) return st;
+  if (p->dtype == ATTN_BF16 && (Sq % kTile != 0 || Skv % kTile != 0)) return ATTN_ERR_UNSUPPORTED;
+  st = resolve_status(f);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int elem = p->dtype == ATTN_F32 ? 4 : 2;
+  if (Skv == 0) {  // every row is empty: O = 0, LSE = -inf
+    fill_empty_rows<<<256, 256, 0, s>>>(o, lse, (size_t)B * Hq * Sq, D, elem);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+  cudaError_t e;
+  if (p->dtype == ATTN_F32) {
+    e = launch_fwd_f32(f, s);
+  } else {
+    e = launch_fwd_tc(f, s);
+  }
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+MATTN_API size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq) {
+  if (B < 0 || Hq < 0 || Sq < 0) return 0;
+  return sizeof(float) * (size_t)B * Hq * Sq;
+}
+
+MATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                               void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                               int Sq, int Skv, int D, unsigned variant, const attn_params* p,
+                               struct CUstream_st* stream) {
+  BwdProblem bp;
+  attn_status st = fill_problem(bp.f, q, k, v, const_cast<void*>(o), const_cast<float*>(lse), B,
+                                Hq, Hkv, Sq, Skv, D, variant, p);
+  if (st != ATTN_OK) return st;
+  if (p->dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (Sq % kTile != 0 || Skv % kTile != 0) return ATTN_ERR_UNSUPPORTED;
+  if (B == 0 || Sq == 0 || Skv == 0) return ATTN_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+    return ATTN_ERR_MISALIGNED;
+  if (workspace_bytes < attn_bwd_workspace_bytes(B, Hq, Sq)) return ATTN_ERR_WORKSPACE_TOO_SMALL;
+  st = check_block_mask(p->block_mask, variant, p, B, Sq, Skv, true);
+  if (st != ATTN_OK) return st;
+  st = resolve_status(bp.f);
+  if (st != ATTN_OK) return st;
+  bp.dO = dO;
+  bp.dq = dq;
+  bp.dk = dk;
+  bp.dv = dv;
+  bp.delta = static_cast<float*>(workspace);
+  if (p->block_mask) {
+    const attn_block_mask* bm = p->block_mask;
+    bp.t_lists = BlockLists{bm->t_full_cnt, bm->t_part_cnt, bm->t_full_idx, bm->t_part_idx,
+                            bm->t_order, bm->nkv, bm->nq};
+  } else {
+    bp.t_lists = BlockLists{nullptr, nullptr, nullptr, nullptr, nullptr, 0, 0};
+  }
+  const cudaError_t e = launch_bwd_tc(bp, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+MATTN_API attn_status attn_check_status(int* status_dev, struct CUstream_st* stream) {
+  int* addr = status_dev ? status_dev : default_status();
+  if (!addr) return ATTN_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, addr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (h != 0 && cudaMemset(addr, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return static_cast<attn_status>(h);
+}

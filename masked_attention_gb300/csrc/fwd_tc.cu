@@ -1,0 +1,565 @@
+// bf16 forward on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// Algorithm: the 1-pass FlashAttention recurrence named on the
+// Online-Softmax/FlashAttention page (online softmax: running max m, running
+// sum l, accumulator rescaled when m grows), with score_mod applied per element
+// before the softmax and the mask applied only on partial tiles (FlexAttention
+// page: "FlexAttention" section, the variant list, and the item on exploiting
+// mask sparsity). The score matrix never leaves the SM.
+//
+// Work unit: one 128-row query tile of two query heads (2h, 2h+1) of one batch
+// element; both heads see the same key-tile list because the mask does not
+// depend on the head. Units are taken longest-first (block-mask `order`) by a
+// persistent grid of one CTA per SM.
+//
+// Warp roles (384 threads, three warpgroups):
+//   warps 0-3  softmax for head A (thread t owns query row t: TMEM lane t)
+//   warps 4-7  softmax for head B
+//   warp  8    TMA producer: Q tiles once per unit, then K/V tiles into a ring
+//   warp  9    MMA issuer (one thread) and TMEM owner
+//   warps 10-11 idle
+// The third warpgroup hands registers to the softmax warpgroups (setmaxnreg).
+// Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A, O_B (D columns
+// each) from 256. P (bf16) overwrites the first 64 columns of its S tile and
+// is the A operand of the P.V product, read straight from TMEM.
+//
+// Per key tile j and head X:  S_X = Q_X K_j^T (SS MMA) -> softmax warps read
+// S_X, write P_X -> O_X += P_X V_j (TS MMA). The MMA warp alternates heads so
+// one head's softmax overlaps the other head's products.
+#include <cmath>
+#include <mutex>
+
+#include "launch.h"
+
+namespace mattn {
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kRegsSoftmax = 224;  // 2 x 128 x 224 + 128 x 56 = 64512 = 384 x 168
+constexpr int kRegsOther = 56;
+constexpr int kSoftmaxThreads = 128;
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+
+template <int D>
+struct Cfg {
+  static constexpr int kTileBytes = kTile * D * 2;  // one 128-row bf16 tile
+  static constexpr int kBoxes = D / 64;             // 64-column (128-byte) TMA boxes
+  static constexpr int kBoxBytes = kTile * 128;
+  static constexpr int kSlots = D == 128 ? 4 : 8;   // K/V ring
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffSlots = 2 * kTileBytes;
+  static constexpr int kOffBars = kOffSlots + kSlots * kTileBytes;
+  // barriers: q_full, q_empty, drain, s_full[2], p_full[2], o_done[2], o_free[2],
+  // slot_full[kSlots], slot_empty[kSlots]
+  static constexpr int kNumBars = 11 + 2 * kSlots;
+  static constexpr int kOffDoc = kOffBars + kNumBars * 8;
+  static constexpr int kOffMisc = kOffDoc + 8 * kTile * 4;  // per-warp doc ids
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;     // slack for 1024-byte alignment
+  static constexpr uint32_t kColO0 = 256;
+};
+
+struct Unit {
+  int b, qt, h[2];  // h[1] < 0: single-head unit
+  int n_full, n_part;
+  const int* lf;
+  const int* lp;
+  __device__ __forceinline__ int n() const { return n_full + n_part; }
+  __device__ __forceinline__ int kt(int j) const {
+    return j < n_full ? (lf ? lf[j] : j) : (lp ? lp[j - n_full] : j - n_full);
+  }
+};
+
+__device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp) {
+  const int nq = p.Sq / kTile, nkv = p.Skv / kTile;
+  const int rank = u / nhp, hp = u % nhp;
+  const bool causal_bound = (p.variant & ATTN_MASK_CAUSAL) && !(p.variant & ATTN_MASK_PREFIX);
+  int row;
+  if (p.lists.full_cnt) {
+    row = p.lists.order[rank];
+  } else if (causal_bound) {
+    row = (rank % p.B) * nq + (nq - 1 - rank / p.B);  // longest first
+  } else {
+    row = rank;
+  }
+  Unit U;
+  U.b = row / nq;
+  U.qt = row % nq;
+  U.h[0] = 2 * hp;
+  U.h[1] = 2 * hp + 1 < p.Hq ? 2 * hp + 1 : -1;
+  if (p.lists.full_cnt) {
+    U.n_full = p.lists.full_cnt[row];
+    U.n_part = p.lists.part_cnt[row];
+    U.lf = p.lists.full_idx + (size_t)row * p.lists.nkv;
+    U.lp = p.lists.part_idx + (size_t)row * p.lists.nkv;
+  } else {
+    const int last = causal_bound ? min(nkv, U.qt + 1) : nkv;
+    const bool masked = (p.variant & ATTN_MASK_BITS) != 0;
+    U.n_full = masked ? 0 : last;
+    U.n_part = masked ? last : 0;
+    U.lf = U.lp = nullptr;
+  }
+  return U;
+}
+
+// Drain wait used on the abort path: ignores the abort flag, short limit.
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > 200000000ull) return;
+  }
+}
+
+template <int D, int SCORE>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdProblem p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sSlots = smem + C::kOffSlots;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* drain = bars + 2;
+  uint64_t* s_full = bars + 3;   // [2]
+  uint64_t* p_full = bars + 5;   // [2]
+  uint64_t* o_done = bars + 7;   // [2]
+  uint64_t* o_free = bars + 9;   // [2]
+  uint64_t* slot_full = bars + 11;
+  uint64_t* slot_empty = bars + 11 + C::kSlots;
+  int* sdoc = reinterpret_cast<int*>(smem + C::kOffDoc);
+  uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Watchdog wd{abort_flag, p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(drain, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(s_full + x, 1);
+      mbar_init(p_full + x, kSoftmaxThreads);
+      mbar_init(o_done + x, 1);
+      mbar_init(o_free + x, kSoftmaxThreads);
+    }
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(slot_full + s, 1);
+      mbar_init(slot_empty + s, 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(tmem_base_smem, 512);
+    tmem_relinquish();
+  }
+  if (warp == kWarpProducer && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_base_smem;
+
+  const int nhp = (p.Hq + 1) / 2;
+  const int num_units = p.B * (p.Sq / kTile) * nhp;
+  const int group = p.Hq / p.Hkv;
+
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+  }
+  if (warp == kWarpProducer) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t slot_it = 0, q_it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const Unit U = decode_unit(p, u, nhp);
+        const int n = U.n();
+        if (n == 0) continue;
+        const bool two = U.h[1] >= 0;
+        const int hk0 = U.h[0] / group, hk1 = two ? U.h[1] / group : hk0;
+        const bool shared = !two || hk0 == hk1;
+        ok = wait_bounded(q_empty, (q_it & 1) ^ 1, wd);
+        if (!ok) break;
+        mbar_arrive_expect_tx(q_full, (two ? 2 : 1) * C::kTileBytes);
+        for (int x = 0; x < (two ? 2 : 1); ++x) {
+          const int row = (U.b * p.Hq + U.h[x]) * p.Sq + U.qt * kTile;
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_2d(sQ + x * C::kTileBytes + bx * C::kBoxBytes, &tm_q, q_full, bx * 64, row);
+        }
+        ++q_it;
+        for (int j = 0; j < n && ok; ++j) {
+          const int kt = U.kt(j);
+          const int rows[2] = {(U.b * p.Hkv + hk0) * p.Skv + kt * kTile,
+                               (U.b * p.Hkv + hk1) * p.Skv + kt * kTile};
+          // order: K_A, [K_B], V_A, [V_B]
+          for (int t = 0; t < (shared ? 2 : 4) && ok; ++t) {
+            const int per = shared ? 1 : 2;
+            const bool is_v = t >= per;
+            const int x = shared ? 0 : (t % 2);
+            const int slot = slot_it % C::kSlots;
+            ok = wait_bounded(slot_empty + slot, ((slot_it / C::kSlots) & 1) ^ 1, wd);
+            if (!ok) break;
+            mbar_arrive_expect_tx(slot_full + slot, C::kTileBytes);
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+              tma_load_2d(sSlots + slot * C::kTileBytes + bx * C::kBoxBytes, is_v ? &tm_v : &tm_k,
+                          slot_full + slot, bx * 64, rows[x]);
+            ++slot_it;
+          }
+        }
+      }
+      if (!ok) {  // let copies in flight land before the CTA exits
+        for (uint32_t k = 0; k < C::kSlots && k < slot_it; ++k) {
+          const uint32_t it = slot_it - 1 - k;
+          wait_drain(slot_full + it % C::kSlots, (it / C::kSlots) & 1);
+        }
+        if (q_it > 0) wait_drain(q_full, (q_it - 1) & 1);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false);
+      constexpr uint32_t kIdescPV = idesc_bf16(128, D, true);
+      const uint32_t sQ_addr = smem_u32(sQ);
+      const uint32_t slots_addr = smem_u32(sSlots);
+      uint32_t slot_it = 0, q_it = 0, p_it[2] = {0, 0}, o_it[2] = {0, 0};
+      bool ok = true;
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        const Unit U = decode_unit(p, u, nhp);
+        const int n = U.n();
+        if (n == 0) continue;
+        const bool two = U.h[1] >= 0;
+        const bool shared = !two || (U.h[0] / group == U.h[1] / group);
+        const int T = shared ? 2 : 4;  // ring slots per key tile
+        ok = wait_bounded(q_full, q_it & 1, wd);
+        if (!ok) break;
+        ++q_it;
+        tc_fence_after();
+        // slot sequence numbers of key tile j for head x
+        auto k_seq = [&](int j, int x) -> uint32_t {
+          return slot_it + j * T + (shared ? 0 : x);
+        };
+        auto v_seq = [&](int j, int x) -> uint32_t {
+          return slot_it + j * T + (shared ? 1 : 2 + x);
+        };
+        auto issue_s = [&](int j, int x) -> bool {
+          const uint32_t seq = k_seq(j, x);
+          const uint32_t slot = seq % C::kSlots;
+          if (x == 0 || !shared) {
+            if (!wait_bounded(slot_full + slot, (seq / C::kSlots) & 1, wd)) return false;
+            tc_fence_after();
+          }
+          const uint32_t a0 = sQ_addr + x * C::kTileBytes;
+          const uint32_t b0 = slots_addr + slot * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
+            mma_bf16_ss(tmem + 128u * x, sdesc_sw128(a0 + off, 16, 1024),
+                        sdesc_sw128(b0 + off, 16, 1024), kIdescQK, kk > 0);
+          }
+          mma_commit(s_full + x);
+          if (!shared || x == 1 || !two) mma_commit(slot_empty + slot);
+          return true;
+        };
+        auto issue_pv = [&](int j, int x) -> bool {
+          if (!wait_bounded(p_full + x, p_it[x] & 1, wd)) return false;
+          ++p_it[x];
+          if (j == 0) {
+            if (!wait_bounded(o_free + x, (o_it[x] & 1) ^ 1, wd)) return false;
+            ++o_it[x];
+          }
+          const uint32_t seq = v_seq(j, x);
+          const uint32_t slot = seq % C::kSlots;
+          if (x == 0 || !shared) {
+            if (!wait_bounded(slot_full + slot, (seq / C::kSlots) & 1, wd)) return false;
+          }
+          tc_fence_after();
+          const uint32_t b0 = slots_addr + slot * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            mma_bf16_ts(tmem + C::kColO0 + D * x, tmem + 128u * x + kk * 8,
+                        sdesc_sw128(b0 + kk * 16 * 128, C::kBoxBytes, 1024), kIdescPV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          if (!shared || x == 1 || !two) mma_commit(slot_empty + slot);
+          return true;
+        };
+        const int nx = two ? 2 : 1;
+        for (int x = 0; x < nx && ok; ++x) ok = issue_s(0, x);
+        if (ok && n == 1) mma_commit(q_empty);
+        for (int j = 0; j < n && ok; ++j) {
+          for (int x = 0; x < nx && ok; ++x) {
+            ok = issue_pv(j, x);
+            if (!ok) break;
+            if (j + 1 < n) ok = issue_s(j + 1, x);
+            else mma_commit(o_done + x);
+          }
+          if (ok && j + 1 == n - 1) mma_commit(q_empty);
+        }
+        slot_it += n * T;
+      }
+      // all products issued by this thread are complete before TMEM is freed
+      mma_commit(drain);
+      wait_drain(drain, 0);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------- softmax
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    const int x = warp / 4;            // head slot 0 or 1
+    const int t = threadIdx.x & 127;   // query row within the tile == TMEM lane
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    const uint32_t colS = tmem + lane_base + 128u * x;
+    const uint32_t colO = tmem + lane_base + C::kColO0 + D * x;
+    int* wdoc = sdoc + warp * kTile;   // this warp's copy of the key tile's document ids
+    const float sl2 = p.score.scale * kLog2e;
+    uint32_t s_it = 0, o_it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const Unit U = decode_unit(p, u, nhp);
+      const int h = U.h[x];
+      if (h < 0) continue;
+      const int n = U.n();
+      const int i = U.qt * kTile + t;
+      const size_t orow = ((size_t)(U.b * p.Hq + h) * p.Sq + i);
+      __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + orow * D;
+      if (n == 0) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(O)[c] = z;
+        p.lse[orow] = -INFINITY;
+        continue;
+      }
+      const float slope = (SCORE & 1) ? alibi_slope(p.score, h) : 0.0f;
+      const float slope2 = slope * kLog2e;
+      const int* docb = (p.variant & ATTN_MASK_DOCUMENT)
+                            ? p.mask.doc_id + (size_t)U.b * p.mask.doc_len : nullptr;
+      const int doc_i = docb ? docb[i] : 0;
+      const int P = (p.variant & ATTN_MASK_PREFIX) ? p.mask.prefix_len[U.b] : INT_MIN;
+      float m_ref = -INFINITY, l = 0.0f;
+
+      for (int j = 0; j < n; ++j) {
+        const int kt = U.kt(j);
+        const int j0 = kt * kTile;
+        const bool partial = j >= U.n_full;
+        if (partial && docb) {
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) wdoc[lane + 32 * c] = docb[j0 + lane + 32 * c];
+          __syncwarp();
+        }
+        ok = __all_sync(0xffffffffu, wait_bounded(s_full + x, s_it & 1, wd));
+        if (!ok) break;
+        ++s_it;
+        tc_fence_after();
+        float s[kTile];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(colS + 32 * c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(r[e]);
+        }
+        // score_mod, in log2 units
+        const float base = float(j0 - i);  // (j - i) = base + c
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) {
+          if constexpr (SCORE == 0) {
+            s[c] = s[c] * sl2;
+          } else if constexpr (SCORE == 1) {
+            s[c] = fmaf(s[c], sl2, slope2 * (base + float(c)));
+          } else if constexpr (SCORE == 2) {
+            s[c] = (p.score.softcap * kLog2e) *
+                   tanh_approx(s[c] * (p.score.scale / p.score.softcap));
+          } else {
+            const float y = fmaf(s[c], p.score.scale, slope * (base + float(c)));
+            s[c] = (p.score.softcap * kLog2e) * tanh_approx(y * (1.0f / p.score.softcap));
+          }
+        }
+        if (partial) {  // mask_mod on the tile's pairs
+          const int hi = (p.variant & ATTN_MASK_CAUSAL) ? i - j0 : INT_MAX;
+          const int lo = (p.variant & ATTN_MASK_WINDOW) ? i - j0 - p.mask.window : INT_MIN;
+          const int pre = P == INT_MIN ? INT_MIN : P - j0;
+#pragma unroll
+          for (int c = 0; c < kTile; ++c) {
+            bool keep = (c <= hi) && (c > lo);
+            if (docb) keep = keep && (wdoc[c] == doc_i);
+            keep = keep || (c < pre);
+            s[c] = keep ? s[c] : -INFINITY;
+          }
+        }
+        float mt = s[0];
+#pragma unroll
+        for (int c = 1; c < kTile; ++c) mt = fmaxf(mt, s[c]);
+        // lazy rescale: move the reference max only when it grows by > 2^8
+        const bool grow = mt > m_ref + kRescaleThreshold;
+        float alpha = 1.0f;
+        if (grow) {
+          alpha = ex2_approx(m_ref - mt);  // m_ref = -inf gives 0
+          l *= alpha;
+        }
+        const bool need_o = grow && j > 0 && m_ref != -INFINITY;
+        if (__any_sync(0xffffffffu, need_o)) {
+          const float a = need_o ? alpha : 1.0f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(colO + 32 * c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a);
+            tmem_st32(colO + 32 * c, r);
+          }
+        }
+        if (grow) m_ref = mt;
+        const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
+        float sum = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float p0 = ex2_approx(s[64 * c + 2 * e] - m_use);
+            const float p1 = ex2_approx(s[64 * c + 2 * e + 1] - m_use);
+            sum += p0 + p1;
+            r[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(colS + 32 * c, r);
+        }
+        l += sum;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full + x);
+      }
+      if (!ok) break;
+      // epilogue: O / l -> bf16, LSE = ln(sum exp)
+      ok = __all_sync(0xffffffffu, wait_bounded(o_done + x, o_it & 1, wd));
+      if (!ok) break;
+      ++o_it;
+      tc_fence_after();
+      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(colO + 32 * c, r);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+        uint4* dst = reinterpret_cast<uint4*>(O + 32 * c);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+      }
+      tc_fence_before();
+      mbar_arrive(o_free + x);
+      p.lse[orow] = l > 0.0f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ----------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2-D view [rows, D] of a [B, H, S, D] bf16 tensor; box = 128 rows x 64 columns,
+// 128-byte swizzle (the layout the tcgen05 descriptors above expect).
+bool make_map(CUtensorMap* map, const void* base, long long rows, int D) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+template <int D, int SCORE>
+cudaError_t launch_typed(const FwdProblem& p, cudaStream_t stream) {
+  using C = Cfg<D>;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, p.q, (long long)p.B * p.Hq * p.Sq, D) ||
+      !make_map(&mk, p.k, (long long)p.B * p.Hkv * p.Skv, D) ||
+      !make_map(&mv, p.v, (long long)p.B * p.Hkv * p.Skv, D))
+    return cudaErrorInvalidValue;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(fwd_tc_kernel<D, SCORE>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int units = p.B * (p.Sq / kTile) * ((p.Hq + 1) / 2);
+  const int grid = units < sm_count() ? units : sm_count();
+  if (grid == 0) return cudaSuccess;
+  fwd_tc_kernel<D, SCORE><<<grid, kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const FwdProblem& p, cudaStream_t stream) {
+  const int score = ((p.variant & ATTN_SCORE_ALIBI) ? 1 : 0) |
+                    ((p.variant & ATTN_SCORE_SOFTCAP) ? 2 : 0);
+  if (p.D == 64) {
+    switch (score) {
+      case 0: return launch_typed<64, 0>(p, stream);
+      case 1: return launch_typed<64, 1>(p, stream);
+      case 2: return launch_typed<64, 2>(p, stream);
+      default: return launch_typed<64, 3>(p, stream);
+    }
+  }
+  switch (score) {
+    case 0: return launch_typed<128, 0>(p, stream);
+    case 1: return launch_typed<128, 1>(p, stream);
+    case 2: return launch_typed<128, 2>(p, stream);
+    default: return launch_typed<128, 3>(p, stream);
+  }
+}
+
+}  // namespace mattn

@@ -1,0 +1,47 @@
+// Internal interface between the C ABI (api.cu) and the kernel translation
+// units. Nothing here is exported from the shared library.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace mattn {
+
+struct FwdProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, Hq, Hkv, Sq, Skv, D;
+  unsigned variant;
+  MaskArgs mask;
+  ScoreArgs score;
+  BlockLists lists;  // lists.full_cnt == nullptr: visit every tile the causal bound allows
+  int* status;
+  uint64_t timeout_ns;
+};
+
+struct BwdProblem {
+  FwdProblem f;        // q, k, v, o (read), lse (read)
+  const void* dO;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;        // workspace [B, Hq, Sq]
+  BlockLists t_lists;  // transposed lists (per key tile), or full_cnt == nullptr
+};
+
+// Block-mask builder: writes counts, ascending index lists and the
+// longest-first order for the per-query-tile (transposed = 0) or per-key-tile
+// (transposed = 1) view.
+cudaError_t launch_block_mask(const MaskArgs& m, int B, int Sq, int Skv, int transposed,
+                              int* cnt_full, int* cnt_part, int* idx_full, int* idx_part,
+                              int* order, cudaStream_t stream);
+
+cudaError_t launch_fwd_f32(const FwdProblem& p, cudaStream_t stream);
+cudaError_t launch_fwd_tc(const FwdProblem& p, cudaStream_t stream);
+cudaError_t launch_bwd_tc(const BwdProblem& p, cudaStream_t stream);
+
+}  // namespace mattn

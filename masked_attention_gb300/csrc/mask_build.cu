@@ -1,0 +1,171 @@
+// Block-mask builder (FlexAttention page, item on exploiting the sparsity of
+// the attention mask): for every (query tile, key tile) pair decide whether all,
+// some or none of its pairs are kept, then write ascending lists of the full
+// and partial tiles, plus a longest-first order of the list rows.
+//
+// Classification is exact. Interval bounds decide most tiles without looking
+// at single pairs (causal, window and prefix terms from the tile corners, the
+// document term from the min/max document id of each range); a tile whose
+// bounds decide nothing is classified by evaluating the mask on its pairs.
+#include "launch.h"
+
+namespace mattn {
+namespace {
+
+constexpr int kEmpty = 0, kPartial = 1, kFull = 2;
+
+struct Range {
+  int lo, hi;  // inclusive
+};
+
+__device__ __forceinline__ void warp_doc_minmax(const int* doc, Range r, int& mn, int& mx) {
+  const int lane = threadIdx.x & 31;
+  mn = INT_MAX;
+  mx = INT_MIN;
+  for (int p = r.lo + lane; p <= r.hi; p += 32) {
+    const int d = doc[p];
+    mn = min(mn, d);
+    mx = max(mx, d);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+}
+
+// Sound tri-state per term: 2 = every pair kept, 0 = no pair kept, 1 = unknown.
+__device__ __forceinline__ int bounds_state(const MaskArgs& m, int b, Range ri, Range rj,
+                                            int qmin, int qmax, int kmin, int kmax) {
+  bool and_all = true, and_none = false;
+  if (m.variant & ATTN_MASK_CAUSAL) {  // j <= i
+    and_all = and_all && (rj.hi <= ri.lo);
+    and_none = and_none || (rj.lo > ri.hi);
+  }
+  if (m.variant & ATTN_MASK_WINDOW) {  // i - j < W
+    and_all = and_all && (ri.hi - rj.lo < m.window);
+    and_none = and_none || (ri.lo - rj.hi >= m.window);
+  }
+  if (m.variant & ATTN_MASK_DOCUMENT) {  // doc[i] == doc[j]
+    and_all = and_all && (qmin == qmax && kmin == kmax && qmin == kmin);
+    and_none = and_none || (qmax < kmin || kmax < qmin);
+  }
+  if (m.variant & ATTN_MASK_PREFIX) {  // OR j < P
+    const int P = m.prefix_len[b];
+    if (rj.hi < P) return kFull;
+    const bool pre_none = rj.lo >= P;
+    if (and_none && pre_none) return kEmpty;
+    if (and_all) return kFull;
+    return kPartial + 8;  // undecided
+  }
+  if (and_none) return kEmpty;
+  if (and_all) return kFull;
+  return kPartial + 8;  // undecided
+}
+
+__global__ void __launch_bounds__(128) classify_kernel(MaskArgs m, int Sq, int Skv,
+                                                       int transposed, int* cnt_full,
+                                                       int* cnt_part, int* idx_full,
+                                                       int* idx_part) {
+  extern __shared__ signed char sstate[];
+  const int b = blockIdx.y;
+  const int outer = blockIdx.x;
+  const int nq = (Sq + kTile - 1) / kTile;
+  const int nkv = (Skv + kTile - 1) / kTile;
+  const int n_outer = transposed ? nkv : nq;
+  const int n_inner = transposed ? nq : nkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int* doc = (m.variant & ATTN_MASK_DOCUMENT) ? m.doc_id + (size_t)b * m.doc_len : nullptr;
+
+  const int outer_len = transposed ? Skv : Sq;
+  const Range ro{outer * kTile, min((outer + 1) * kTile, outer_len) - 1};
+  int omin = 0, omax = 0;
+  if (doc) warp_doc_minmax(doc, ro, omin, omax);  // every warp computes it
+
+  for (int inner = warp; inner < n_inner; inner += 4) {
+    const int inner_len = transposed ? Sq : Skv;
+    const Range rn{inner * kTile, min((inner + 1) * kTile, inner_len) - 1};
+    int nmin = 0, nmax = 0;
+    if (doc) warp_doc_minmax(doc, rn, nmin, nmax);
+    const Range ri = transposed ? rn : ro;
+    const Range rj = transposed ? ro : rn;
+    const int qmin = transposed ? nmin : omin, qmax = transposed ? nmax : omax;
+    const int kmin = transposed ? omin : nmin, kmax = transposed ? omax : nmax;
+    int st = bounds_state(m, b, ri, rj, qmin, qmax, kmin, kmax);
+    if (st >= 8) {  // undecided: look at the pairs
+      bool any_keep = false, any_drop = false;
+      const int ncols = rj.hi - rj.lo + 1;
+      for (int i = ri.lo; i <= ri.hi; ++i) {
+        for (int c = lane; c < ncols; c += 32) {
+          const bool k = mask_keep(m, b, i, rj.lo + c);
+          any_keep |= k;
+          any_drop |= !k;
+        }
+        if (__any_sync(0xffffffffu, any_keep) && __any_sync(0xffffffffu, any_drop)) break;
+      }
+      const bool wk = __any_sync(0xffffffffu, any_keep);
+      const bool wd = __any_sync(0xffffffffu, any_drop);
+      st = wk ? (wd ? kPartial : kFull) : kEmpty;
+    }
+    if (lane == 0) sstate[inner] = static_cast<signed char>(st);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const size_t row = (size_t)b * n_outer + outer;
+    int nf = 0, np = 0;
+    for (int inner = 0; inner < n_inner; ++inner) {
+      const int st = sstate[inner];
+      if (st == kFull) idx_full[row * n_inner + nf++] = inner;
+      else if (st == kPartial) idx_part[row * n_inner + np++] = inner;
+    }
+    cnt_full[row] = nf;
+    cnt_part[row] = np;
+  }
+}
+
+// Longest-first order of the B * n_outer list rows: counting sort on the
+// number of visited tiles (full + partial), descending, ties by row index.
+__global__ void order_kernel(const int* cnt_full, const int* cnt_part, int n_rows, int n_inner,
+                             int* order) {
+  extern __shared__ int hist[];  // n_inner + 2 buckets
+  for (int c = threadIdx.x; c < n_inner + 2; c += blockDim.x) hist[c] = 0;
+  __syncthreads();
+  for (int r = threadIdx.x; r < n_rows; r += blockDim.x)
+    atomicAdd(&hist[cnt_full[r] + cnt_part[r]], 1);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int pos = 0;  // exclusive prefix from the largest cost down
+    for (int c = n_inner; c >= 0; --c) {
+      const int n = hist[c];
+      hist[c] = pos;
+      pos += n;
+    }
+    for (int r = 0; r < n_rows; ++r) order[hist[cnt_full[r] + cnt_part[r]]++] = r;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_block_mask(const MaskArgs& m, int B, int Sq, int Skv, int transposed,
+                              int* cnt_full, int* cnt_part, int* idx_full, int* idx_part,
+                              int* order, cudaStream_t stream) {
+  const int nq = (Sq + kTile - 1) / kTile;
+  const int nkv = (Skv + kTile - 1) / kTile;
+  const int n_outer = transposed ? nkv : nq;
+  const int n_inner = transposed ? nq : nkv;
+  dim3 grid(n_outer, B);
+  classify_kernel<<<grid, 128, n_inner, stream>>>(m, Sq, Skv, transposed, cnt_full, cnt_part,
+                                                  idx_full, idx_part);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t hist_bytes = sizeof(int) * (size_t)(n_inner + 2);
+  if (hist_bytes > 48 * 1024) {
+    e = cudaFuncSetAttribute(order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)hist_bytes);
+    if (e != cudaSuccess) return e;
+  }
+  order_kernel<<<1, 256, hist_bytes, stream>>>(cnt_full, cnt_part, B * n_outer, n_inner, order);
+  return cudaGetLastError();
+}
+
+}  // namespace mattn
