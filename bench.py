@@ -222,7 +222,7 @@ def run_ours(args, rank: int, world: int) -> None:
     local = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = make_workload(WORKLOAD)
+    w = make_workload(WORKLOAD, **({"B": args.batch} if args.batch else {}))
     variant = M.MASK_CAUSAL | M.SCORE_ALIBI  # the workload's mask and score terms
     assert w.causal and w.alibi and not (w.document or w.prefix or w.window or w.softcap)
     pairs = kept_pairs(w)
@@ -239,12 +239,18 @@ def run_ours(args, rank: int, world: int) -> None:
     def step():
         bm = M.build_block_mask(variant & 0xF, w.B, w.Sq, w.Skv, buf=bm_buf, stream=stream)
         M.attn_fwd(q, k, v, o, lse, variant, block_mask=bm, stream=stream)
-        return bm
 
     def barrier():
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
+
+    def max_over_ranks(*vals):
+        if world == 1:
+            return vals
+        t = torch.tensor(vals, device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return tuple(float(x) for x in t)
 
     for _ in range(max(args.warmup, 3)):
         flush.fill_(1)
@@ -252,63 +258,56 @@ def run_ours(args, rank: int, world: int) -> None:
     if M.attn_check_status() != M.ATTN_OK:
         raise RuntimeError("device status error during warm-up")
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
+          for _ in range(args.steps)]
     barrier()
     with ClockSampler(local) as clocks:
-        t_wall = time.perf_counter()
         for s in range(args.steps):
-            flush.fill_(s & 0xFF)
+            flush.fill_(s & 0xFF)  # L2 flush, outside the events
             ev[s][0].record(stream)
             bm = M.build_block_mask(variant & 0xF, w.B, w.Sq, w.Skv, buf=bm_buf, stream=stream)
             ev[s][1].record(stream)
             M.attn_fwd(q, k, v, o, lse, variant, block_mask=bm, stream=stream)
             ev[s][2].record(stream)
         barrier()
-        t_wall = time.perf_counter() - t_wall
     if M.attn_check_status() != M.ATTN_OK:
         raise RuntimeError("device status error during the timed steps")
-    step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    fwd_ms = [b.elapsed_time(c) for _, b, c in ev]
-    total_s = sum(step_ms) / 1e3
-    fwd_s = sum(fwd_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s, fwd_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s, fwd_s = float(t[0]), float(t[1])
+    total_s = sum(a.elapsed_time(c) for a, _, c in ev) / 1e3
+    fwd_s = sum(b.elapsed_time(c) for _, b, c in ev) / 1e3
+    total_s, fwd_s = max_over_ranks(total_s, fwd_s)
 
-    # end to end through the public API: pinned host inputs in, O and LSE out
-    hq, hk, hv = (t.pin_memory() for t in (w.q, w.k, w.v))
-    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    e2e = None
+    if not args.no_e2e:
+        # end to end through the public API: pinned host inputs in, O and LSE out
+        hq, hk, hv = (t.pin_memory() for t in (w.q, w.k, w.v))
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
 
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        step()
-        ho.copy_(o, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
 
-    for _ in range(3):
-        flush.fill_(2)
-        e2e_step()
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    barrier()
-    for s in range(args.steps):
-        flush.fill_(s & 0xFF)
-        e2e_ev[s][0].record(stream)
-        e2e_step()
-        e2e_ev[s][1].record(stream)
-    barrier()
-    e2e_s = sum(a.elapsed_time(b) for a, b in e2e_ev) / 1e3
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t[0])
+        for _ in range(3):
+            flush.fill_(2)
+            e2e_step()
+        eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        barrier()
+        for s in range(args.steps):
+            flush.fill_(s & 0xFF)
+            eev[s][0].record(stream)
+            e2e_step()
+            eev[s][1].record(stream)
+        barrier()
+        (e2e_s,) = max_over_ranks(sum(a.elapsed_time(b) for a, b in eev) / 1e3)
+        e2e = {"value": world * flops * args.steps / e2e_s / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     if rank != 0:
         return
@@ -326,15 +325,15 @@ def run_ours(args, rank: int, world: int) -> None:
         "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak,
                      "unit": "TFLOP/s", "frac": fwd_tflops / peak,
                      "traffic": profiled_traffic(digest),
-                     "kernel": "fwd_tc_kernel<64, alibi>",
-                     "peak_source": f"{peak_kind} bf16 dense (burst), MEASURED_PEAKS.json"
-                                    if peak_kind == "measured" else "fallback 1.9 PFLOP/s"},
-        "e2e": {"value": world * flops * args.steps / e2e_s / 1e12, "unit": "TFLOPS",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                     "kernel": "fwd_tc_kernel<D=64, ALiBi>",
+                     "peak_source": ("measured bf16 dense burst (MEASURED_PEAKS.json)"
+                                     if peak_kind == "measured" else "fallback 1.9 PFLOP/s")},
+        "e2e": e2e,
         "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
         "flops_per_step": flops,
         "fwd_ms_per_launch": fwd_s / args.steps * 1e3,
+        "mask_ms_per_step": (total_s - fwd_s) / args.steps * 1e3,
         "source_digest": digest,
     }
     if not args.no_cpu_baseline:
@@ -352,6 +351,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0, help="override B (profiling cases only)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

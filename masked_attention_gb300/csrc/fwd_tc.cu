@@ -29,6 +29,7 @@
 #include <cmath>
 #include <mutex>
 
+#include "host_util.h"
 #include "launch.h"
 
 namespace mattn {
@@ -102,14 +103,6 @@ __device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp)
     U.lf = U.lp = nullptr;
   }
   return U;
-}
-
-// Drain wait used on the abort path: ignores the abort flag, short limit.
-__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_ns() - t0 > 200000000ull) return;
-  }
 }
 
 template <int D, int SCORE>
@@ -479,53 +472,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ----------------------------------------------------------------- host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
-// 2-D view [rows, D] of a [B, H, S, D] bf16 tensor; box = 128 rows x 64 columns,
-// 128-byte swizzle (the layout the tcgen05 descriptors above expect).
-bool make_map(CUtensorMap* map, const void* base, long long rows, int D) {
-  EncodeTiledFn fn = get_encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, 128};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int sm_count() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
-}
-
 template <int D, int SCORE>
 cudaError_t launch_typed(const FwdProblem& p, cudaStream_t stream) {
   using C = Cfg<D>;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, p.q, (long long)p.B * p.Hq * p.Sq, D) ||
-      !make_map(&mk, p.k, (long long)p.B * p.Hkv * p.Skv, D) ||
-      !make_map(&mv, p.v, (long long)p.B * p.Hkv * p.Skv, D))
+  if (!make_map_bf16(&mq, p.q, (long long)p.B * p.Hq * p.Sq, D) ||
+      !make_map_bf16(&mk, p.k, (long long)p.B * p.Hkv * p.Skv, D) ||
+      !make_map_bf16(&mv, p.v, (long long)p.B * p.Hkv * p.Skv, D))
     return cudaErrorInvalidValue;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;

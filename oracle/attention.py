@@ -160,7 +160,7 @@ def attention_forward(q, k, v, spec: Spec, rows: Optional[Sequence[int]] = None,
             m = np.where(keep, s, NEG_INF).max(axis=1)
             m_safe = np.where(np.isfinite(m), m, 0.0)
             # pass 2: sum of exponentials relative to the maximum
-            e = np.where(keep, np.exp(s - m_safe[:, None]), 0.0)
+            e = np.exp(np.where(keep, s - m_safe[:, None], -np.inf))
             l = e.sum(axis=1)
             # pass 3: normalise and weight the values
             with np.errstate(invalid="ignore", divide="ignore"):

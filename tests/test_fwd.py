@@ -55,7 +55,8 @@ def check(w, O, L, O_ref, L_ref, rows=None):
         bad = (err > tol) & mask[..., None]
         assert not bad.any(), (err[mask].max(), int(bad.sum()))
     both_inf = np.isneginf(L) & np.isneginf(L_ref)
-    lerr = np.where(both_inf, 0.0, np.abs(L - L_ref))[mask]
+    with np.errstate(invalid="ignore"):
+        lerr = np.where(both_inf, 0.0, np.abs(L - L_ref))[mask]
     assert lerr.max() <= lse_tol(w, L_ref), lerr.max()
 
 
