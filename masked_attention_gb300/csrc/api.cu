@@ -280,7 +280,8 @@ MATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, cons
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
     return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace))
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
+      !aligned16(lse) || ((variant & ATTN_MASK_DOCUMENT) && !aligned16(p->doc_id)))
     return ATTN_ERR_MISALIGNED;
   if (workspace_bytes < attn_bwd_workspace_bytes(B, Hq, Sq)) return ATTN_ERR_WORKSPACE_TOO_SMALL;
   st = check_block_mask(p->block_mask, variant, p, B, Sq, Skv, true);

@@ -1,0 +1,98 @@
+"""Backward parity: dQ, dK, dV of the CUDA path against the oracle's analytic
+fp64 gradients (FlexAttention page, "Performance": a deterministic backward
+that recomputes intermediates).
+
+Tolerance: bf16 outputs, |g - g_ref| <= max(1e-2, 0.5 ulp_bf16(g_ref) +
+1e-2 |g_ref| / 8). The kernels round P and dS to bf16 before the products
+(relative 2^-9 per term), so a gradient that sums many terms of one sign
+carries an error proportional to its size; 1/8 of 1e-2 relative covers 2^-9
+with margin, and below |g_ref| = 1 the 1e-2 bound of the task applies as is.
+"""
+import numpy as np
+import pytest
+
+from oracle import attention_backward
+from synth import make_workload
+from tests.helpers import GpuRun, oracle_spec
+
+pytestmark = pytest.mark.gpu
+
+
+def grad_tol(ref):
+    a = np.abs(ref)
+    ulp = np.where(a > 0, 2.0 ** (np.floor(np.log2(np.maximum(a, 1e-30))) - 7), 0.0)
+    return np.maximum(1e-2, 0.5 * ulp + 1e-2 * a / 8)
+
+
+def run_bwd(w, use_block_mask=True):
+    import torch
+    import masked_attention_gb300 as M
+    g = GpuRun(w, use_block_mask=use_block_mask, transposed=True)
+    O, L = g.fwd()
+    dq = torch.empty_like(g.q)
+    dk = torch.empty_like(g.k)
+    dv = torch.empty_like(g.v)
+    ws = torch.empty(M.attn_bwd_workspace_bytes(w.B, w.Hq, w.Sq), dtype=torch.uint8,
+                     device="cuda")
+    M.attn_bwd(g.q, g.k, g.v, O, L, g.do, dq, dk, dv, ws, g.variant, **g.kwargs())
+    torch.cuda.synchronize()
+    assert M.attn_check_status() == M.ATTN_OK
+    return g, dq, dk, dv
+
+
+def check_grads(w, dq, dk, dv, heads=None):
+    dQ, dK, dV, _, _ = attention_backward(w.q, w.k, w.v, w.do, oracle_spec(w), heads=heads)
+    out = {}
+    for name, got, ref in (("dq", dq, dQ), ("dk", dk, dK), ("dv", dv, dV)):
+        got = got.float().cpu().numpy().astype(np.float64)
+        if heads is not None:
+            sel = [(b, h if name == "dq" else h // (w.Hq // w.Hkv)) for b, h in heads]
+            got = np.stack([got[b, h] for b, h in sel])
+            ref = np.stack([ref[b, h] for b, h in sel])
+        err = np.abs(got - ref)
+        bad = err > grad_tol(ref)
+        out[name] = float(err.max())
+        assert not bad.any(), (name, float(err.max()), int(bad.sum()))
+    return out
+
+
+CASES = {
+    "causal_d128": dict(B=2, Hq=2, Hkv=2, S=512, D=128, causal=True),
+    "causal_alibi_d64": dict(B=1, Hq=4, Hkv=4, S=768, D=64, causal=True, alibi=True),
+    "gqa_prefix_softcap_d128": dict(B=1, Hq=4, Hkv=2, S=512, D=128, causal=True, prefix=True,
+                                    softcap=20.0, prefix_lo=100, prefix_hi=300),
+    "doc_window_causal_d128": dict(B=1, Hq=2, Hkv=2, S=1024, D=128, causal=True, window=300,
+                                   document=True, doc_lo=100, doc_hi=500),
+    "full_d64": dict(B=1, Hq=2, Hkv=1, S=384, D=64),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_bwd_reduced(name):
+    w = make_workload(0, seed=500 + sorted(CASES).index(name), backward=True, **CASES[name])
+    _, dq, dk, dv = run_bwd(w)
+    check_grads(w, dq, dk, dv)
+
+
+@pytest.mark.parametrize("name", ["causal_d128", "doc_window_causal_d128"])
+def test_bwd_without_block_mask(name):
+    w = make_workload(0, seed=500 + sorted(CASES).index(name), backward=True, **CASES[name])
+    _, dq, dk, dv = run_bwd(w, use_block_mask=False)
+    check_grads(w, dq, dk, dv)
+
+
+def test_bwd_full_size_workload5_sampled_heads():
+    """The training-step workload at full size; every gradient of three
+    (b, h) heads is checked (heads are independent under MHA)."""
+    w = make_workload(5)
+    _, dq, dk, dv = run_bwd(w)
+    check_grads(w, dq, dk, dv, heads=[(0, 0), (3, 7), (7, 15)])
+
+
+def test_bwd_deterministic():
+    import torch
+    w = make_workload(0, seed=77, backward=True, **CASES["gqa_prefix_softcap_d128"])
+    _, a, b, c = run_bwd(w)
+    for _ in range(2):
+        _, a2, b2, c2 = run_bwd(w)
+        assert torch.equal(a, a2) and torch.equal(b, b2) and torch.equal(c, c2)
