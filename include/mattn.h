@@ -113,7 +113,7 @@ typedef struct attn_block_mask {
 /* Parameters of a call (host struct). */
 typedef struct attn_params {
   int dtype;                   /* ATTN_BF16 or ATTN_F32: type of q, k, v, o, do, dq, dk, dv */
-  float scale;                 /* multiplies q.k; 0 selects 1/sqrt(D) */
+  float scale;                 /* multiplies q.k, > 0; 0 selects 1/sqrt(D) */
   int window;                  /* ATTN_MASK_WINDOW: keys with i - j < window; >= 1 */
   float softcap;               /* ATTN_SCORE_SOFTCAP: cap c > 0 */
   const float* alibi_slopes;   /* ATTN_SCORE_ALIBI: device fp32 [Hq], or NULL for 2^(-8(h+1)/Hq) */

@@ -125,7 +125,7 @@ attn_status fill_problem(FwdProblem& f, const void* q, const void* k, const void
   if (p->dtype != ATTN_BF16 && p->dtype != ATTN_F32) return ATTN_ERR_UNSUPPORTED;
   attn_status st = check_mask_params(variant, p, B);
   if (st != ATTN_OK) return st;
-  if (!std::isfinite(p->scale)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(p->scale) || p->scale < 0.0f) return ATTN_ERR_INVALID_ARG;
   f = FwdProblem{};
   f.q = q;
   f.k = k;

@@ -298,6 +298,57 @@ __device__ __forceinline__ float tanh_approx(float x) {
   return y;
 }
 
+// Packed fp32 pairs (sm_100 family): two lanes of fp32 arithmetic per instruction.
+union F2 {
+  float2 f;
+  unsigned long long u;
+};
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  F2 x, y, z, d;
+  x.f = a;
+  y.f = b;
+  z.f = c;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.u) : "l"(x.u), "l"(y.u), "l"(z.u));
+  return d.f;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  F2 x, y, d;
+  x.f = a;
+  y.f = b;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d.u) : "l"(x.u), "l"(y.u));
+  return d.f;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  F2 x, y, d;
+  x.f = a;
+  y.f = b;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d.u) : "l"(x.u), "l"(y.u));
+  return d.f;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of n (a multiple of 16) values with 8 independent chains.
+template <int N>
+__device__ __forceinline__ float row_max(const float* v) {
+  float m[8];
+#pragma unroll
+  for (int a = 0; a < 8; ++a) m[a] = fmaxf(v[a], v[a + 8]);
+#pragma unroll
+  for (int c = 16; c < N; c += 16) {
+#pragma unroll
+    for (int a = 0; a < 8; ++a) m[a] = fmax3(m[a], v[c + a], v[c + 8 + a]);
+  }
+  return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half), .y = hi
   return *reinterpret_cast<uint32_t*>(&v);

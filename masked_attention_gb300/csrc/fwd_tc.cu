@@ -41,7 +41,6 @@ constexpr int kRegsOther = 56;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
 
 template <int D>
 struct Cfg {
@@ -68,10 +67,28 @@ struct Unit {
   const int* lf;
   const int* lp;
   __device__ __forceinline__ int n() const { return n_full + n_part; }
+  // Visiting order: partial tiles, then full tiles, each from the largest key
+  // index down. Keys near the query usually carry the largest scores (causal
+  // diagonal, ALiBi), so the running maximum settles early and the
+  // accumulator is rarely rescaled. The softmax result does not depend on it.
+  __device__ __forceinline__ bool partial(int j) const { return j < n_part; }
   __device__ __forceinline__ int kt(int j) const {
-    return j < n_full ? (lf ? lf[j] : j) : (lp ? lp[j - n_full] : j - n_full);
+    if (j < n_part) {
+      const int a = n_part - 1 - j;
+      return lp ? lp[a] : a;
+    }
+    const int a = n_full - 1 - (j - n_part);
+    return lf ? lf[a] : a;
   }
 };
+
+// Static schedule of a persistent CTA: round r takes unit r*G + c for even r
+// and r*G + (G-1-c) for odd r (G CTAs, c = blockIdx.x). On a longest-first
+// unit order this zigzag evens out the total work per CTA.
+__device__ __forceinline__ int zigzag_unit(int r) {
+  const int c = (r & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
+  return r * (int)gridDim.x + c;
+}
 
 __device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp) {
   const int nq = p.Sq / kTile, nkv = p.Skv / kTile;
@@ -176,7 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t slot_it = 0, q_it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
+        const int u = zigzag_unit(r);
+        if (u >= num_units) continue;
         const Unit U = decode_unit(p, u, nhp);
         const int n = U.n();
         if (n == 0) continue;
@@ -229,7 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t slots_addr = smem_u32(sSlots);
       uint32_t slot_it = 0, q_it = 0, p_it[2] = {0, 0}, o_it[2] = {0, 0};
       bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
+        const int u = zigzag_unit(r);
+        if (u >= num_units) continue;
         const Unit U = decode_unit(p, u, nhp);
         const int n = U.n();
         if (n == 0) continue;
@@ -316,10 +337,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t colS = tmem + lane_base + 128u * x;
     const uint32_t colO = tmem + lane_base + C::kColO0 + D * x;
     int* wdoc = sdoc + warp * kTile;   // this warp's copy of the key tile's document ids
-    const float sl2 = p.score.scale * kLog2e;
+    const float sl2 = p.score.scale * kLog2e;              // raw score -> log2 units
+    const float sc = p.score.scale / p.score.softcap;      // raw score -> tanh argument
+    const float cl2 = p.score.softcap * kLog2e;            // tanh -> log2 units
     uint32_t s_it = 0, o_it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+    for (int rr = 0; rr * (int)gridDim.x < num_units && ok; ++rr) {
+      const int u = zigzag_unit(rr);
+      if (u >= num_units) continue;
       const Unit U = decode_unit(p, u, nhp);
       const int h = U.h[x];
       if (h < 0) continue;
@@ -340,11 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int doc_i = docb ? docb[i] : 0;
       const int P = (p.variant & ATTN_MASK_PREFIX) ? p.mask.prefix_len[U.b] : INT_MIN;
       float m_ref = -INFINITY, l = 0.0f;
+      int kt_next = U.kt(0);
 
       for (int j = 0; j < n; ++j) {
-        const int kt = U.kt(j);
+        const int kt = kt_next;
+        if (j + 1 < n) kt_next = U.kt(j + 1);  // issued early: used next iteration
         const int j0 = kt * kTile;
-        const bool partial = j >= U.n_full;
+        const bool partial = U.partial(j);
         if (partial && docb) {
           __syncwarp();
 #pragma unroll
@@ -356,81 +383,114 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++s_it;
         tc_fence_after();
         float s[kTile];
+        auto load_s = [&]() {
+          uint32_t* r = reinterpret_cast<uint32_t*>(s);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld32(colS + 32 * c, r);
+          for (int c = 0; c < 4; ++c)
+            tmem_ld32(colS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
           tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(r[e]);
-        }
-        // score_mod, in log2 units
+        };
         const float base = float(j0 - i);  // (j - i) = base + c
-#pragma unroll
-        for (int c = 0; c < kTile; ++c) {
+        const int hi = (p.variant & ATTN_MASK_CAUSAL) ? i - j0 : INT_MAX;
+        const int lo = (p.variant & ATTN_MASK_WINDOW) ? i - j0 - p.mask.window : INT_MIN;
+        const int pre = P == INT_MIN ? INT_MIN : P - j0;
+        // s <- score_mod(s) in log2 units minus `shift`, masked entries -inf
+        auto transform = [&](float shift) {
           if constexpr (SCORE == 0) {
-            s[c] = s[c] * sl2;
+            const float2 m2 = make_float2(sl2, sl2), sh2 = make_float2(-shift, -shift);
+#pragma unroll
+            for (int c = 0; c < kTile; c += 2) {
+              const float2 e = ffma2(make_float2(s[c], s[c + 1]), m2, sh2);
+              s[c] = e.x;
+              s[c + 1] = e.y;
+            }
           } else if constexpr (SCORE == 1) {
-            s[c] = fmaf(s[c], sl2, slope2 * (base + float(c)));
-          } else if constexpr (SCORE == 2) {
-            s[c] = (p.score.softcap * kLog2e) *
-                   tanh_approx(s[c] * (p.score.scale / p.score.softcap));
+            const float b0 = fmaf(slope2, base, -shift);
+#pragma unroll
+            for (int c = 0; c < kTile; ++c) s[c] = fmaf(s[c], sl2, fmaf(slope2, float(c), b0));
           } else {
-            const float y = fmaf(s[c], p.score.scale, slope * (base + float(c)));
-            s[c] = (p.score.softcap * kLog2e) * tanh_approx(y * (1.0f / p.score.softcap));
+            const float b0 = slope * base;
+            const float2 cl = make_float2(cl2, cl2), sh2 = make_float2(-shift, -shift);
+#pragma unroll
+            for (int c = 0; c < kTile; c += 2) {
+              float2 y;
+              if constexpr (SCORE == 2) {
+                y = fmul2(make_float2(s[c], s[c + 1]), make_float2(sc, sc));
+              } else {
+                const float ic = 1.0f / p.score.softcap;
+                y.x = fmaf(s[c], p.score.scale, fmaf(slope, float(c), b0)) * ic;
+                y.y = fmaf(s[c + 1], p.score.scale, fmaf(slope, float(c + 1), b0)) * ic;
+              }
+              const float2 e = ffma2(make_float2(tanh_approx(y.x), tanh_approx(y.y)), cl, sh2);
+              s[c] = e.x;
+              s[c + 1] = e.y;
+            }
           }
-        }
-        if (partial) {  // mask_mod on the tile's pairs
-          const int hi = (p.variant & ATTN_MASK_CAUSAL) ? i - j0 : INT_MAX;
-          const int lo = (p.variant & ATTN_MASK_WINDOW) ? i - j0 - p.mask.window : INT_MIN;
-          const int pre = P == INT_MIN ? INT_MIN : P - j0;
+          if (partial) {  // mask_mod on the tile's pairs
 #pragma unroll
-          for (int c = 0; c < kTile; ++c) {
-            bool keep = (c <= hi) && (c > lo);
-            if (docb) keep = keep && (wdoc[c] == doc_i);
-            keep = keep || (c < pre);
-            s[c] = keep ? s[c] : -INFINITY;
+            for (int c = 0; c < kTile; ++c) {
+              bool keep = (c <= hi) && (c > lo);
+              if (docb) keep = keep && (wdoc[c] == doc_i);
+              keep = keep || (c < pre);
+              s[c] = keep ? s[c] : -INFINITY;
+            }
           }
-        }
-        float mt = s[0];
+        };
+        // s <- 2^s in place; returns the sum (four packed accumulators)
+        auto exponentiate = [&]() -> float {
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-        for (int c = 1; c < kTile; ++c) mt = fmaxf(mt, s[c]);
-        // lazy rescale: move the reference max only when it grows by > 2^8
-        const bool grow = mt > m_ref + kRescaleThreshold;
-        float alpha = 1.0f;
-        if (grow) {
-          alpha = ex2_approx(m_ref - mt);  // m_ref = -inf gives 0
-          l *= alpha;
-        }
-        const bool need_o = grow && j > 0 && m_ref != -INFINITY;
-        if (__any_sync(0xffffffffu, need_o)) {
-          const float a = need_o ? alpha : 1.0f;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(colO + 32 * c, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a);
-            tmem_st32(colO + 32 * c, r);
+          for (int c = 0; c < kTile; c += 2) {
+            s[c] = ex2_approx(s[c]);
+            s[c + 1] = ex2_approx(s[c + 1]);
+            acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
           }
+          const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+          return a.x + a.y;
+        };
+        // Steady state: exponentiate against the current reference max with no
+        // max pass. A tile whose sum is not finite or exceeds 2^64 (the first
+        // tile, or a tile whose scores outgrow the reference) is redone with
+        // its true maximum, rescaling l and O.
+        load_s();
+        transform(m_ref);
+        float tsum = exponentiate();
+        const bool redo = !(tsum <= 18446744073709551616.0f);
+        if (__any_sync(0xffffffffu, redo)) {
+          load_s();
+          transform(0.0f);
+          const float mt = row_max<kTile>(s);
+          const float m_new = redo ? fmaxf(m_ref, mt) : m_ref;
+          const float alpha = ex2_approx(m_ref - m_new);  // m_ref = -inf gives 0
+          const bool need_o = redo && j > 0 && m_ref != -INFINITY && m_new > m_ref;
+          if (redo) l *= (m_new > m_ref ? alpha : 1.0f);
+          if (__any_sync(0xffffffffu, need_o)) {
+            const float a = need_o ? alpha : 1.0f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t r[32];
+              tmem_ld32(colO + 32 * c, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a);
+              tmem_st32(colO + 32 * c, r);
+            }
+          }
+          m_ref = m_new;
+          const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
+#pragma unroll
+          for (int c = 0; c < kTile; ++c) s[c] -= m_use;
+          tsum = exponentiate();
         }
-        if (grow) m_ref = mt;
-        const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
-        float sum = 0.0f;
+        l += tsum;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t r[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float p0 = ex2_approx(s[64 * c + 2 * e] - m_use);
-            const float p1 = ex2_approx(s[64 * c + 2 * e + 1] - m_use);
-            sum += p0 + p1;
-            r[e] = pack_bf16x2(p0, p1);
-          }
+          for (int e = 0; e < 32; ++e) r[e] = pack_bf16x2(s[64 * c + 2 * e], s[64 * c + 2 * e + 1]);
           tmem_st32(colS + 32 * c, r);
         }
-        l += sum;
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(p_full + x);

@@ -123,25 +123,40 @@ __global__ void __launch_bounds__(128) classify_kernel(MaskArgs m, int Sq, int S
   }
 }
 
-// Longest-first order of the B * n_outer list rows: counting sort on the
-// number of visited tiles (full + partial), descending, ties by row index.
+// Longest-first order of the B * n_outer list rows, by the number of visited
+// tiles (full + partial), descending, ties by row index. Each thread ranks its
+// rows against all others (costs staged in shared memory); large inputs that
+// do not fit fall back to one thread's counting sort over global memory.
+constexpr int kOrderSmemRows = 12288;
+
 __global__ void order_kernel(const int* cnt_full, const int* cnt_part, int n_rows, int n_inner,
                              int* order) {
-  extern __shared__ int hist[];  // n_inner + 2 buckets
-  for (int c = threadIdx.x; c < n_inner + 2; c += blockDim.x) hist[c] = 0;
-  __syncthreads();
-  for (int r = threadIdx.x; r < n_rows; r += blockDim.x)
-    atomicAdd(&hist[cnt_full[r] + cnt_part[r]], 1);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int pos = 0;  // exclusive prefix from the largest cost down
-    for (int c = n_inner; c >= 0; --c) {
-      const int n = hist[c];
-      hist[c] = pos;
-      pos += n;
+  extern __shared__ int cost[];
+  if (n_rows <= kOrderSmemRows) {
+    for (int r = threadIdx.x; r < n_rows; r += blockDim.x) cost[r] = cnt_full[r] + cnt_part[r];
+    __syncthreads();
+    for (int r = threadIdx.x; r < n_rows; r += blockDim.x) {
+      const int c = cost[r];
+      int rank = 0;
+      for (int k = 0; k < n_rows; ++k) {
+        const int ck = cost[k];
+        rank += (ck > c) || (ck == c && k < r);
+      }
+      order[rank] = r;
     }
-    for (int r = 0; r < n_rows; ++r) order[hist[cnt_full[r] + cnt_part[r]]++] = r;
+    return;
   }
+  if (threadIdx.x != 0) return;
+  int* hist = cost;  // n_inner + 2 buckets
+  for (int c = 0; c < n_inner + 2; ++c) hist[c] = 0;
+  for (int r = 0; r < n_rows; ++r) ++hist[cnt_full[r] + cnt_part[r]];
+  int pos = 0;
+  for (int c = n_inner; c >= 0; --c) {
+    const int n = hist[c];
+    hist[c] = pos;
+    pos += n;
+  }
+  for (int r = 0; r < n_rows; ++r) order[hist[cnt_full[r] + cnt_part[r]]++] = r;
 }
 
 }  // namespace
@@ -158,13 +173,14 @@ cudaError_t launch_block_mask(const MaskArgs& m, int B, int Sq, int Skv, int tra
                                                   idx_full, idx_part);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t hist_bytes = sizeof(int) * (size_t)(n_inner + 2);
-  if (hist_bytes > 48 * 1024) {
+  const int n_rows = B * n_outer;
+  const size_t smem = sizeof(int) * (size_t)(n_rows <= kOrderSmemRows ? n_rows : n_inner + 2);
+  if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(order_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)hist_bytes);
+                             (int)smem);
     if (e != cudaSuccess) return e;
   }
-  order_kernel<<<1, 256, hist_bytes, stream>>>(cnt_full, cnt_part, B * n_outer, n_inner, order);
+  order_kernel<<<1, 1024, smem, stream>>>(cnt_full, cnt_part, n_rows, n_inner, order);
   return cudaGetLastError();
 }
 
