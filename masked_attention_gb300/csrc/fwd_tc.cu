@@ -122,6 +122,84 @@ __device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp)
   return U;
 }
 
+// Per-row, per-tile constants of the score transform.
+struct TileCtx {
+  float sl2, sc, cl2, slope, slope2, scale, inv_cap;
+  float base;        // j0 - i: (j - i) = base + c
+  int hi, lo, pre;   // mask bounds on the column c (see transform_tile)
+  const int* wdoc;   // document ids of the key tile (shared memory), or nullptr
+  int doc_i;
+};
+
+__device__ __forceinline__ void load_tile(uint32_t col, float (&s)[kTile]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t r[32];
+    tmem_ld32(col + 32 * c, r);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(r[e]);
+  }
+  tmem_ld_wait();
+}
+
+// s <- score_mod(s) in log2 units minus `shift`; masked entries -inf.
+template <int SCORE>
+__device__ __forceinline__ void transform_tile(float (&s)[kTile], const TileCtx& t, float shift,
+                                               bool partial) {
+  if constexpr (SCORE == 0) {
+    const float2 m2 = make_float2(t.sl2, t.sl2), sh2 = make_float2(-shift, -shift);
+#pragma unroll
+    for (int c = 0; c < kTile; c += 2) {
+      const float2 e = ffma2(make_float2(s[c], s[c + 1]), m2, sh2);
+      s[c] = e.x;
+      s[c + 1] = e.y;
+    }
+  } else if constexpr (SCORE == 1) {
+    const float b0 = fmaf(t.slope2, t.base, -shift);
+#pragma unroll
+    for (int c = 0; c < kTile; ++c) s[c] = fmaf(s[c], t.sl2, fmaf(t.slope2, float(c), b0));
+  } else {
+    const float b0 = t.slope * t.base;
+    const float2 cl = make_float2(t.cl2, t.cl2), sh2 = make_float2(-shift, -shift);
+#pragma unroll
+    for (int c = 0; c < kTile; c += 2) {
+      float2 y;
+      if constexpr (SCORE == 2) {
+        y = fmul2(make_float2(s[c], s[c + 1]), make_float2(t.sc, t.sc));
+      } else {
+        y.x = fmaf(s[c], t.scale, fmaf(t.slope, float(c), b0)) * t.inv_cap;
+        y.y = fmaf(s[c + 1], t.scale, fmaf(t.slope, float(c + 1), b0)) * t.inv_cap;
+      }
+      const float2 e = ffma2(make_float2(tanh_approx(y.x), tanh_approx(y.y)), cl, sh2);
+      s[c] = e.x;
+      s[c + 1] = e.y;
+    }
+  }
+  if (partial) {  // mask_mod: keep (c <= hi && c > lo && same document) || c < pre
+#pragma unroll
+    for (int c = 0; c < kTile; ++c) {
+      bool keep = (c <= t.hi) && (c > t.lo);
+      if (t.wdoc) keep = keep && (t.wdoc[c] == t.doc_i);
+      keep = keep || (c < t.pre);
+      s[c] = keep ? s[c] : -INFINITY;
+    }
+  }
+}
+
+// s <- 2^s in place; returns the sum (four packed accumulators).
+__device__ __forceinline__ float exp2_tile(float (&s)[kTile]) {
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                   make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int c = 0; c < kTile; c += 2) {
+    s[c] = ex2_approx(s[c]);
+    s[c + 1] = ex2_approx(s[c + 1]);
+    acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
+  }
+  const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+  return a.x + a.y;
+}
+
 template <int D, int SCORE>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -383,88 +461,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++s_it;
         tc_fence_after();
         float s[kTile];
-        auto load_s = [&]() {
-          uint32_t* r = reinterpret_cast<uint32_t*>(s);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            tmem_ld32(colS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
-          tmem_ld_wait();
-        };
-        const float base = float(j0 - i);  // (j - i) = base + c
-        const int hi = (p.variant & ATTN_MASK_CAUSAL) ? i - j0 : INT_MAX;
-        const int lo = (p.variant & ATTN_MASK_WINDOW) ? i - j0 - p.mask.window : INT_MIN;
-        const int pre = P == INT_MIN ? INT_MIN : P - j0;
-        // s <- score_mod(s) in log2 units minus `shift`, masked entries -inf
-        auto transform = [&](float shift) {
-          if constexpr (SCORE == 0) {
-            const float2 m2 = make_float2(sl2, sl2), sh2 = make_float2(-shift, -shift);
-#pragma unroll
-            for (int c = 0; c < kTile; c += 2) {
-              const float2 e = ffma2(make_float2(s[c], s[c + 1]), m2, sh2);
-              s[c] = e.x;
-              s[c + 1] = e.y;
-            }
-          } else if constexpr (SCORE == 1) {
-            const float b0 = fmaf(slope2, base, -shift);
-#pragma unroll
-            for (int c = 0; c < kTile; ++c) s[c] = fmaf(s[c], sl2, fmaf(slope2, float(c), b0));
-          } else {
-            const float b0 = slope * base;
-            const float2 cl = make_float2(cl2, cl2), sh2 = make_float2(-shift, -shift);
-#pragma unroll
-            for (int c = 0; c < kTile; c += 2) {
-              float2 y;
-              if constexpr (SCORE == 2) {
-                y = fmul2(make_float2(s[c], s[c + 1]), make_float2(sc, sc));
-              } else {
-                const float ic = 1.0f / p.score.softcap;
-                y.x = fmaf(s[c], p.score.scale, fmaf(slope, float(c), b0)) * ic;
-                y.y = fmaf(s[c + 1], p.score.scale, fmaf(slope, float(c + 1), b0)) * ic;
-              }
-              const float2 e = ffma2(make_float2(tanh_approx(y.x), tanh_approx(y.y)), cl, sh2);
-              s[c] = e.x;
-              s[c + 1] = e.y;
-            }
-          }
-          if (partial) {  // mask_mod on the tile's pairs
-#pragma unroll
-            for (int c = 0; c < kTile; ++c) {
-              bool keep = (c <= hi) && (c > lo);
-              if (docb) keep = keep && (wdoc[c] == doc_i);
-              keep = keep || (c < pre);
-              s[c] = keep ? s[c] : -INFINITY;
-            }
-          }
-        };
-        // s <- 2^s in place; returns the sum (four packed accumulators)
-        auto exponentiate = [&]() -> float {
-          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                           make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-          for (int c = 0; c < kTile; c += 2) {
-            s[c] = ex2_approx(s[c]);
-            s[c + 1] = ex2_approx(s[c + 1]);
-            acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
-          }
-          const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
-          return a.x + a.y;
-        };
+        const TileCtx tc{sl2, sc, cl2, slope, slope2, p.score.scale, 1.0f / p.score.softcap,
+                         float(j0 - i), (p.variant & ATTN_MASK_CAUSAL) ? i - j0 : INT_MAX,
+                         (p.variant & ATTN_MASK_WINDOW) ? i - j0 - p.mask.window : INT_MIN,
+                         P == INT_MIN ? INT_MIN : P - j0, docb ? wdoc : nullptr, doc_i};
         // Steady state: exponentiate against the current reference max with no
         // max pass. A tile whose sum is not finite or exceeds 2^64 (the first
         // tile, or a tile whose scores outgrow the reference) is redone with
         // its true maximum, rescaling l and O.
-        load_s();
-        transform(m_ref);
-        float tsum = exponentiate();
+        load_tile(colS, s);
+        transform_tile<SCORE>(s, tc, m_ref, partial);
+        float tsum = exp2_tile(s);
         const bool redo = !(tsum <= 18446744073709551616.0f);
         if (__any_sync(0xffffffffu, redo)) {
-          load_s();
-          transform(0.0f);
+          load_tile(colS, s);
+          transform_tile<SCORE>(s, tc, 0.0f, partial);
           const float mt = row_max<kTile>(s);
           const float m_new = redo ? fmaxf(m_ref, mt) : m_ref;
           const float alpha = ex2_approx(m_ref - m_new);  // m_ref = -inf gives 0
           const bool need_o = redo && j > 0 && m_ref != -INFINITY && m_new > m_ref;
-          if (redo) l *= (m_new > m_ref ? alpha : 1.0f);
+          if (redo && m_new > m_ref) l *= alpha;
           if (__any_sync(0xffffffffu, need_o)) {
             const float a = need_o ? alpha : 1.0f;
 #pragma unroll
@@ -481,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
 #pragma unroll
           for (int c = 0; c < kTile; ++c) s[c] -= m_use;
-          tsum = exponentiate();
+          tsum = exp2_tile(s);
         }
         l += tsum;
 #pragma unroll

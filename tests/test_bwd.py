@@ -2,11 +2,11 @@
 fp64 gradients (FlexAttention page, "Performance": a deterministic backward
 that recomputes intermediates).
 
-Tolerance: bf16 outputs, |g - g_ref| <= max(1e-2, 0.5 ulp_bf16(g_ref) +
-1e-2 |g_ref| / 8). The kernels round P and dS to bf16 before the products
-(relative 2^-9 per term), so a gradient that sums many terms of one sign
-carries an error proportional to its size; 1/8 of 1e-2 relative covers 2^-9
-with margin, and below |g_ref| = 1 the 1e-2 bound of the task applies as is.
+Tolerance: the 1e-2 bound on bf16 outputs applies to the computed value, on
+top of the unavoidable rounding of the output itself to bf16:
+|g - g_ref| <= 1e-2 + 0.5 ulp_bf16(g_ref). (Rounding alone costs half an ulp,
+0.0078 for |g| in [2, 4) and 0.0156 in [4, 8); the products round P and dS to
+bf16, relative 2^-9 per term, which is what the 1e-2 budget covers.)
 """
 import numpy as np
 import pytest
@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 def grad_tol(ref):
     a = np.abs(ref)
     ulp = np.where(a > 0, 2.0 ** (np.floor(np.log2(np.maximum(a, 1e-30))) - 7), 0.0)
-    return np.maximum(1e-2, 0.5 * ulp + 1e-2 * a / 8)
+    return 1e-2 + 0.5 * ulp
 
 
 def run_bwd(w, use_block_mask=True):
