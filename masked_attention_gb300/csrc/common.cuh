@@ -114,11 +114,27 @@ struct Watchdog {
   uint64_t timeout_ns;
 };
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about `hint_ns` nanoseconds pass, instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, const Watchdog& w) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
+  const uint32_t hint = w.timeout_ns < 1000000ull ? (uint32_t)w.timeout_ns : 1000000u;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, hint)) return true;
     if (*w.abort_flag) return false;
     if (global_ns() - t0 > w.timeout_ns) {
       *w.abort_flag = 1;

@@ -268,91 +268,100 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------- producer
-    if (lane == 0) {
-      uint32_t slot_it = 0, q_it = 0;
-      bool ok = true;
-      for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
-        const int u = zigzag_unit(r);
-        if (u >= num_units) continue;
-        const Unit U = decode_unit(p, u, nhp);
-        const int n = U.n();
-        if (n == 0) continue;
-        const bool two = U.h[1] >= 0;
-        const int hk0 = U.h[0] / group, hk1 = two ? U.h[1] / group : hk0;
-        const bool shared = !two || hk0 == hk1;
-        ok = wait_bounded(q_empty, (q_it & 1) ^ 1, wd);
-        if (!ok) break;
+    // The whole warp runs the loop (waits stay converged); lane 0 issues.
+    const bool leader = lane == 0;
+    uint32_t slot_it = 0, q_it = 0;
+    bool ok = true;
+    for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
+      const int u = zigzag_unit(r);
+      if (u >= num_units) continue;
+      const Unit U = decode_unit(p, u, nhp);
+      const int n = U.n();
+      if (n == 0) continue;
+      const bool two = U.h[1] >= 0;
+      const int hk0 = U.h[0] / group, hk1 = two ? U.h[1] / group : hk0;
+      const bool shared = !two || hk0 == hk1;
+      ok = __all_sync(0xffffffffu, wait_bounded(q_empty, (q_it & 1) ^ 1, wd));
+      if (!ok) break;
+      if (leader) {
         mbar_arrive_expect_tx(q_full, (two ? 2 : 1) * C::kTileBytes);
         for (int x = 0; x < (two ? 2 : 1); ++x) {
           const int row = (U.b * p.Hq + U.h[x]) * p.Sq + U.qt * kTile;
           for (int bx = 0; bx < C::kBoxes; ++bx)
             tma_load_2d(sQ + x * C::kTileBytes + bx * C::kBoxBytes, &tm_q, q_full, bx * 64, row);
         }
-        ++q_it;
-        for (int j = 0; j < n && ok; ++j) {
-          const int kt = U.kt(j);
-          const int rows[2] = {(U.b * p.Hkv + hk0) * p.Skv + kt * kTile,
-                               (U.b * p.Hkv + hk1) * p.Skv + kt * kTile};
-          // order: K_A, [K_B], V_A, [V_B]
-          for (int t = 0; t < (shared ? 2 : 4) && ok; ++t) {
-            const int per = shared ? 1 : 2;
-            const bool is_v = t >= per;
-            const int x = shared ? 0 : (t % 2);
-            const int slot = slot_it % C::kSlots;
-            ok = wait_bounded(slot_empty + slot, ((slot_it / C::kSlots) & 1) ^ 1, wd);
-            if (!ok) break;
+      }
+      __syncwarp();
+      ++q_it;
+      for (int j = 0; j < n && ok; ++j) {
+        const int kt = U.kt(j);
+        const int rows[2] = {(U.b * p.Hkv + hk0) * p.Skv + kt * kTile,
+                             (U.b * p.Hkv + hk1) * p.Skv + kt * kTile};
+        // order: K_A, [K_B], V_A, [V_B]
+        for (int t = 0; t < (shared ? 2 : 4) && ok; ++t) {
+          const int per = shared ? 1 : 2;
+          const bool is_v = t >= per;
+          const int x = shared ? 0 : (t % 2);
+          const int slot = slot_it % C::kSlots;
+          ok = __all_sync(0xffffffffu,
+                          wait_bounded(slot_empty + slot, ((slot_it / C::kSlots) & 1) ^ 1, wd));
+          if (!ok) break;
+          if (leader) {
             mbar_arrive_expect_tx(slot_full + slot, C::kTileBytes);
             for (int bx = 0; bx < C::kBoxes; ++bx)
               tma_load_2d(sSlots + slot * C::kTileBytes + bx * C::kBoxBytes, is_v ? &tm_v : &tm_k,
                           slot_full + slot, bx * 64, rows[x]);
-            ++slot_it;
           }
+          __syncwarp();
+          ++slot_it;
         }
       }
-      if (!ok) {  // let copies in flight land before the CTA exits
-        for (uint32_t k = 0; k < C::kSlots && k < slot_it; ++k) {
-          const uint32_t it = slot_it - 1 - k;
-          wait_drain(slot_full + it % C::kSlots, (it / C::kSlots) & 1);
-        }
-        if (q_it > 0) wait_drain(q_full, (q_it - 1) & 1);
+    }
+    if (!ok) {  // let copies in flight land before the CTA exits
+      for (uint32_t k = 0; k < C::kSlots && k < slot_it; ++k) {
+        const uint32_t it = slot_it - 1 - k;
+        wait_drain(slot_full + it % C::kSlots, (it / C::kSlots) & 1);
       }
+      if (q_it > 0) wait_drain(q_full, (q_it - 1) & 1);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false);
-      constexpr uint32_t kIdescPV = idesc_bf16(128, D, true);
-      const uint32_t sQ_addr = smem_u32(sQ);
-      const uint32_t slots_addr = smem_u32(sSlots);
-      uint32_t slot_it = 0, q_it = 0, p_it[2] = {0, 0}, o_it[2] = {0, 0};
-      bool ok = true;
-      for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
-        const int u = zigzag_unit(r);
-        if (u >= num_units) continue;
-        const Unit U = decode_unit(p, u, nhp);
-        const int n = U.n();
-        if (n == 0) continue;
-        const bool two = U.h[1] >= 0;
-        const bool shared = !two || (U.h[0] / group == U.h[1] / group);
-        const int T = shared ? 2 : 4;  // ring slots per key tile
-        ok = wait_bounded(q_full, q_it & 1, wd);
-        if (!ok) break;
-        ++q_it;
-        tc_fence_after();
-        // slot sequence numbers of key tile j for head x
-        auto k_seq = [&](int j, int x) -> uint32_t {
-          return slot_it + j * T + (shared ? 0 : x);
-        };
-        auto v_seq = [&](int j, int x) -> uint32_t {
-          return slot_it + j * T + (shared ? 1 : 2 + x);
-        };
-        auto issue_s = [&](int j, int x) -> bool {
-          const uint32_t seq = k_seq(j, x);
-          const uint32_t slot = seq % C::kSlots;
-          if (x == 0 || !shared) {
-            if (!wait_bounded(slot_full + slot, (seq / C::kSlots) & 1, wd)) return false;
-            tc_fence_after();
-          }
+    // The whole warp runs the loop (waits stay converged); lane 0 issues the
+    // products and the commits.
+    const bool leader = lane == 0;
+    constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false);
+    constexpr uint32_t kIdescPV = idesc_bf16(128, D, true);
+    const uint32_t sQ_addr = smem_u32(sQ);
+    const uint32_t slots_addr = smem_u32(sSlots);
+    uint32_t slot_it = 0, q_it = 0, p_it[2] = {0, 0}, o_it[2] = {0, 0};
+    bool ok = true;
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, wait_bounded(bar, parity, wd));
+    };
+    for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
+      const int u = zigzag_unit(r);
+      if (u >= num_units) continue;
+      const Unit U = decode_unit(p, u, nhp);
+      const int n = U.n();
+      if (n == 0) continue;
+      const bool two = U.h[1] >= 0;
+      const bool shared = !two || (U.h[0] / group == U.h[1] / group);
+      const int T = shared ? 2 : 4;  // ring slots per key tile
+      ok = wait_all(q_full, q_it & 1);
+      if (!ok) break;
+      ++q_it;
+      tc_fence_after();
+      // slot sequence numbers of key tile j for head x
+      auto k_seq = [&](int j, int x) -> uint32_t { return slot_it + j * T + (shared ? 0 : x); };
+      auto v_seq = [&](int j, int x) -> uint32_t { return slot_it + j * T + (shared ? 1 : 2 + x); };
+      auto issue_s = [&](int j, int x) -> bool {
+        const uint32_t seq = k_seq(j, x);
+        const uint32_t slot = seq % C::kSlots;
+        if (x == 0 || !shared) {
+          if (!wait_all(slot_full + slot, (seq / C::kSlots) & 1)) return false;
+          tc_fence_after();
+        }
+        if (leader) {
           const uint32_t a0 = sQ_addr + x * C::kTileBytes;
           const uint32_t b0 = slots_addr + slot * C::kTileBytes;
 #pragma unroll
@@ -363,21 +372,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(s_full + x);
           if (!shared || x == 1 || !two) mma_commit(slot_empty + slot);
-          return true;
-        };
-        auto issue_pv = [&](int j, int x) -> bool {
-          if (!wait_bounded(p_full + x, p_it[x] & 1, wd)) return false;
-          ++p_it[x];
-          if (j == 0) {
-            if (!wait_bounded(o_free + x, (o_it[x] & 1) ^ 1, wd)) return false;
-            ++o_it[x];
-          }
-          const uint32_t seq = v_seq(j, x);
-          const uint32_t slot = seq % C::kSlots;
-          if (x == 0 || !shared) {
-            if (!wait_bounded(slot_full + slot, (seq / C::kSlots) & 1, wd)) return false;
-          }
-          tc_fence_after();
+        }
+        __syncwarp();
+        return true;
+      };
+      auto issue_pv = [&](int j, int x) -> bool {
+        if (!wait_all(p_full + x, p_it[x] & 1)) return false;
+        ++p_it[x];
+        if (j == 0) {
+          if (!wait_all(o_free + x, (o_it[x] & 1) ^ 1)) return false;
+          ++o_it[x];
+        }
+        const uint32_t seq = v_seq(j, x);
+        const uint32_t slot = seq % C::kSlots;
+        if (x == 0 || !shared) {
+          if (!wait_all(slot_full + slot, (seq / C::kSlots) & 1)) return false;
+        }
+        tc_fence_after();
+        if (leader) {
           const uint32_t b0 = slots_addr + slot * C::kTileBytes;
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -386,26 +398,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (j > 0 || kk > 0) ? 1u : 0u);
           }
           if (!shared || x == 1 || !two) mma_commit(slot_empty + slot);
-          return true;
-        };
-        const int nx = two ? 2 : 1;
-        for (int x = 0; x < nx && ok; ++x) ok = issue_s(0, x);
-        if (ok && n == 1) mma_commit(q_empty);
-        for (int j = 0; j < n && ok; ++j) {
-          for (int x = 0; x < nx && ok; ++x) {
-            ok = issue_pv(j, x);
-            if (!ok) break;
-            if (j + 1 < n) ok = issue_s(j + 1, x);
-            else mma_commit(o_done + x);
-          }
-          if (ok && j + 1 == n - 1) mma_commit(q_empty);
         }
-        slot_it += n * T;
+        __syncwarp();
+        return true;
+      };
+      const int nx = two ? 2 : 1;
+      for (int x = 0; x < nx && ok; ++x) ok = issue_s(0, x);
+      if (ok && n == 1 && leader) mma_commit(q_empty);
+      for (int j = 0; j < n && ok; ++j) {
+        for (int x = 0; x < nx && ok; ++x) {
+          ok = issue_pv(j, x);
+          if (!ok) break;
+          if (j + 1 < n) ok = issue_s(j + 1, x);
+          else if (leader) mma_commit(o_done + x);
+        }
+        if (ok && j + 1 == n - 1 && leader) mma_commit(q_empty);
       }
-      // all products issued by this thread are complete before TMEM is freed
-      mma_commit(drain);
-      wait_drain(drain, 0);
+      __syncwarp();
+      slot_it += n * T;
     }
+    // all products issued by this warp are complete before TMEM is freed
+    if (leader) mma_commit(drain);
+    __syncwarp();
+    wait_drain(drain, 0);
   } else if (warp < 8) {
     // ------------------------------------------------------------- softmax
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
