@@ -5,10 +5,12 @@
 // recomputes the probabilities from the forward's LSE and uses no atomics, so
 // reruns are bitwise identical:
 //
-//   delta_kernel   Delta_i = <dO_i, O_i>                              (fp32)
 //   bwd_kernel<dQ> per (b, h, query tile), over its key tiles:
 //                  S = Q K^T, P = exp(score_mod(S) - LSE), dP = dO V^T,
-//                  dS = P (dP - Delta) score_mod', dQ += dS K         (x scale)
+//                  Delta_i = sum_j P dP (exact: it equals <dO_i, O_i> for the
+//                  exact O, which the bf16 output of the forward is not),
+//                  A += (P g dP) K, B += (P g) K, dQ = scale (A - Delta B)
+//                  with g = score_mod'; Delta goes to the workspace.
 //   bwd_kernel<dKV> per (b, kv head, key tile), over the query heads of its
 //                  group and the query tiles of the transposed block mask:
 //                  S^T = K Q^T, P^T, dV += P^T dO, dP^T = V dO^T,
@@ -20,9 +22,9 @@
 //              tiles (plus LSE, Delta and document ids of the dKV stream) into
 //              a ring
 //   warp  5    MMA issuer and TMEM owner
-// Tensor memory: S [0,128), dP [128,256), accumulators from 256. P (bf16) and
-// dS (bf16) overwrite the first 64 columns of S and dP and are the A operands
-// of the TS products.
+// Tensor memory: S [0,128), dP [128,256), accumulators from 256 (dQ: A, B;
+// dKV: dV, dK). The bf16 A operands of the TS products (dQ: P g and P g dP;
+// dKV: P and dS) overwrite the first 64 columns of S and dP.
 #include <cmath>
 #include <mutex>
 
@@ -64,8 +66,9 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
-  const float* delta;
-  BlockLists lists;  // forward lists (dQ) or transposed lists (dKV)
+  const float* delta;  // Delta, read by the dKV kernel
+  float* delta_out;    // Delta, written by the dQ kernel (same buffer)
+  BlockLists lists;    // forward lists (dQ) or transposed lists (dKV)
 };
 
 // One unit of work and its iteration list.
@@ -129,25 +132,6 @@ __device__ __forceinline__ int dense_first(const BwdArgs& a, const BUnit& U) {
   const FwdProblem& p = a.f;
   const bool causal_bound = (p.variant & ATTN_MASK_CAUSAL) && !(p.variant & ATTN_MASK_PREFIX);
   return (!a.lists.full_cnt && MODE == kDKV && causal_bound) ? U.tile : 0;
-}
-
-__global__ void delta_kernel(const __nv_bfloat16* __restrict__ o,
-                             const __nv_bfloat16* __restrict__ dO, float* __restrict__ delta,
-                             size_t rows, int D) {
-  const size_t row = (size_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const __nv_bfloat16* a = o + row * D;
-  const __nv_bfloat16* b = dO + row * D;
-  float acc = 0.0f;
-  for (int d = 2 * lane; d < D; d += 64) {
-    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(a + d));
-    const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(b + d));
-    acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
-  }
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) delta[row] = acc;
 }
 
 template <int D, int SCORE, int MODE>
@@ -219,7 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------- producer
-    if (lane == 0) {
+    {
+      const bool leader = lane == 0;
       uint32_t slot_it = 0, fix_it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
@@ -227,10 +212,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = U.n();
         if (n == 0) continue;
         const int first = dense_first<MODE>(a, U);
-        ok = wait_bounded(fix_empty, (fix_it & 1) ^ 1, wd);
+        ok = __all_sync(0xffffffffu, wait_bounded(fix_empty, (fix_it & 1) ^ 1, wd));
         if (!ok) break;
-        mbar_arrive_expect_tx(fix_full, 2 * C::kTileBytes);
-        {
+        if (leader) {
+          mbar_arrive_expect_tx(fix_full, 2 * C::kTileBytes);
           // dQ: Q and dO rows of (b, h, tile); dKV: K and V rows of (b, hk, tile)
           const int row = MODE == kDQ ? (U.b * p.Hq + U.h) * p.Sq + U.tile * kTile
                                       : (U.b * p.Hkv + U.h) * p.Skv + U.tile * kTile;
@@ -241,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sFix + C::kTileBytes + bx * C::kBoxBytes, m1, fix_full, bx * 64, row);
           }
         }
+        __syncwarp();
         ++fix_it;
         for (int it = 0; it < n && ok; ++it) {
           int hoff, t;
@@ -248,14 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           U.at(it, hoff, t, partial);
           t += first;
           const int slot = slot_it % C::kSlots;
-          ok = wait_bounded(slot_empty + slot, ((slot_it / C::kSlots) & 1) ^ 1, wd);
+          ok = __all_sync(0xffffffffu,
+                          wait_bounded(slot_empty + slot, ((slot_it / C::kSlots) & 1) ^ 1, wd));
           if (!ok) break;
           uint8_t* base = sSlots + slot * C::kSlotBytes;
           uint32_t bytes = 2 * C::kTileBytes;
           if (has_doc) bytes += 512;
           if (MODE == kDKV) bytes += 1024;
-          mbar_arrive_expect_tx(slot_full + slot, bytes);
-          if (MODE == kDQ) {
+          if (leader) mbar_arrive_expect_tx(slot_full + slot, bytes);
+          if (leader && MODE == kDQ) {
             const int row = (U.b * p.Hkv + U.h / group) * p.Skv + t * kTile;
             for (int bx = 0; bx < C::kBoxes; ++bx) {
               tma_load_2d(base + bx * C::kBoxBytes, &tm_k, slot_full + slot, bx * 64, row);
@@ -266,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               bulk_load(base + 2 * C::kTileBytes,
                         p.mask.doc_id + (size_t)U.b * p.mask.doc_len + t * kTile, 512,
                         slot_full + slot);
-          } else {
+          } else if (leader) {
             const int h = U.h * group + hoff;
             const size_t qrow = (size_t)(U.b * p.Hq + h) * p.Sq + t * kTile;
             for (int bx = 0; bx < C::kBoxes; ++bx) {
@@ -281,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_load(base + 2 * C::kTileBytes + 512, p.lse + qrow, 512, slot_full + slot);
             bulk_load(base + 2 * C::kTileBytes + 1024, a.delta + qrow, 512, slot_full + slot);
           }
+          __syncwarp();
           ++slot_it;
         }
       }
@@ -294,7 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {
+      const bool leader = lane == 0;
       constexpr uint32_t kIdescSS = idesc_bf16(128, 128, false);
       constexpr uint32_t kIdescTS = idesc_bf16(128, D, true);
       const uint32_t fix_addr = smem_u32(sFix);
@@ -305,68 +294,87 @@ __global__ void __launch_bounds__(kThreads, 1)
         const BUnit U = decode_bwd<MODE>(a, u);
         const int n = U.n();
         if (n == 0) continue;
-        ok = wait_bounded(fix_full, fix_it & 1, wd);
+        ok = __all_sync(0xffffffffu, wait_bounded(fix_full, fix_it & 1, wd));
         if (!ok) break;
         ++fix_it;
         tc_fence_after();
         for (int it = 0; it < n && ok; ++it) {
           const uint32_t seq = slot_it + it;
           const uint32_t slot = seq % C::kSlots;
-          ok = wait_bounded(slot_full + slot, (seq / C::kSlots) & 1, wd);
+          ok = __all_sync(0xffffffffu, wait_bounded(slot_full + slot, (seq / C::kSlots) & 1, wd));
           if (!ok) break;
           tc_fence_after();
           const uint32_t s0 = slots_addr + slot * C::kSlotBytes;  // K (dQ) or Q (dKV)
           const uint32_t s1 = s0 + C::kTileBytes;                 // V (dQ) or dO (dKV)
           // S = fix0 . slot0^T and dP = fix1 . slot1^T (K-major operands)
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
-            mma_bf16_ss(tmem, sdesc_sw128(fix_addr + off, 16, 1024),
-                        sdesc_sw128(s0 + off, 16, 1024), kIdescSS, kk > 0);
-          }
-          mma_commit(s_full);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
+              mma_bf16_ss(tmem, sdesc_sw128(fix_addr + off, 16, 1024),
+                          sdesc_sw128(s0 + off, 16, 1024), kIdescSS, kk > 0);
+            }
+            mma_commit(s_full);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
-            mma_bf16_ss(tmem + 128, sdesc_sw128(fix_addr + C::kTileBytes + off, 16, 1024),
-                        sdesc_sw128(s1 + off, 16, 1024), kIdescSS, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
+              mma_bf16_ss(tmem + 128, sdesc_sw128(fix_addr + C::kTileBytes + off, 16, 1024),
+                          sdesc_sw128(s1 + off, 16, 1024), kIdescSS, kk > 0);
+            }
+            mma_commit(dp_full);
           }
-          mma_commit(dp_full);
+          __syncwarp();
           if (it == 0) {
-            ok = wait_bounded(acc_free, (acc_it & 1) ^ 1, wd);
+            ok = __all_sync(0xffffffffu, wait_bounded(acc_free, (acc_it & 1) ^ 1, wd));
             if (!ok) break;
           }
           if (MODE == kDKV) {  // dV += P^T dO (B = dO tile, MN-major)
-            ok = wait_bounded(p_full, p_it & 1, wd);
+            ok = __all_sync(0xffffffffu, wait_bounded(p_full, p_it & 1, wd));
             if (!ok) break;
             ++p_it;
             tc_fence_after();
+            if (leader) {
 #pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_bf16_ts(tmem + C::kColAcc, tmem + kk * 8,
-                          sdesc_sw128(s1 + kk * 16 * 128, C::kBoxBytes, 1024), kIdescTS,
-                          (it > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_bf16_ts(tmem + C::kColAcc, tmem + kk * 8,
+                            sdesc_sw128(s1 + kk * 16 * 128, C::kBoxBytes, 1024), kIdescTS,
+                            (it > 0 || kk > 0) ? 1u : 0u);
+            }
+            __syncwarp();
           }
-          ok = wait_bounded(ds_full, ds_it & 1, wd);
+          ok = __all_sync(0xffffffffu, wait_bounded(ds_full, ds_it & 1, wd));
           if (!ok) break;
           ++ds_it;
           tc_fence_after();
-          // dQ += dS K   or   dK += dS^T Q   (B = slot0 tile, MN-major)
-          const uint32_t acc = MODE == kDQ ? C::kColAcc : C::kColAcc + D;
+          // dQ: A += (P g dP) K, B += (P g) K;   dKV: dK += dS^T Q   (B = slot0, MN-major)
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk)
-            mma_bf16_ts(tmem + acc, tmem + 128 + kk * 8,
-                        sdesc_sw128(s0 + kk * 16 * 128, C::kBoxBytes, 1024), kIdescTS,
-                        (it > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(slot_empty + slot);
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              mma_bf16_ts(tmem + C::kColAcc + D, tmem + 128 + kk * 8,
+                          sdesc_sw128(s0 + kk * 16 * 128, C::kBoxBytes, 1024), kIdescTS,
+                          (it > 0 || kk > 0) ? 1u : 0u);
+            if (MODE == kDQ) {
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_bf16_ts(tmem + C::kColAcc, tmem + kk * 8,
+                            sdesc_sw128(s0 + kk * 16 * 128, C::kBoxBytes, 1024), kIdescTS,
+                            (it > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(slot_empty + slot);
+          }
+          __syncwarp();
         }
         if (!ok) break;
         ++acc_it;
-        mma_commit(acc_done);
-        mma_commit(fix_empty);
+        if (leader) {
+          mma_commit(acc_done);
+          mma_commit(fix_empty);
+        }
+        __syncwarp();
         slot_it += n;
       }
-      mma_commit(drain);
+      if (leader) mma_commit(drain);
+      __syncwarp();
       wait_drain(drain, 0);
     }
   } else {
@@ -388,9 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (n == 0) {
         const uint4 z = make_uint4(0, 0, 0, 0);
         if (MODE == kDQ) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) +
-                                                ((size_t)(U.b * p.Hq + U.h) * p.Sq + r) * D);
+          const size_t qrow = (size_t)(U.b * p.Hq + U.h) * p.Sq + r;
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) + qrow * D);
           for (int c = 0; c < D / 8; ++c) dst[c] = z;
+          a.delta_out[qrow] = 0.0f;
         } else {
           const size_t off = ((size_t)(U.b * p.Hkv + U.h) * p.Skv + r) * D;
           uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk) + off);
@@ -407,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t qrow = (size_t)(U.b * p.Hq + U.h) * p.Sq + r;
         const float l = p.lse[qrow];
         row_lse2 = l == -INFINITY ? INFINITY : l * kLog2e;  // empty row: every p is 0
-        row_delta = a.delta[qrow];
+        row_delta = 0.0f;  // accumulated: sum_j P dP
       }
       for (int it = 0; it < n; ++it) {
         int hoff, tt;
@@ -426,8 +435,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ok = __all_sync(0xffffffffu, wait_bounded(s_full, s_it & 1, wd));
         if (!ok) break;
-        tc_fence_after();
         const int c0 = tt * kTile;  // first column position (key for dQ, query for dKV)
+        if constexpr (MODE == kDQ) {
+          // Wait for S and dP; 32 columns at a time: P g -> S columns, P g dP -> dP
+          // columns (bf16, packed below the columns still to be read), Delta += P dP.
+          ok = __all_sync(0xffffffffu, wait_bounded(dp_full, s_it & 1, wd));
+          if (!ok) break;
+          ++s_it;
+          tc_fence_after();
+          const float slope = (SCORE & 1) ? alibi_slope(p.score, h) : 0.0f;
+          int lo = INT_MIN, hi = INT_MAX, pre = INT_MIN;  // row i = r, column j = c0 + c
+          if (partial) {
+            if (p.variant & ATTN_MASK_CAUSAL) hi = r - c0 + 1;
+            if (p.variant & ATTN_MASK_WINDOW) lo = r - c0 - p.mask.window + 1;
+            if (P != INT_MIN) pre = P - c0;
+          }
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            uint32_t rs[32], rp[32];
+            tmem_ld32(colS + 32 * qq, rs);
+            tmem_ld32(colP + 32 * qq, rp);
+            tmem_ld_wait();
+            uint32_t pg_pk[16], pd_pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float pg2[2], pd2[2];
+#pragma unroll
+              for (int z = 0; z < 2; ++z) {
+                const int c = 32 * qq + e + z;
+                float x = __uint_as_float(rs[e + z]) * scale, g = 1.0f;
+                if constexpr ((SCORE & 1) != 0) x = fmaf(slope, float(c0 - r + c), x);
+                if constexpr ((SCORE & 2) != 0) {
+                  const float th = tanh_approx(x * (1.0f / p.score.softcap));
+                  x = p.score.softcap * th;
+                  g = 1.0f - th * th;
+                }
+                float pr = ex2_approx(fmaf(x, kLog2e, -row_lse2));
+                if (partial) {
+                  bool keep = (c >= lo) && (c < hi);
+                  if (docb) keep = keep && (sdoc[c] == my_doc);
+                  keep = keep || (c < pre);
+                  pr = keep ? pr : 0.0f;
+                }
+                const float dp = __uint_as_float(rp[e + z]);
+                row_delta = fmaf(pr, dp, row_delta);
+                pg2[z] = pr * g;
+                pd2[z] = pg2[z] * dp;
+              }
+              pg_pk[e >> 1] = pack_bf16x2(pg2[0], pg2[1]);
+              pd_pk[e >> 1] = pack_bf16x2(pd2[0], pd2[1]);
+            }
+            tmem_st16(colS + 16 * qq, pg_pk);
+            tmem_st16(colP + 16 * qq, pd_pk);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(ds_full);
+          continue;
+        }
+        tc_fence_after();
         float v[kTile];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -541,9 +607,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
       };
-      if (MODE == kDQ) {
-        store_row(colAcc, static_cast<__nv_bfloat16*>(a.dq) + ((size_t)(U.b * p.Hq + U.h) * p.Sq + r) * D,
-                  scale);
+      if (MODE == kDQ) {  // dQ = scale (A - Delta B); Delta to the workspace
+        const size_t qrow = (size_t)(U.b * p.Hq + U.h) * p.Sq + r;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + qrow * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ra[32], rb[32];
+          tmem_ld32(colAcc + D + 32 * c, ra);
+          tmem_ld32(colAcc + 32 * c, rb);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float x0 = scale * fmaf(-row_delta, __uint_as_float(rb[2 * e]), __uint_as_float(ra[2 * e]));
+            const float x1 = scale * fmaf(-row_delta, __uint_as_float(rb[2 * e + 1]), __uint_as_float(ra[2 * e + 1]));
+            pk[e] = pack_bf16x2(x0, x1);
+          }
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+        a.delta_out[qrow] = row_delta;
       } else {
         const size_t off = ((size_t)(U.b * p.Hkv + U.h) * p.Skv + r) * D;
         store_row(colAcc, static_cast<__nv_bfloat16*>(a.dv) + off, 1.0f);
@@ -584,20 +668,14 @@ cudaError_t launch_one(const BwdArgs& a, const CUtensorMap& mq, const CUtensorMa
 template <int D, int SCORE>
 cudaError_t launch_typed(const BwdProblem& bp, cudaStream_t stream) {
   const FwdProblem& f = bp.f;
-  const size_t rows = (size_t)f.B * f.Hq * f.Sq;
-  delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(f.o), static_cast<const __nv_bfloat16*>(bp.dO),
-      bp.delta, rows, D);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv, mdo;
   if (!make_map_bf16(&mq, f.q, (long long)f.B * f.Hq * f.Sq, D) ||
       !make_map_bf16(&mk, f.k, (long long)f.B * f.Hkv * f.Skv, D) ||
       !make_map_bf16(&mv, f.v, (long long)f.B * f.Hkv * f.Skv, D) ||
       !make_map_bf16(&mdo, bp.dO, (long long)f.B * f.Hq * f.Sq, D))
     return cudaErrorInvalidValue;
-  BwdArgs a{f, bp.dO, bp.dq, bp.dk, bp.dv, bp.delta, f.lists};
-  e = launch_one<D, SCORE, kDQ>(a, mq, mk, mv, mdo, f.B * (f.Sq / kTile) * f.Hq, stream);
+  BwdArgs a{f, bp.dO, bp.dq, bp.dk, bp.dv, bp.delta, bp.delta, f.lists};
+  cudaError_t e = launch_one<D, SCORE, kDQ>(a, mq, mk, mv, mdo, f.B * (f.Sq / kTile) * f.Hq, stream);
   if (e != cudaSuccess) return e;
   a.lists = bp.t_lists;
   return launch_one<D, SCORE, kDKV>(a, mq, mk, mv, mdo, f.B * (f.Skv / kTile) * f.Hkv, stream);

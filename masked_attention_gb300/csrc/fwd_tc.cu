@@ -131,38 +131,41 @@ struct TileCtx {
   int doc_i;
 };
 
-__device__ __forceinline__ void load_tile(uint32_t col, float (&s)[kTile]) {
+__device__ __forceinline__ void load_cols(uint32_t col, float* s, int n32) {
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    uint32_t r[32];
-    tmem_ld32(col + 32 * c, r);
+    if (c < n32) {
+      uint32_t r[32];
+      tmem_ld32(col + 32 * c, r);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(r[e]);
+      for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(r[e]);
+    }
   }
   tmem_ld_wait();
 }
 
-// s <- score_mod(s) in log2 units minus `shift`; masked entries -inf.
-template <int SCORE>
-__device__ __forceinline__ void transform_tile(float (&s)[kTile], const TileCtx& t, float shift,
+// s[0..N) <- score_mod(s) in log2 units minus `shift` for the columns
+// c0 .. c0+N-1 of the tile; masked entries -inf.
+template <int SCORE, int N>
+__device__ __forceinline__ void transform_cols(float* s, int c0, const TileCtx& t, float shift,
                                                bool partial) {
   if constexpr (SCORE == 0) {
     const float2 m2 = make_float2(t.sl2, t.sl2), sh2 = make_float2(-shift, -shift);
 #pragma unroll
-    for (int c = 0; c < kTile; c += 2) {
+    for (int c = 0; c < N; c += 2) {
       const float2 e = ffma2(make_float2(s[c], s[c + 1]), m2, sh2);
       s[c] = e.x;
       s[c + 1] = e.y;
     }
   } else if constexpr (SCORE == 1) {
-    const float b0 = fmaf(t.slope2, t.base, -shift);
+    const float b0 = fmaf(t.slope2, t.base + float(c0), -shift);
 #pragma unroll
-    for (int c = 0; c < kTile; ++c) s[c] = fmaf(s[c], t.sl2, fmaf(t.slope2, float(c), b0));
+    for (int c = 0; c < N; ++c) s[c] = fmaf(s[c], t.sl2, fmaf(t.slope2, float(c), b0));
   } else {
-    const float b0 = t.slope * t.base;
+    const float b0 = t.slope * (t.base + float(c0));
     const float2 cl = make_float2(t.cl2, t.cl2), sh2 = make_float2(-shift, -shift);
 #pragma unroll
-    for (int c = 0; c < kTile; c += 2) {
+    for (int c = 0; c < N; c += 2) {
       float2 y;
       if constexpr (SCORE == 2) {
         y = fmul2(make_float2(s[c], s[c + 1]), make_float2(t.sc, t.sc));
@@ -177,24 +180,26 @@ __device__ __forceinline__ void transform_tile(float (&s)[kTile], const TileCtx&
   }
   if (partial) {  // mask_mod: keep (c <= hi && c > lo && same document) || c < pre
 #pragma unroll
-    for (int c = 0; c < kTile; ++c) {
-      bool keep = (c <= t.hi) && (c > t.lo);
-      if (t.wdoc) keep = keep && (t.wdoc[c] == t.doc_i);
-      keep = keep || (c < t.pre);
+    for (int c = 0; c < N; ++c) {
+      const int cc = c0 + c;
+      bool keep = (cc <= t.hi) && (cc > t.lo);
+      if (t.wdoc) keep = keep && (t.wdoc[cc] == t.doc_i);
+      keep = keep || (cc < t.pre);
       s[c] = keep ? s[c] : -INFINITY;
     }
   }
 }
 
-// s <- 2^s in place; returns the sum (four packed accumulators).
-__device__ __forceinline__ float exp2_tile(float (&s)[kTile]) {
+// pk[0..N/2) <- bf16 pairs of 2^s; returns the fp32 sum.
+template <int N>
+__device__ __forceinline__ float exp2_pack(const float* s, uint32_t* pk) {
   float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                    make_float2(0.f, 0.f)};
 #pragma unroll
-  for (int c = 0; c < kTile; c += 2) {
-    s[c] = ex2_approx(s[c]);
-    s[c + 1] = ex2_approx(s[c + 1]);
-    acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
+  for (int c = 0; c < N; c += 2) {
+    const float2 pr = make_float2(ex2_approx(s[c]), ex2_approx(s[c + 1]));
+    acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], pr);
+    pk[c >> 1] = pack_bf16x2(pr.x, pr.y);
   }
   const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
   return a.x + a.y;
@@ -475,23 +480,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++s_it;
         tc_fence_after();
-        float s[kTile];
         const TileCtx tc{sl2, sc, cl2, slope, slope2, p.score.scale, 1.0f / p.score.softcap,
                          float(j0 - i), (p.variant & ATTN_MASK_CAUSAL) ? i - j0 : INT_MAX,
                          (p.variant & ATTN_MASK_WINDOW) ? i - j0 - p.mask.window : INT_MIN,
                          P == INT_MIN ? INT_MIN : P - j0, docb ? wdoc : nullptr, doc_i};
         // Steady state: exponentiate against the current reference max with no
-        // max pass. A tile whose sum is not finite or exceeds 2^64 (the first
-        // tile, or a tile whose scores outgrow the reference) is redone with
+        // max pass, 64 columns at a time, keeping P as packed bf16. A tile whose
+        // sum is not finite or exceeds 2^64 (the first tile, or a tile whose
+        // scores outgrow the reference) is redone from S (still in TMEM) with
         // its true maximum, rescaling l and O.
-        load_tile(colS, s);
-        transform_tile<SCORE>(s, tc, m_ref, partial);
-        float tsum = exp2_tile(s);
+        uint32_t pk[64];
+        float tsum = 0.0f;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          float v[64];
+          load_cols(colS + 64 * hf, v, 2);
+          transform_cols<SCORE, 64>(v, 64 * hf, tc, m_ref, partial);
+          tsum += exp2_pack<64>(v, pk + 32 * hf);
+        }
         const bool redo = !(tsum <= 18446744073709551616.0f);
         if (__any_sync(0xffffffffu, redo)) {
-          load_tile(colS, s);
-          transform_tile<SCORE>(s, tc, 0.0f, partial);
-          const float mt = row_max<kTile>(s);
+          // pass 1: the tile's maximum, 32 columns at a time
+          float mt = -INFINITY;
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq) {
+            float v[32];
+            load_cols(colS + 32 * qq, v, 1);
+            transform_cols<SCORE, 32>(v, 32 * qq, tc, 0.0f, partial);
+            mt = fmaxf(mt, row_max<32>(v));
+          }
           const float m_new = redo ? fmaxf(m_ref, mt) : m_ref;
           const float alpha = ex2_approx(m_ref - m_new);  // m_ref = -inf gives 0
           const bool need_o = redo && j > 0 && m_ref != -INFINITY && m_new > m_ref;
@@ -509,19 +526,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           m_ref = m_new;
+          // pass 2: exponentiate against the new reference
           const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
+          tsum = 0.0f;
 #pragma unroll
-          for (int c = 0; c < kTile; ++c) s[c] -= m_use;
-          tsum = exp2_tile(s);
+          for (int qq = 0; qq < 4; ++qq) {
+            float v[32];
+            load_cols(colS + 32 * qq, v, 1);
+            transform_cols<SCORE, 32>(v, 32 * qq, tc, m_use, partial);
+            tsum += exp2_pack<32>(v, pk + 16 * qq);
+          }
         }
         l += tsum;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t r[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = pack_bf16x2(s[64 * c + 2 * e], s[64 * c + 2 * e + 1]);
-          tmem_st32(colS + 32 * c, r);
-        }
+        tmem_st32(colS, *reinterpret_cast<uint32_t(*)[32]>(pk));
+        tmem_st32(colS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(p_full + x);
