@@ -124,7 +124,14 @@ typedef struct attn_params {
                                         visited with the mask evaluated per element */
   int* status;                 /* device int32 status word, or NULL for the library's own */
   unsigned long long timeout_ns; /* limit of each device-side wait; 0 = 4 s */
+  unsigned fault_inject;       /* 0 in normal use. ATTN_FAULT_NO_LOADS: the tensor-core
+                                  kernels' load warp issues no copy, so every wait for data
+                                  runs out after timeout_ns and the call reports
+                                  ATTN_ERR_TIMEOUT (tests the bounded-wait path; no GPU
+                                  fault is involved) */
 } attn_params;
+
+#define ATTN_FAULT_NO_LOADS 1u
 
 /* Forward: O = softmax(score_mod(scale*QK^T) under the mask) V and LSE.
  *   q [B,Hq,Sq,D], k and v [B,Hkv,Skv,D], o [B,Hq,Sq,D] (dtype p->dtype),

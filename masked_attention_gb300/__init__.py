@@ -31,6 +31,7 @@ MASK_CAUSAL, MASK_WINDOW, MASK_DOCUMENT, MASK_PREFIX = 1 << 0, 1 << 1, 1 << 2, 1
 SCORE_ALIBI, SCORE_SOFTCAP = 1 << 8, 1 << 9
 BF16, F32 = 0, 1
 TILE = 128
+FAULT_NO_LOADS = 1
 
 
 class attn_block_mask(ctypes.Structure):
@@ -50,7 +51,7 @@ class attn_params(ctypes.Structure):
                 ("softcap", ctypes.c_float), ("alibi_slopes", ctypes.c_void_p),
                 ("doc_id", ctypes.c_void_p), ("prefix_len", ctypes.c_void_p),
                 ("block_mask", ctypes.POINTER(attn_block_mask)), ("status", ctypes.c_void_p),
-                ("timeout_ns", ctypes.c_ulonglong)]
+                ("timeout_ns", ctypes.c_ulonglong), ("fault_inject", ctypes.c_uint)]
 
 
 _lib = None
@@ -161,7 +162,8 @@ class BlockMask:
 
 
 def _params(dtype: int, scale: float, window: int, softcap: float, alibi_slopes, doc_id,
-            prefix_len, block_mask: Optional[BlockMask], status, timeout_ns: int) -> attn_params:
+            prefix_len, block_mask: Optional[BlockMask], status, timeout_ns: int,
+            fault_inject: int = 0) -> attn_params:
     p = attn_params()
     p.dtype = dtype
     p.scale = scale
@@ -173,6 +175,7 @@ def _params(dtype: int, scale: float, window: int, softcap: float, alibi_slopes,
     p.block_mask = ctypes.pointer(block_mask.struct) if block_mask is not None else None
     p.status = _ptr(status)
     p.timeout_ns = timeout_ns
+    p.fault_inject = fault_inject
     return p
 
 
@@ -206,7 +209,7 @@ def attn_fwd(q, k, v, o, lse, variant: int = 0, *, B=None, Hq=None, Hkv=None, Sq
              Skv=None, D=None, dtype: Optional[int] = None, scale: float = 0.0, window: int = 0,
              softcap: float = 0.0, alibi_slopes=None, doc_id=None, prefix_len=None,
              block_mask: Optional[BlockMask] = None, status=None, timeout_ns: int = 0,
-             stream=None) -> None:
+             fault_inject: int = 0, stream=None) -> None:
     """O and LSE of masked attention; writes ``o`` and ``lse`` in place.
 
     ``q`` [B,Hq,Sq,D], ``k``/``v`` [B,Hkv,Skv,D], ``o`` like ``q``, ``lse`` fp32
@@ -219,7 +222,7 @@ def attn_fwd(q, k, v, o, lse, variant: int = 0, *, B=None, Hq=None, Hkv=None, Sq
         import torch
         dtype = F32 if q.dtype == torch.float32 else BF16
     p = _params(dtype, scale, window, softcap, alibi_slopes, doc_id, prefix_len, block_mask,
-                status, timeout_ns)
+                status, timeout_ns, fault_inject)
     st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
                         variant, ctypes.byref(p), _stream(stream))
     _check(st, "attn_fwd")
@@ -228,7 +231,7 @@ def attn_fwd(q, k, v, o, lse, variant: int = 0, *, B=None, Hq=None, Hkv=None, Sq
 def attn_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, variant: int = 0, *,
              scale: float = 0.0, window: int = 0, softcap: float = 0.0, alibi_slopes=None,
              doc_id=None, prefix_len=None, block_mask: Optional[BlockMask] = None, status=None,
-             timeout_ns: int = 0, stream=None) -> None:
+             timeout_ns: int = 0, fault_inject: int = 0, stream=None) -> None:
     """dQ, dK, dV of ``sum(dO * O)``; writes ``dq``, ``dk``, ``dv`` in place.
     ``workspace``: a CUDA tensor of at least ``attn_bwd_workspace_bytes`` bytes."""
     import torch
@@ -236,7 +239,7 @@ def attn_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, variant: int = 0, *,
     Hkv, Skv = k.shape[1], k.shape[2]
     dtype = F32 if q.dtype == torch.float32 else BF16
     p = _params(dtype, scale, window, softcap, alibi_slopes, doc_id, prefix_len, block_mask,
-                status, timeout_ns)
+                status, timeout_ns, fault_inject)
     ws_bytes = workspace.numel() * workspace.element_size()
     st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
                         _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, B, Hq, Hkv, Sq, Skv, D,

@@ -153,6 +153,7 @@ attn_status fill_problem(FwdProblem& f, const void* q, const void* k, const void
   }
   f.status = p->status;  // resolved by resolve_status() once every check has passed
   f.timeout_ns = p->timeout_ns ? p->timeout_ns : 4000000000ull;
+  f.fault_inject = p->fault_inject;
   return ATTN_OK;
 }
 

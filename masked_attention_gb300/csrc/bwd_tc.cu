@@ -5,12 +5,16 @@
 // recomputes the probabilities from the forward's LSE and uses no atomics, so
 // reruns are bitwise identical:
 //
+//   delta_kernel   an estimate Dhat_i = <dO_i, O_i> from the bf16 output O
 //   bwd_kernel<dQ> per (b, h, query tile), over its key tiles:
-//                  S = Q K^T, P = exp(score_mod(S) - LSE), dP = dO V^T,
-//                  Delta_i = sum_j P dP (exact: it equals <dO_i, O_i> for the
-//                  exact O, which the bf16 output of the forward is not),
-//                  A += (P g dP) K, B += (P g) K, dQ = scale (A - Delta B)
-//                  with g = score_mod'; Delta goes to the workspace.
+//                  S = Q K^T, P = exp(score_mod(S) - LSE), dP = dO V^T, and
+//                  the exact Delta_i = sum_j P dP (it equals <dO_i, O_i> for
+//                  the exact O; the bf16 O is off by up to an ulp, which on
+//                  rows with few keys moves dQ by ~1e-2), accumulated on the fly:
+//                  A += bf16(P g (dP - Dhat)) K, B += bf16(P g) K,
+//                  dQ = scale (A - (Delta - Dhat) B), g = score_mod'.
+//                  A carries the well-conditioned bulk (like dS itself), the
+//                  correction term is small. Delta goes to the workspace.
 //   bwd_kernel<dKV> per (b, kv head, key tile), over the query heads of its
 //                  group and the query tiles of the transposed block mask:
 //                  S^T = K Q^T, P^T, dV += P^T dO, dP^T = V dO^T,
@@ -134,6 +138,25 @@ __device__ __forceinline__ int dense_first(const BwdArgs& a, const BUnit& U) {
   return (!a.lists.full_cnt && MODE == kDKV && causal_bound) ? U.tile : 0;
 }
 
+__global__ void delta_kernel(const __nv_bfloat16* __restrict__ o,
+                             const __nv_bfloat16* __restrict__ dO, float* __restrict__ delta,
+                             size_t rows, int D) {
+  const size_t row = (size_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const __nv_bfloat16* a = o + row * D;
+  const __nv_bfloat16* b = dO + row * D;
+  float acc = 0.0f;
+  for (int d = 2 * lane; d < D; d += 64) {
+    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(a + d));
+    const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(b + d));
+    acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+  }
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (lane == 0) delta[row] = acc;
+}
+
 template <int D, int SCORE, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -204,7 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------- producer
     {
-      const bool leader = lane == 0;
+      // With ATTN_FAULT_NO_LOADS nothing is issued and the consumers' waits run out.
+      const bool leader = lane == 0 && !(p.fault_inject & ATTN_FAULT_NO_LOADS);
       uint32_t slot_it = 0, fix_it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
@@ -411,12 +435,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int* docb = has_doc ? p.mask.doc_id + (size_t)U.b * p.mask.doc_len : nullptr;
       const int my_doc = docb ? docb[r] : 0;
       const int P = (p.variant & ATTN_MASK_PREFIX) ? p.mask.prefix_len[U.b] : INT_MIN;
-      float row_lse2 = 0.0f, row_delta = 0.0f;
+      float row_lse2 = 0.0f, row_delta = 0.0f, row_dhat = 0.0f;
       if (MODE == kDQ) {
         const size_t qrow = (size_t)(U.b * p.Hq + U.h) * p.Sq + r;
         const float l = p.lse[qrow];
         row_lse2 = l == -INFINITY ? INFINITY : l * kLog2e;  // empty row: every p is 0
-        row_delta = 0.0f;  // accumulated: sum_j P dP
+        row_dhat = a.delta[qrow];  // estimate from the bf16 O (delta_kernel)
+        row_delta = 0.0f;          // exact: sum_j P dP, accumulated below
       }
       for (int it = 0; it < n; ++it) {
         int hoff, tt;
@@ -480,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float dp = __uint_as_float(rp[e + z]);
                 row_delta = fmaf(pr, dp, row_delta);
                 pg2[z] = pr * g;
-                pd2[z] = pg2[z] * dp;
+                pd2[z] = pg2[z] * (dp - row_dhat);
               }
               pg_pk[e >> 1] = pack_bf16x2(pg2[0], pg2[1]);
               pd_pk[e >> 1] = pack_bf16x2(pd2[0], pd2[1]);
@@ -607,9 +632,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
       };
-      if (MODE == kDQ) {  // dQ = scale (A - Delta B); Delta to the workspace
+      if (MODE == kDQ) {  // dQ = scale (A - (Delta - Dhat) B); Delta to the workspace
         const size_t qrow = (size_t)(U.b * p.Hq + U.h) * p.Sq + r;
         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + qrow * D;
+        const float corr = row_delta - row_dhat;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ra[32], rb[32];
@@ -619,8 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float x0 = scale * fmaf(-row_delta, __uint_as_float(rb[2 * e]), __uint_as_float(ra[2 * e]));
-            const float x1 = scale * fmaf(-row_delta, __uint_as_float(rb[2 * e + 1]), __uint_as_float(ra[2 * e + 1]));
+            const float x0 = scale * fmaf(-corr, __uint_as_float(rb[2 * e]), __uint_as_float(ra[2 * e]));
+            const float x1 = scale * fmaf(-corr, __uint_as_float(rb[2 * e + 1]), __uint_as_float(ra[2 * e + 1]));
             pk[e] = pack_bf16x2(x0, x1);
           }
           uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
@@ -668,6 +694,12 @@ cudaError_t launch_one(const BwdArgs& a, const CUtensorMap& mq, const CUtensorMa
 template <int D, int SCORE>
 cudaError_t launch_typed(const BwdProblem& bp, cudaStream_t stream) {
   const FwdProblem& f = bp.f;
+  const size_t rows = (size_t)f.B * f.Hq * f.Sq;
+  delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(f.o), static_cast<const __nv_bfloat16*>(bp.dO),
+      bp.delta, rows, D);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv, mdo;
   if (!make_map_bf16(&mq, f.q, (long long)f.B * f.Hq * f.Sq, D) ||
       !make_map_bf16(&mk, f.k, (long long)f.B * f.Hkv * f.Skv, D) ||
@@ -675,7 +707,7 @@ cudaError_t launch_typed(const BwdProblem& bp, cudaStream_t stream) {
       !make_map_bf16(&mdo, bp.dO, (long long)f.B * f.Hq * f.Sq, D))
     return cudaErrorInvalidValue;
   BwdArgs a{f, bp.dO, bp.dq, bp.dk, bp.dv, bp.delta, bp.delta, f.lists};
-  cudaError_t e = launch_one<D, SCORE, kDQ>(a, mq, mk, mv, mdo, f.B * (f.Sq / kTile) * f.Hq, stream);
+  e = launch_one<D, SCORE, kDQ>(a, mq, mk, mv, mdo, f.B * (f.Sq / kTile) * f.Hq, stream);
   if (e != cudaSuccess) return e;
   a.lists = bp.t_lists;
   return launch_one<D, SCORE, kDKV>(a, mq, mk, mv, mdo, f.B * (f.Skv / kTile) * f.Hkv, stream);

@@ -274,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------- producer
     // The whole warp runs the loop (waits stay converged); lane 0 issues.
-    const bool leader = lane == 0;
+    // With ATTN_FAULT_NO_LOADS nothing is issued and the consumers' waits run out.
+    const bool leader = lane == 0 && !(p.fault_inject & ATTN_FAULT_NO_LOADS);
     uint32_t slot_it = 0, q_it = 0;
     bool ok = true;
     for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {

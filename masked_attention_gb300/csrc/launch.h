@@ -21,6 +21,7 @@ struct FwdProblem {
   BlockLists lists;  // lists.full_cnt == nullptr: visit every tile the causal bound allows
   int* status;
   uint64_t timeout_ns;
+  unsigned fault_inject;  // ATTN_FAULT_NO_LOADS: the load warp issues nothing
 };
 
 struct BwdProblem {

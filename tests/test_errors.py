@@ -2,10 +2,11 @@
 ATTN_ERR_TIMEOUT through the status word and leave the context usable; a
 block mask that does not match the call is rejected before launching.
 
-The timeout is provoked honestly: a wait limit of 1 microsecond is shorter
-than the first TMA load, so a real wait runs out; nothing is corrupted and no
-fault is raised. The kernel then drains its copies and products in flight,
-frees its tensor memory and returns.
+The timeout is provoked on the host's request: with ATTN_FAULT_NO_LOADS the
+load warp issues no copy, so the other warps wait for data that never comes
+and their bounded waits run out (a 20 ms limit here). No GPU fault is raised:
+the kernel drains, frees its tensor memory and returns, and the status word
+reports ATTN_ERR_TIMEOUT.
 """
 import numpy as np
 import pytest
@@ -31,7 +32,7 @@ def test_forward_timeout_reports_status_and_recovers():
     o = torch.empty_like(g.q)
     lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device="cuda")
     M.attn_fwd(g.q, g.k, g.v, o, lse, g.variant, block_mask=g.bm, status=status,
-               timeout_ns=1000)
+               timeout_ns=20_000_000, fault_inject=M.FAULT_NO_LOADS)
     assert M.attn_check_status(status) == M.ATTN_ERR_TIMEOUT
     assert int(status.item()) == 0  # attn_check_status clears it
     # the context still works: a normal call afterwards is correct
@@ -54,7 +55,7 @@ def test_backward_timeout_reports_status_and_recovers():
                      device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     M.attn_bwd(g.q, g.k, g.v, O, L, g.do, dq, dk, dv, ws, g.variant, block_mask=g.bm,
-               status=status, timeout_ns=1000)
+               status=status, timeout_ns=20_000_000, fault_inject=M.FAULT_NO_LOADS)
     assert M.attn_check_status(status) == M.ATTN_ERR_TIMEOUT
     M.attn_bwd(g.q, g.k, g.v, O, L, g.do, dq, dk, dv, ws, g.variant, block_mask=g.bm)
     assert M.attn_check_status() == M.ATTN_OK
