@@ -8,7 +8,7 @@
 #include <cuda_bf16.h>
 #include <cuda.h>
 
-#include "../../include/mattn.h"
+#include "mattn.h"  // include/ is on the include path
 
 namespace mattn {
 

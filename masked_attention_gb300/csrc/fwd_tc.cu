@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (!ok) {  // let copies in flight land before the CTA exits
+    if (!ok && !(p.fault_inject & ATTN_FAULT_NO_LOADS)) {  // let copies in flight land
       for (uint32_t k = 0; k < C::kSlots && k < slot_it; ++k) {
         const uint32_t it = slot_it - 1 - k;
         wait_drain(slot_full + it % C::kSlots, (it / C::kSlots) & 1);
