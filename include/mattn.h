@@ -176,6 +176,24 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      int B, int Hq, int Hkv, int Sq, int Skv, int D,
                      unsigned variant, const attn_params* p, struct CUstream_st* stream);
 
+/* attn_bwd for callers that cannot allocate device memory. The page this
+ * library follows has no counterpart: it exists for code that is handed its
+ * tensors but has no way to obtain a workspace (a framework that owns every
+ * device allocation and forbids raw cudaMalloc, a plug-in without an
+ * allocator). Same arguments and results as attn_bwd without `workspace`:
+ * the Delta row terms live in a fixed array inside the library (8 MiB per
+ * GPU that loads it, held until the process exits), so B*Hq*Sq may be at most
+ * 2,097,152; larger problems return ATTN_ERR_WORKSPACE_TOO_SMALL before
+ * anything runs. No cudaMalloc, cudaFree or other allocating call is made.
+ * The first call on a device looks up the array's device address (make it
+ * before any stream capture). Every call shares the array, which keeps the
+ * last call's contents (none needs to start at zero); calls that overlap on
+ * the GPU race on it. */
+attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                             int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                             unsigned variant, const attn_params* p, struct CUstream_st* stream);
+
 /* Synchronises `stream`, reads the device status word (`status_dev`, or the
  * library's own when NULL), resets it to 0 and returns it as an attn_status. */
 attn_status attn_check_status(int* status_dev, struct CUstream_st* stream);

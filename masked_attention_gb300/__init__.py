@@ -18,7 +18,7 @@ from typing import Optional
 __all__ = [
     "MASK_CAUSAL", "MASK_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX", "SCORE_ALIBI",
     "SCORE_SOFTCAP", "BF16", "F32", "AttnError", "BlockMask", "attn_fwd", "attn_bwd",
-    "build_block_mask", "attn_block_mask_bytes", "attn_bwd_workspace_bytes",
+    "build_block_mask", "attn_block_mask_bytes", "attn_bwd_workspace_bytes", "attn_bwd_noalloc",
     "attn_check_status", "attn_status_str", "lib", "LIB_PATH",
 ]
 
@@ -79,6 +79,9 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, u, P,
                                vp]
         L.attn_bwd.restype = i
+        L.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, u,
+                                       P, vp]
+        L.attn_bwd_noalloc.restype = i
         L.attn_check_status.argtypes = [vp, vp]
         L.attn_check_status.restype = i
         L.attn_status_str.argtypes = [i]
@@ -245,6 +248,26 @@ def attn_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, variant: int = 0, *,
                         _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, B, Hq, Hkv, Sq, Skv, D,
                         variant, ctypes.byref(p), _stream(stream))
     _check(st, "attn_bwd")
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, variant: int = 0, *,
+                     scale: float = 0.0, window: int = 0, softcap: float = 0.0,
+                     alibi_slopes=None, doc_id=None, prefix_len=None,
+                     block_mask: Optional[BlockMask] = None, status=None, timeout_ns: int = 0,
+                     stream=None) -> None:
+    """attn_bwd without a workspace argument, for callers that cannot allocate
+    device memory: the library's own fixed array holds the row terms (at most
+    B*Hq*Sq = 2,097,152; see include/mattn.h). Writes dq, dk, dv in place."""
+    import torch
+    B, Hq, Sq, D = q.shape
+    Hkv, Skv = k.shape[1], k.shape[2]
+    dtype = F32 if q.dtype == torch.float32 else BF16
+    p = _params(dtype, scale, window, softcap, alibi_slopes, doc_id, prefix_len, block_mask,
+                status, timeout_ns)
+    st = lib().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Skv, D, variant,
+                                ctypes.byref(p), _stream(stream))
+    _check(st, "attn_bwd_noalloc")
 
 
 def attn_check_status(status=None, stream=None) -> int:
