@@ -36,8 +36,8 @@ namespace mattn {
 namespace {
 
 constexpr int kThreads = 384;
-constexpr int kRegsSoftmax = 224;  // 2 x 128 x 224 + 128 x 56 = 64512 = 384 x 168
-constexpr int kRegsOther = 56;
+constexpr int kRegsSoftmax = 208;  // 2 x 128 x 208 + 128 x 88 = 64512 = 384 x 168
+constexpr int kRegsOther = 88;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
@@ -130,6 +130,34 @@ struct TileCtx {
   const int* wdoc;   // document ids of the key tile (shared memory), or nullptr
   int doc_i;
 };
+
+// Whole-warp bounded wait (every lane polls; the result is the same for all).
+__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
+  return __all_sync(0xffffffffu, wait_bounded(bar, parity, wd));
+}
+
+// S = Q K^T over D (K-major operands, 128-byte swizzle): K-step kk advances
+// 32 bytes inside a 64-column box and moves to the next box every 4 steps.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = (uint64_t)(((kk / 4) * kTile * 128 + (kk % 4) * 32) >> 4);
+    mma_bf16_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0);
+  }
+}
+
+// O += P V: P (bf16, 8 TMEM columns per 16 keys) times V (MN-major); K-step kk
+// advances 16 key rows = 2048 bytes.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t b_desc,
+                                         uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk)
+    mma_bf16_ts(d_tmem, p_tmem + kk * 8, b_desc + (uint64_t)((kk * 16 * 128) >> 4), idesc,
+                (accumulate || kk > 0) ? 1u : 0u);
+}
 
 __device__ __forceinline__ void load_cols(uint32_t col, float* s, int n32) {
 #pragma unroll
@@ -333,90 +361,90 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop (waits stay converged); lane 0 issues the
-    // products and the commits.
+    // products and the commits. Loop state stays in registers and the
+    // shared-memory descriptors are precomputed: the start-address field is
+    // in 16-byte units, so an offset is added as (bytes >> 4).
     const bool leader = lane == 0;
     constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false);
     constexpr uint32_t kIdescPV = idesc_bf16(128, D, true);
-    const uint32_t sQ_addr = smem_u32(sQ);
-    const uint32_t slots_addr = smem_u32(sSlots);
-    uint32_t slot_it = 0, q_it = 0, p_it[2] = {0, 0}, o_it[2] = {0, 0};
+    const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t dK0 = sdesc_sw128(smem_u32(sSlots), 16, 1024);
+    const uint64_t dV0 = sdesc_sw128(smem_u32(sSlots), C::kBoxBytes, 1024);
+    uint32_t slot_it = 0, q_it = 0, p_it0 = 0, p_it1 = 0, o_it0 = 0, o_it1 = 0;
     bool ok = true;
-    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, wait_bounded(bar, parity, wd));
-    };
     for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
       const int u = zigzag_unit(r);
       if (u >= num_units) continue;
       const Unit U = decode_unit(p, u, nhp);
       const int n = U.n();
       if (n == 0) continue;
-      const bool two = U.h[1] >= 0;
-      const bool shared = !two || (U.h[0] / group == U.h[1] / group);
-      const int T = shared ? 2 : 4;  // ring slots per key tile
-      ok = wait_all(q_full, q_it & 1);
+      const int nx = U.h[1] >= 0 ? 2 : 1;
+      const bool shared = nx == 1 || (U.h[0] / group == U.h[1] / group);
+      const uint32_t T = shared ? 2u : 4u;  // ring slots per key tile
+      ok = wait_warp(q_full, q_it & 1, wd);
       if (!ok) break;
       ++q_it;
       tc_fence_after();
-      // slot sequence numbers of key tile j for head x
-      auto k_seq = [&](int j, int x) -> uint32_t { return slot_it + j * T + (shared ? 0 : x); };
-      auto v_seq = [&](int j, int x) -> uint32_t { return slot_it + j * T + (shared ? 1 : 2 + x); };
-      auto issue_s = [&](int j, int x) -> bool {
-        const uint32_t seq = k_seq(j, x);
+      // S_x(0) for both heads
+      for (int x = 0; x < nx && ok; ++x) {
+        const uint32_t seq = slot_it + (shared ? 0u : (uint32_t)x);
         const uint32_t slot = seq % C::kSlots;
         if (x == 0 || !shared) {
-          if (!wait_all(slot_full + slot, (seq / C::kSlots) & 1)) return false;
+          ok = wait_warp(slot_full + slot, (seq / C::kSlots) & 1, wd);
+          if (!ok) break;
           tc_fence_after();
         }
         if (leader) {
-          const uint32_t a0 = sQ_addr + x * C::kTileBytes;
-          const uint32_t b0 = slots_addr + slot * C::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
-            mma_bf16_ss(tmem + 128u * x, sdesc_sw128(a0 + off, 16, 1024),
-                        sdesc_sw128(b0 + off, 16, 1024), kIdescQK, kk > 0);
-          }
+          issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
+                      dK0 + ((slot * C::kTileBytes) >> 4), kIdescQK);
           mma_commit(s_full + x);
-          if (!shared || x == 1 || !two) mma_commit(slot_empty + slot);
+          if (!shared || x == nx - 1) mma_commit(slot_empty + slot);
         }
         __syncwarp();
-        return true;
-      };
-      auto issue_pv = [&](int j, int x) -> bool {
-        if (!wait_all(p_full + x, p_it[x] & 1)) return false;
-        ++p_it[x];
-        if (j == 0) {
-          if (!wait_all(o_free + x, (o_it[x] & 1) ^ 1)) return false;
-          ++o_it[x];
-        }
-        const uint32_t seq = v_seq(j, x);
-        const uint32_t slot = seq % C::kSlots;
-        if (x == 0 || !shared) {
-          if (!wait_all(slot_full + slot, (seq / C::kSlots) & 1)) return false;
-        }
-        tc_fence_after();
-        if (leader) {
-          const uint32_t b0 = slots_addr + slot * C::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            mma_bf16_ts(tmem + C::kColO0 + D * x, tmem + 128u * x + kk * 8,
-                        sdesc_sw128(b0 + kk * 16 * 128, C::kBoxBytes, 1024), kIdescPV,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          if (!shared || x == 1 || !two) mma_commit(slot_empty + slot);
-        }
-        __syncwarp();
-        return true;
-      };
-      const int nx = two ? 2 : 1;
-      for (int x = 0; x < nx && ok; ++x) ok = issue_s(0, x);
+      }
       if (ok && n == 1 && leader) mma_commit(q_empty);
       for (int j = 0; j < n && ok; ++j) {
         for (int x = 0; x < nx && ok; ++x) {
-          ok = issue_pv(j, x);
+          // O_x += P_x V_j
+          ok = wait_warp(p_full + x, (x ? p_it1 : p_it0) & 1, wd);
           if (!ok) break;
-          if (j + 1 < n) ok = issue_s(j + 1, x);
-          else if (leader) mma_commit(o_done + x);
+          if (x) ++p_it1; else ++p_it0;
+          if (j == 0) {
+            ok = wait_warp(o_free + x, ((x ? o_it1 : o_it0) & 1) ^ 1, wd);
+            if (!ok) break;
+            if (x) ++o_it1; else ++o_it0;
+          }
+          const uint32_t vseq = slot_it + j * T + (shared ? 1u : 2u + x);
+          const uint32_t vslot = vseq % C::kSlots;
+          if (x == 0 || !shared) {
+            ok = wait_warp(slot_full + vslot, (vseq / C::kSlots) & 1, wd);
+            if (!ok) break;
+          }
+          tc_fence_after();
+          if (leader) {
+            issue_pv<D>(tmem + C::kColO0 + D * x, tmem + 128u * x,
+                        dV0 + ((vslot * C::kTileBytes) >> 4), kIdescPV, j > 0);
+            if (!shared || x == nx - 1) mma_commit(slot_empty + vslot);
+          }
+          __syncwarp();
+          if (j + 1 < n) {  // S_x(j+1)
+            const uint32_t kseq = slot_it + (j + 1) * T + (shared ? 0u : (uint32_t)x);
+            const uint32_t kslot = kseq % C::kSlots;
+            if (x == 0 || !shared) {
+              ok = wait_warp(slot_full + kslot, (kseq / C::kSlots) & 1, wd);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            if (leader) {
+              issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
+                          dK0 + ((kslot * C::kTileBytes) >> 4), kIdescQK);
+              mma_commit(s_full + x);
+              if (!shared || x == nx - 1) mma_commit(slot_empty + kslot);
+            }
+            __syncwarp();
+          } else if (leader) {
+            mma_commit(o_done + x);
+          }
         }
         if (ok && j + 1 == n - 1 && leader) mma_commit(q_empty);
       }
