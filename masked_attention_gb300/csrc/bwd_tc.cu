@@ -480,7 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t rs[32], rp[32];
             tmem_ld32(colS + 32 * qq, rs);
             tmem_ld32(colP + 32 * qq, rp);
-            tmem_ld_wait();
+            tmem_ld_wait_regs(rs);
+            tmem_ld_wait_regs(rp);
             uint32_t pg_pk[16], pd_pk[16];
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
@@ -524,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) {
           uint32_t rr[32];
           tmem_ld32(colS + 32 * c, rr);
-          tmem_ld_wait();
+          tmem_ld_wait_regs(rr);
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[32 * c + e] = __uint_as_float(rr[e]);
         }
@@ -591,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 4; ++c) {
           uint32_t rr[32];
           tmem_ld32(colP + 32 * c, rr);
-          tmem_ld_wait();
+          tmem_ld_wait_regs(rr);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const int cc = 32 * c + e;
@@ -622,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < D / 32; ++c) {
           uint32_t rr[32];
           tmem_ld32(col + 32 * c, rr);
-          tmem_ld_wait();
+          tmem_ld_wait_regs(rr);
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
@@ -641,7 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t ra[32], rb[32];
           tmem_ld32(colAcc + D + 32 * c, ra);
           tmem_ld32(colAcc + 32 * c, rb);
-          tmem_ld_wait();
+          tmem_ld_wait_regs(ra);
+          tmem_ld_wait_regs(rb);
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {

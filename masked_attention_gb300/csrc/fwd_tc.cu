@@ -159,17 +159,15 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
                 (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// Loads n32 x 32 columns of this thread's TMEM lane into s (one wait for all).
 __device__ __forceinline__ void load_cols(uint32_t col, float* s, int n32) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(s);
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    if (c < n32) {
-      uint32_t r[32];
-      tmem_ld32(col + 32 * c, r);
+  for (int c = 0; c < 4; ++c)
+    if (c < n32) tmem_ld32(col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
 #pragma unroll
-      for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(r[e]);
-    }
-  }
-  tmem_ld_wait();
+  for (int c = 0; c < 4; ++c)
+    if (c < n32) tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
 }
 
 // s[0..N) <- score_mod(s) in log2 units minus `shift` for the columns
@@ -267,9 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(s_full + x, 1);
-      mbar_init(p_full + x, kSoftmaxThreads);
+      mbar_init(p_full + x, kSoftmaxThreads / 32);  // one arrive per softmax warp
       mbar_init(o_done + x, 1);
-      mbar_init(o_free + x, kSoftmaxThreads);
+      mbar_init(o_free + x, kSoftmaxThreads / 32);
     }
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(slot_full + s, 1);
@@ -520,14 +518,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         // its true maximum, rescaling l and O.
         uint32_t pk[64];
         float tsum = 0.0f;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          float v[64];
-          load_cols(colS + 64 * hf, v, 2);
-          transform_cols<SCORE, 64>(v, 64 * hf, tc, m_ref, partial);
-          tsum += exp2_pack<64>(v, pk + 32 * hf);
+        // A unit's first tile has no reference yet (m_ref = -inf in every row):
+        // it goes straight to the max pass below.
+        bool redo = true;
+        if (j > 0) {
+          // the second half's load is in flight while the first half is processed
+          float v0[64], v1[64];
+          load_cols(colS, v0, 2);
+          tmem_ld32(colS + 64, *reinterpret_cast<uint32_t(*)[32]>(v1));
+          tmem_ld32(colS + 96, *reinterpret_cast<uint32_t(*)[32]>(v1 + 32));
+          transform_cols<SCORE, 64>(v0, 0, tc, m_ref, partial);
+          tsum = exp2_pack<64>(v0, pk);
+          tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(v1));
+          tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(v1 + 32));
+          transform_cols<SCORE, 64>(v1, 64, tc, m_ref, partial);
+          tsum += exp2_pack<64>(v1, pk + 32);
+          redo = !(tsum <= 18446744073709551616.0f);
         }
-        const bool redo = !(tsum <= 18446744073709551616.0f);
         if (__any_sync(0xffffffffu, redo)) {
           // pass 1: the tile's maximum, 32 columns at a time
           float mt = -INFINITY;
@@ -548,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < D / 32; ++c) {
               uint32_t r[32];
               tmem_ld32(colO + 32 * c, r);
-              tmem_ld_wait();
+              tmem_ld_wait_regs(r);
 #pragma unroll
               for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a);
               tmem_st32(colO + 32 * c, r);
@@ -571,7 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st32(colS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full + x);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full + x);
       }
       if (!ok) break;
       // epilogue: O / l -> bf16, LSE = ln(sum exp)
@@ -584,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
         tmem_ld32(colO + 32 * c, r);
-        tmem_ld_wait();
+        tmem_ld_wait_regs(r);
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
@@ -595,7 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
       }
       tc_fence_before();
-      mbar_arrive(o_free + x);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free + x);
       p.lse[orow] = l > 0.0f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
