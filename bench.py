@@ -203,11 +203,27 @@ def run_reference(args, rank: int, world: int) -> None:
     print(json.dumps(line), flush=True)
 
 
+def variant_of(w, M):
+    """The library's variant bits for a workload (its mask and score terms)."""
+    v = 0
+    v |= M.MASK_CAUSAL if w.causal else 0
+    v |= M.MASK_WINDOW if w.window is not None else 0
+    v |= M.MASK_DOCUMENT if w.document else 0
+    v |= M.MASK_PREFIX if w.prefix else 0
+    v |= M.SCORE_ALIBI if w.alibi else 0
+    v |= M.SCORE_SOFTCAP if w.softcap is not None else 0
+    return v
+
+
 def config_dict(w):
-    return {"workload": f"bf16 causal + ALiBi attention forward, B={w.B} Hq={w.Hq} Hkv={w.Hkv} "
+    terms = [t for t, on in (("causal", w.causal), (f"window {w.window}", w.window is not None),
+                             ("document", w.document), ("prefix", w.prefix),
+                             ("ALiBi slope_h = 2^(-8(h+1)/H)", w.alibi),
+                             (f"soft-cap {w.softcap}", w.softcap is not None)) if on]
+    return {"workload": f"{w.name} attention forward, B={w.B} Hq={w.Hq} Hkv={w.Hkv} "
                         f"S={w.Sq} D={w.D}",
             "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.Sq, "D": w.D,
-            "variant": "causal + alibi (slope_h = 2^(-8(h+1)/H))", "seed": w.seed,
+            "variant": " + ".join(terms), "seed": w.seed,
             "l2": "flushed between timed steps (512 MiB write)",
             "step": "build_block_mask + attn_fwd"}
 
@@ -222,9 +238,8 @@ def run_ours(args, rank: int, world: int) -> None:
     local = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = make_workload(WORKLOAD, **({"B": args.batch} if args.batch else {}))
-    variant = M.MASK_CAUSAL | M.SCORE_ALIBI  # the workload's mask and score terms
-    assert w.causal and w.alibi and not (w.document or w.prefix or w.window or w.softcap)
+    w = make_workload(args.workload, **({"B": args.batch} if args.batch else {}))
+    variant = variant_of(w, M)
     pairs = kept_pairs(w)
     flops = 4.0 * w.D * pairs * w.Hq  # per step, whole batch
     stream = torch.cuda.current_stream()
@@ -236,9 +251,14 @@ def run_ours(args, rank: int, world: int) -> None:
                          device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
+    doc = torch.from_numpy(w.doc_id).to(dev) if w.document else None
+    pre = torch.from_numpy(w.prefix_len).to(dev) if w.prefix else None
+    mkw = dict(window=w.window or 0, doc_id=doc, prefix_len=pre)
+    fkw = dict(mkw, softcap=w.softcap or 0.0)
+
     def step():
-        bm = M.build_block_mask(variant & 0xF, w.B, w.Sq, w.Skv, buf=bm_buf, stream=stream)
-        M.attn_fwd(q, k, v, o, lse, variant, block_mask=bm, stream=stream)
+        bm = M.build_block_mask(variant & 0xF, w.B, w.Sq, w.Skv, buf=bm_buf, stream=stream, **mkw)
+        M.attn_fwd(q, k, v, o, lse, variant, block_mask=bm, stream=stream, **fkw)
 
     def barrier():
         if world > 1:
@@ -265,9 +285,10 @@ def run_ours(args, rank: int, world: int) -> None:
         for s in range(args.steps):
             flush.fill_(s & 0xFF)  # L2 flush, outside the events
             ev[s][0].record(stream)
-            bm = M.build_block_mask(variant & 0xF, w.B, w.Sq, w.Skv, buf=bm_buf, stream=stream)
+            bm = M.build_block_mask(variant & 0xF, w.B, w.Sq, w.Skv, buf=bm_buf, stream=stream,
+                                    **mkw)
             ev[s][1].record(stream)
-            M.attn_fwd(q, k, v, o, lse, variant, block_mask=bm, stream=stream)
+            M.attn_fwd(q, k, v, o, lse, variant, block_mask=bm, stream=stream, **fkw)
             ev[s][2].record(stream)
         barrier()
     if M.attn_check_status() != M.ATTN_OK:
@@ -325,7 +346,7 @@ def run_ours(args, rank: int, world: int) -> None:
         "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak,
                      "unit": "TFLOP/s", "frac": fwd_tflops / peak,
                      "traffic": profiled_traffic(digest),
-                     "kernel": "fwd_tc_kernel<D=64, ALiBi>",
+                     "kernel": f"fwd_tc_kernel<D={w.D}>",
                      "peak_source": ("measured bf16 dense burst (MEASURED_PEAKS.json)"
                                      if peak_kind == "measured" else "fallback 1.9 PFLOP/s")},
         "e2e": e2e,
@@ -353,6 +374,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0, help="override B (profiling cases only)")
+    ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[2, 3, 4, 5],
+                    help="diagnostic runs on the other bf16 workloads (forward only)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
