@@ -498,9 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 float pr = ex2_approx(fmaf(x, kLog2e, -row_lse2));
                 if (partial) {
-                  bool keep = (c >= lo) && (c < hi);
-                  if (docb) keep = keep && (sdoc[c] == my_doc);
-                  keep = keep || (c < pre);
+                  // bitwise terms, document id read on a warp-uniform condition:
+                  // no divergent branch per element
+                  const bool same = docb ? (sdoc[c] == my_doc) : true;
+                  const bool keep = ((c >= lo) & (c < hi) & same) | (c < pre);
                   pr = keep ? pr : 0.0f;
                 }
                 const float dp = __uint_as_float(rp[e + z]);
@@ -565,9 +566,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (MODE == kDKV) lse2 = slse[c] == -INFINITY ? INFINITY : slse[c] * kLog2e;
             float pr = ex2_approx(fmaf(x, kLog2e, -lse2));
             if (partial) {
-              bool keep = (c >= lo) && (c < hi);
-              if (docb) keep = keep && (sdoc[c] == my_doc);
-              keep = keep || (c < pre);
+              // bitwise terms, document id read on a warp-uniform condition:
+              // no divergent branch per element
+              const bool same = docb ? (sdoc[c] == my_doc) : true;
+              const bool keep = ((c >= lo) & (c < hi) & same) | (c < pre);
               pr = keep ? pr : 0.0f;
             }
             if constexpr (MODE == kDKV) {

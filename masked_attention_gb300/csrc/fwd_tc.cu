@@ -54,11 +54,14 @@ struct Cfg {
   // barriers: q_full, q_empty, drain, s_full[2], p_full[2], o_done[2], o_free[2],
   // slot_full[kSlots], slot_empty[kSlots]
   static constexpr int kNumBars = 11 + 2 * kSlots;
-  static constexpr int kOffDoc = kOffBars + kNumBars * 8;
-  static constexpr int kOffMisc = kOffDoc + 8 * kTile * 4;  // per-warp doc ids
+  // per-warp document ids, read as int4: 16-byte aligned
+  static constexpr int kOffDoc = (kOffBars + kNumBars * 8 + 15) & ~15;
+  static constexpr int kOffMisc = kOffDoc + 8 * kTile * 4;
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;     // slack for 1024-byte alignment
   static constexpr uint32_t kColO0 = 256;
+  static_assert(kOffDoc % 16 == 0 && (kTile * 4) % 16 == 0, "int4 reads of document ids");
+  static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
 };
 
 struct Unit {
@@ -204,14 +207,31 @@ __device__ __forceinline__ void transform_cols(float* s, int c0, const TileCtx& 
       s[c + 1] = e.y;
     }
   }
-  if (partial) {  // mask_mod: keep (c <= hi && c > lo && same document) || c < pre
+  // mask_mod: keep (lo < c <= hi and same document) or c < pre. The terms are
+  // combined with bitwise operators and the document ids are read
+  // unconditionally, four at a time: a short-circuit form would make every
+  // element a divergent branch around a load (rows differ in hi), which costs
+  // tens of cycles per element.
+  if (partial) {
+    if (t.wdoc) {
 #pragma unroll
-    for (int c = 0; c < N; ++c) {
-      const int cc = c0 + c;
-      bool keep = (cc <= t.hi) && (cc > t.lo);
-      if (t.wdoc) keep = keep && (t.wdoc[cc] == t.doc_i);
-      keep = keep || (cc < t.pre);
-      s[c] = keep ? s[c] : -INFINITY;
+      for (int c = 0; c < N; c += 4) {
+        const int4 dv = *reinterpret_cast<const int4*>(t.wdoc + c0 + c);
+        const int d4[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int cc = c0 + c + e;
+          const bool keep = ((cc <= t.hi) & (cc > t.lo) & (d4[e] == t.doc_i)) | (cc < t.pre);
+          s[c + e] = keep ? s[c + e] : -INFINITY;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < N; ++c) {
+        const int cc = c0 + c;
+        const bool keep = ((cc <= t.hi) & (cc > t.lo)) | (cc < t.pre);
+        s[c] = keep ? s[c] : -INFINITY;
+      }
     }
   }
 }

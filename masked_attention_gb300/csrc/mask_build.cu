@@ -85,13 +85,20 @@ __global__ void __launch_bounds__(128) classify_kernel(MaskArgs m, int Sq, int S
   for (int inner = warp; inner < n_inner; inner += 4) {
     const int inner_len = transposed ? Sq : Skv;
     const Range rn{inner * kTile, min((inner + 1) * kTile, inner_len) - 1};
-    int nmin = 0, nmax = 0;
-    if (doc) warp_doc_minmax(doc, rn, nmin, nmax);
     const Range ri = transposed ? rn : ro;
     const Range rj = transposed ? ro : rn;
-    const int qmin = transposed ? nmin : omin, qmax = transposed ? nmax : omax;
-    const int kmin = transposed ? omin : nmin, kmax = transposed ? omax : nmax;
-    int st = bounds_state(m, b, ri, rj, qmin, qmax, kmin, kmax);
+    // The document term can only remove pairs: a tile the other terms already
+    // leave empty is empty, and its document ids need not be read.
+    MaskArgs m_nodoc = m;
+    m_nodoc.variant &= ~ATTN_MASK_DOCUMENT;
+    int st = bounds_state(m_nodoc, b, ri, rj, 0, 0, 0, 0);
+    if (st != kEmpty && doc) {
+      int nmin = 0, nmax = 0;
+      warp_doc_minmax(doc, rn, nmin, nmax);
+      const int qmin = transposed ? nmin : omin, qmax = transposed ? nmax : omax;
+      const int kmin = transposed ? omin : nmin, kmax = transposed ? omax : nmax;
+      st = bounds_state(m, b, ri, rj, qmin, qmax, kmin, kmax);
+    }
     if (st >= 8) {  // undecided: look at the pairs
       bool any_keep = false, any_drop = false;
       const int ncols = rj.hi - rj.lo + 1;
