@@ -510,19 +510,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int doc_i = docb ? docb[i] : 0;
       const int P = (p.variant & ATTN_MASK_PREFIX) ? p.mask.prefix_len[U.b] : INT_MIN;
       float m_ref = -INFINITY, l = 0.0f;
-      int kt_next = U.kt(0);
+      // Key-tile indices are read two tiles ahead and the document ids of a
+      // partial tile one tile ahead, so neither global read waits on the
+      // critical path (lane l holds ids l, l+32, l+64, l+96).
+      int kt_cur = U.kt(0), kt_n1 = n > 1 ? U.kt(1) : 0;
+      int dcur[4] = {0, 0, 0, 0};
+      if (docb && U.partial(0)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dcur[c] = docb[kt_cur * kTile + lane + 32 * c];
+      }
 
       for (int j = 0; j < n; ++j) {
-        const int kt = kt_next;
-        if (j + 1 < n) kt_next = U.kt(j + 1);  // issued early: used next iteration
+        const int kt = kt_cur;
+        const int kt_n2 = j + 2 < n ? U.kt(j + 2) : 0;
+        int dnext[4] = {0, 0, 0, 0};
+        if (docb && j + 1 < n && U.partial(j + 1)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) dnext[c] = docb[kt_n1 * kTile + lane + 32 * c];
+        }
         const int j0 = kt * kTile;
         const bool partial = U.partial(j);
         if (partial && docb) {
           __syncwarp();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) wdoc[lane + 32 * c] = docb[j0 + lane + 32 * c];
+          for (int c = 0; c < 4; ++c) wdoc[lane + 32 * c] = dcur[c];
           __syncwarp();
         }
+        kt_cur = kt_n1;
+        kt_n1 = kt_n2;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dcur[c] = dnext[c];
         ok = __all_sync(0xffffffffu, wait_bounded(s_full + x, s_it & 1, wd));
         if (!ok) break;
         ++s_it;

@@ -63,7 +63,9 @@ __device__ __forceinline__ int bounds_state(const MaskArgs& m, int b, Range ri, 
   return kPartial + 8;  // undecided
 }
 
-__global__ void __launch_bounds__(128) classify_kernel(MaskArgs m, int Sq, int Skv,
+constexpr int kClassifyThreads = 512;  // 16 warps, one key tile per warp at a time
+
+__global__ void __launch_bounds__(kClassifyThreads) classify_kernel(MaskArgs m, int Sq, int Skv,
                                                        int transposed, int* cnt_full,
                                                        int* cnt_part, int* idx_full,
                                                        int* idx_part) {
@@ -82,7 +84,7 @@ __global__ void __launch_bounds__(128) classify_kernel(MaskArgs m, int Sq, int S
   int omin = 0, omax = 0;
   if (doc) warp_doc_minmax(doc, ro, omin, omax);  // every warp computes it
 
-  for (int inner = warp; inner < n_inner; inner += 4) {
+  for (int inner = warp; inner < n_inner; inner += kClassifyThreads / 32) {
     const int inner_len = transposed ? Sq : Skv;
     const Range rn{inner * kTile, min((inner + 1) * kTile, inner_len) - 1};
     const Range ri = transposed ? rn : ro;
@@ -100,13 +102,30 @@ __global__ void __launch_bounds__(128) classify_kernel(MaskArgs m, int Sq, int S
       st = bounds_state(m, b, ri, rj, qmin, qmax, kmin, kmax);
     }
     if (st >= 8) {  // undecided: look at the pairs
-      bool any_keep = false, any_drop = false;
+      // Lane l owns columns l, l+32, l+64, l+96 of the tile; their document
+      // ids stay in registers and each row reads its own id once. The terms
+      // are combined bitwise, so no lane branches around a load.
       const int ncols = rj.hi - rj.lo + 1;
+      int dj[4];
+      bool valid[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int c = lane + 32 * k;
+        valid[k] = c < ncols;
+        dj[k] = (doc && valid[k]) ? doc[rj.lo + c] : 0;
+      }
+      const bool causal = m.variant & ATTN_MASK_CAUSAL, window = m.variant & ATTN_MASK_WINDOW;
+      const int P = (m.variant & ATTN_MASK_PREFIX) ? m.prefix_len[b] : INT_MIN;
+      bool any_keep = false, any_drop = false;
       for (int i = ri.lo; i <= ri.hi; ++i) {
-        for (int c = lane; c < ncols; c += 32) {
-          const bool k = mask_keep(m, b, i, rj.lo + c);
-          any_keep |= k;
-          any_drop |= !k;
+        const int di = doc ? doc[i] : 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int j = rj.lo + lane + 32 * k;
+          const bool keep = ((!causal | (j <= i)) & (!window | (i - j < m.window)) & (dj[k] == di)) |
+                            (j < P);
+          any_keep |= valid[k] & keep;
+          any_drop |= valid[k] & !keep;
         }
         if (__any_sync(0xffffffffu, any_keep) && __any_sync(0xffffffffu, any_drop)) break;
       }
@@ -176,7 +195,7 @@ cudaError_t launch_block_mask(const MaskArgs& m, int B, int Sq, int Skv, int tra
   const int n_outer = transposed ? nkv : nq;
   const int n_inner = transposed ? nq : nkv;
   dim3 grid(n_outer, B);
-  classify_kernel<<<grid, 128, n_inner, stream>>>(m, Sq, Skv, transposed, cnt_full, cnt_part,
+  classify_kernel<<<grid, kClassifyThreads, n_inner, stream>>>(m, Sq, Skv, transposed, cnt_full, cnt_part,
                                                   idx_full, idx_part);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
