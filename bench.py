@@ -93,8 +93,15 @@ def profiled_traffic(kernel_digest: str):
     return traffic if digest == kernel_digest else None
 
 
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """SM clock and clock-event (throttle) reasons sampled during the timed
+    region: NVML read through ctypes every 2 ms on a background thread (the
+    timed region can be a few milliseconds), else nvidia-smi every 200 ms.
+    Only reads; changes no setting."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -102,19 +109,70 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
+        self.samples = []  # (sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self.source = None
+        self.out = ""
+
+    def _nvml_handle(self):
+        import ctypes
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        handle = ctypes.c_void_p()
+        uuid = getattr(torch.cuda.get_device_properties(self.idx), "uuid", None)
+        ok = False
+        if uuid is not None:
+            ok = lib.nvmlDeviceGetHandleByUUID(("GPU-" + str(uuid)).encode(),
+                                               ctypes.byref(handle)) == 0
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.idx, ctypes.byref(handle)) != 0:
+            return None
+        return lib, handle
+
+    def _poll(self, lib, handle):
+        import ctypes
+        clk, reasons = ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if (lib.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(clk)) == 0 and
+                    get_reasons(handle, ctypes.byref(reasons)) == 0):
+                self.samples.append((float(clk.value), int(reasons.value)))
+            self._stop.wait(0.002)
 
     def __enter__(self):
+        import threading
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            got = self._nvml_handle()
+        except (OSError, AttributeError):
+            got = None
+        if got is not None:
+            import ctypes
+            lib, handle = got
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.source = "nvml"
+            self._thread = threading.Thread(target=self._poll, args=got, daemon=True)
+            self._thread.start()
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
         except OSError:
             self.proc = None
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -124,6 +182,14 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
 
     def summary(self):
+        if self.source == "nvml" and self.samples:
+            sm = [c for c, _ in self.samples]
+            bits = 0
+            for _, r in self.samples:
+                bits |= r
+            reasons = sorted(n for k, n in NVML_REASONS.items() if bits & k)
+            return {"sm_mhz": statistics.median(sm), "sm_max_mhz": self.max_mhz,
+                    "reasons": reasons, "samples": len(sm), "source": "nvml, 2 ms"}
         rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 8]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
@@ -134,30 +200,51 @@ class ClockSampler:
                           if r[5 + k].strip().lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(rows), "source": "nvidia-smi, 200 ms"}
 
 
-def oracle_leg(w, seconds_target: float, cores: int):
-    """Times the CPU oracle on whole heads of the workload (a bounded sample),
-    one head per worker process; returns (TFLOPS, sample description, cores)."""
-    import multiprocessing as mp
-    per_head_pairs = kept_pairs(w) // w.B
-    heads = [(b, h) for b in range(w.B) for h in range(w.Hq)]
-    ctx = mp.get_context("spawn")
-    done = 0
-    t0 = time.perf_counter()
-    with ctx.Pool(processes=cores, initializer=_oracle_worker_init,
-                  initargs=(WORKLOAD,)) as pool:
-        # one warm round loads the inputs in every worker, then the timed rounds
-        pool.map(_oracle_head, heads[:cores])
+class OracleTimer:
+    """Times the CPU oracle on whole (b, h) heads of the workload, one head per
+    worker process of a pool started once (spawn, before any GPU work)."""
+
+    def __init__(self, w, cores: int, number: int = WORKLOAD):
+        import multiprocessing as mp
+        self.w = w
+        self.cores = cores
+        self.per_head_flops = 4.0 * w.D * (kept_pairs(w) // w.B)
+        self.heads = [(b, h) for b in range(w.B) for h in range(w.Hq)]
+        self.pool = mp.get_context("spawn").Pool(processes=cores,
+                                                 initializer=_oracle_worker_init,
+                                                 initargs=(number,))
+        self.pool.map(_oracle_head, self.heads[:cores])  # loads the inputs in every worker
+        self.next = 0
+
+    def step(self, seconds: float):
+        """At least one round of `cores` heads and about `seconds` of work;
+        returns (TFLOPS, heads timed)."""
+        done = 0
         t0 = time.perf_counter()
-        while time.perf_counter() - t0 < seconds_target and done < len(heads):
-            batch = heads[done:done + cores]
-            pool.map(_oracle_head, batch)
+        while done == 0 or time.perf_counter() - t0 < seconds:
+            batch = [self.heads[(self.next + k) % len(self.heads)] for k in range(self.cores)]
+            self.next = (self.next + self.cores) % len(self.heads)
+            self.pool.map(_oracle_head, batch)
             done += len(batch)
-    dt = time.perf_counter() - t0
-    flops = 4.0 * w.D * per_head_pairs * done
-    return flops / dt / 1e12, f"{done} of {len(heads)} (b, h) heads, whole rows", cores
+        dt = time.perf_counter() - t0
+        return self.per_head_flops * done / dt / 1e12, done
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def oracle_leg(w, seconds_target: float, cores: int, number: int = WORKLOAD):
+    """One bounded timing of the oracle; returns (TFLOPS, sample description, cores)."""
+    timer = OracleTimer(w, cores, number)
+    try:
+        tf, done = timer.step(seconds_target)
+    finally:
+        timer.close()
+    return tf, f"{done} (b, h) heads of {len(timer.heads)}, whole rows, fp64", cores
 
 
 _W = None
@@ -178,25 +265,36 @@ def _oracle_head(bh):
     return bh
 
 
+REFERENCE_BUDGET_S = 150.0  # whole --impl reference run, warm-up included
+
+
 def run_reference(args, rank: int, world: int) -> None:
+    """The CPU oracle as it stands, on the host's cores: each step times a
+    bounded sample of whole heads, sized so the whole run stays within a few
+    minutes whatever --steps and --warmup are."""
     if rank != 0:
         return
     from synth import make_workload
     w = make_workload(WORKLOAD, with_tensors=False)
     cores = os.cpu_count() or 1
-    steps = []
-    for _ in range(args.warmup):
-        oracle_leg(w, 2.0, cores)
-    for _ in range(args.steps):
-        steps.append(oracle_leg(w, 8.0, cores))
-    value = statistics.median(s[0] for s in steps)
+    per_step = min(8.0, max(0.5, REFERENCE_BUDGET_S / max(1, args.steps + args.warmup)))
+    timer = OracleTimer(w, cores)
+    try:
+        for _ in range(args.warmup):
+            timer.step(per_step)
+        steps = [timer.step(per_step) for _ in range(args.steps)]
+    finally:
+        timer.close()
+    value = statistics.median(tf for tf, _ in steps)
+    sample = (f"about {per_step:.1f} s of whole (b, h) heads per step "
+              f"({steps[0][1]} to {max(d for _, d in steps)} of {len(timer.heads)} heads), fp64")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_dict(w),
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-                         "sample": steps[0][1] + " per step"},
+                         "sample": sample},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -358,7 +456,7 @@ def run_ours(args, rank: int, world: int) -> None:
         "source_digest": digest,
     }
     if not args.no_cpu_baseline:
-        tf, sample, cores = oracle_leg(w, args.cpu_seconds, os.cpu_count() or 1)
+        tf, sample, cores = oracle_leg(w, args.cpu_seconds, os.cpu_count() or 1, args.workload)
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOPS", "cores": cores,
                                 "kind": "oracle", "sample": sample}
     print(json.dumps(line), flush=True)
