@@ -132,7 +132,10 @@ struct TileCtx {
   int hi, lo, pre;   // mask bounds on the column c (see transform_tile)
   const int* wdoc;   // document ids of the key tile (shared memory), or nullptr
   int doc_i;
+  uint32_t modes;    // per 32-column chunk of a partial tile (chunk_modes)
 };
+
+constexpr uint32_t kChunkKept = 0, kChunkMasked = 1, kChunkMixed = 2;
 
 // Whole-warp bounded wait (every lane polls; the result is the same for all).
 __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
@@ -207,33 +210,80 @@ __device__ __forceinline__ void transform_cols(float* s, int c0, const TileCtx& 
       s[c + 1] = e.y;
     }
   }
-  // mask_mod: keep (lo < c <= hi and same document) or c < pre. The terms are
-  // combined with bitwise operators and the document ids are read
-  // unconditionally, four at a time: a short-circuit form would make every
-  // element a divergent branch around a load (rows differ in hi), which costs
-  // tens of cycles per element.
+  // mask_mod on a partial tile: keep (lo < c <= hi and same document) or
+  // c < pre. Chunks of 32 columns that every row of the warp keeps need no
+  // work and chunks no row keeps become -inf (t.modes, see chunk_modes); only
+  // mixed chunks are masked element by element. There the terms are combined
+  // with bitwise operators and the document ids are read unconditionally, four
+  // at a time: a short-circuit form would make every element a divergent
+  // branch around a load.
   if (partial) {
-    if (t.wdoc) {
 #pragma unroll
-      for (int c = 0; c < N; c += 4) {
-        const int4 dv = *reinterpret_cast<const int4*>(t.wdoc + c0 + c);
-        const int d4[4] = {dv.x, dv.y, dv.z, dv.w};
+    for (int q = 0; q < N / 32; ++q) {
+      const int a = c0 + 32 * q;  // first column of the chunk
+      const uint32_t mode = (t.modes >> (2 * (a >> 5))) & 3u;
+      if (mode == kChunkKept) continue;
+      float* sq = s + 32 * q;
+      if (mode == kChunkMasked) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int cc = c0 + c + e;
-          const bool keep = ((cc <= t.hi) & (cc > t.lo) & (d4[e] == t.doc_i)) | (cc < t.pre);
-          s[c + e] = keep ? s[c + e] : -INFINITY;
-        }
+        for (int c = 0; c < 32; ++c) sq[c] = -INFINITY;
+        continue;
       }
-    } else {
+      if (t.wdoc) {
 #pragma unroll
-      for (int c = 0; c < N; ++c) {
-        const int cc = c0 + c;
-        const bool keep = ((cc <= t.hi) & (cc > t.lo)) | (cc < t.pre);
-        s[c] = keep ? s[c] : -INFINITY;
+        for (int c = 0; c < 32; c += 4) {
+          const int4 dv = *reinterpret_cast<const int4*>(t.wdoc + a + c);
+          const int d4[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int cc = a + c + e;
+            const bool keep =
+                ((cc <= t.hi) & (cc > t.lo) & (d4[e] == t.doc_i)) | (cc < t.pre);
+            sq[c + e] = keep ? sq[c + e] : -INFINITY;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int cc = a + c;
+          const bool keep = ((cc <= t.hi) & (cc > t.lo)) | (cc < t.pre);
+          sq[c] = keep ? sq[c] : -INFINITY;
+        }
       }
     }
   }
+}
+
+// Warp-uniform mode of each 32-column chunk of a partial tile, two bits per
+// chunk: kept by every row of the warp, masked for every row, or mixed. From
+// the rows' column bounds and the min/max document id of the chunk's keys;
+// exact for "kept" and "masked", conservative ("mixed") otherwise. Integer
+// compares run at half rate, so deciding whole chunks saves most of the
+// per-element mask work on diagonal, window-edge and document-edge tiles.
+__device__ __forceinline__ uint32_t chunk_modes(const TileCtx& t) {
+  const int lane = threadIdx.x & 31;
+  uint32_t modes = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int a = 32 * q;
+    const bool pre_all = a + 31 < t.pre, pre_none = a >= t.pre;
+    bool all = ((a + 31 <= t.hi) & (a > t.lo)) | pre_all;
+    bool none = ((a > t.hi) | (a + 31 <= t.lo)) & pre_none;
+    if (t.wdoc) {
+      const int dl = t.wdoc[a + lane];
+      const int dmin = __reduce_min_sync(0xffffffffu, dl);
+      const int dmax = __reduce_max_sync(0xffffffffu, dl);
+      const bool d_all = (dmin == t.doc_i) & (dmax == t.doc_i);
+      const bool d_none = (t.doc_i < dmin) | (t.doc_i > dmax);
+      all = (all & d_all) | pre_all;
+      none = none | (d_none & pre_none);
+    }
+    const uint32_t m = __all_sync(0xffffffffu, all)    ? kChunkKept
+                       : __all_sync(0xffffffffu, none) ? kChunkMasked
+                                                       : kChunkMixed;
+    modes |= m << (2 * q);
+  }
+  return modes;
 }
 
 // pk[0..N/2) <- bf16 pairs of 2^s; returns the fp32 sum.
@@ -540,14 +590,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         kt_n1 = kt_n2;
 #pragma unroll
         for (int c = 0; c < 4; ++c) dcur[c] = dnext[c];
+        TileCtx tc{sl2, sc, cl2, slope, slope2, p.score.scale, 1.0f / p.score.softcap,
+                   float(j0 - i), (p.variant & ATTN_MASK_CAUSAL) ? i - j0 : INT_MAX,
+                   (p.variant & ATTN_MASK_WINDOW) ? i - j0 - p.mask.window : INT_MIN,
+                   P == INT_MIN ? INT_MIN : P - j0, docb ? wdoc : nullptr, doc_i, 0u};
+        if (partial) tc.modes = chunk_modes(tc);  // before the wait: off the critical path
         ok = __all_sync(0xffffffffu, wait_bounded(s_full + x, s_it & 1, wd));
         if (!ok) break;
         ++s_it;
         tc_fence_after();
-        const TileCtx tc{sl2, sc, cl2, slope, slope2, p.score.scale, 1.0f / p.score.softcap,
-                         float(j0 - i), (p.variant & ATTN_MASK_CAUSAL) ? i - j0 : INT_MAX,
-                         (p.variant & ATTN_MASK_WINDOW) ? i - j0 - p.mask.window : INT_MIN,
-                         P == INT_MIN ? INT_MIN : P - j0, docb ? wdoc : nullptr, doc_i};
         // Steady state: exponentiate against the current reference max with no
         // max pass, 64 columns at a time, keeping P as packed bf16. A tile whose
         // sum is not finite or exceeds 2^64 (the first tile, or a tile whose
