@@ -41,6 +41,7 @@ constexpr int kRegsOther = 88;
 constexpr int kSoftmaxThreads = 128;
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;
+constexpr int kWarpMma2 = 10;  // second MMA issuer (separate-P kernels: head B)
 
 template <int D>
 struct Cfg {
@@ -52,14 +53,21 @@ struct Cfg {
   static constexpr int kOffSlots = 2 * kTileBytes;
   static constexpr int kOffBars = kOffSlots + kSlots * kTileBytes;
   // barriers: q_full, q_empty, drain, s_full[2], p_full[2], o_done[2], o_free[2],
-  // slot_full[kSlots], slot_empty[kSlots]
-  static constexpr int kNumBars = 11 + 2 * kSlots;
+  // s_free[2], pv_done[2], drain2, slot_full[kSlots], slot_empty[kSlots]
+  static constexpr int kNumBars = 16 + 2 * kSlots;
   // per-warp document ids, read as int4: 16-byte aligned
   static constexpr int kOffDoc = (kOffBars + kNumBars * 8 + 15) & ~15;
   static constexpr int kOffMisc = kOffDoc + 8 * kTile * 4;
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;     // slack for 1024-byte alignment
   static constexpr uint32_t kColO0 = 256;
+  // D = 64 leaves TMEM room for P apart from S (columns 384 + 64x): the
+  // softmax frees S as soon as it has read it and the next Q.K^T overlaps the
+  // rest of its work. At D = 128 the 512 columns hold S_A, S_B, O_A, O_B and P
+  // overwrites S, so the next Q.K^T waits for the P.V product.
+  static constexpr bool kSepP = D == 64;
+  static constexpr uint32_t kColP = 384;
+  static_assert(!kSepP || kColP + 128 <= 512, "tensor memory columns");
   static_assert(kOffDoc % 16 == 0 && (kTile * 4) % 16 == 0, "int4 reads of document ids");
   static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
 };
@@ -320,8 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = bars + 5;   // [2]
   uint64_t* o_done = bars + 7;   // [2]
   uint64_t* o_free = bars + 9;   // [2]
-  uint64_t* slot_full = bars + 11;
-  uint64_t* slot_empty = bars + 11 + C::kSlots;
+  uint64_t* s_free = bars + 11;  // [2] (separate P only) S read by the softmax
+  uint64_t* pv_done = bars + 13; // [2] (separate P only) P.V product complete
+  uint64_t* drain2 = bars + 15;  // (separate P only) second MMA warp's products
+  uint64_t* slot_full = bars + 16;
+  uint64_t* slot_empty = bars + 16 + C::kSlots;
   int* sdoc = reinterpret_cast<int*>(smem + C::kOffDoc);
   uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -330,18 +341,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Watchdog wd{abort_flag, p.status, p.timeout_ns};
 
   if (threadIdx.x == 0) {
+    // With separate P each head has its own MMA warp and every Q tile and
+    // ring slot is released by two commits (one per warp, or two by the one
+    // warp that used it).
     mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
+    mbar_init(q_empty, C::kSepP ? 2 : 1);
     mbar_init(drain, 1);
+    mbar_init(drain2, 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(s_full + x, 1);
       mbar_init(p_full + x, kSoftmaxThreads / 32);  // one arrive per softmax warp
       mbar_init(o_done + x, 1);
       mbar_init(o_free + x, kSoftmaxThreads / 32);
+      mbar_init(s_free + x, kSoftmaxThreads / 32);
+      mbar_init(pv_done + x, 1);
     }
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(slot_full + s, 1);
-      mbar_init(slot_empty + s, 1);
+      mbar_init(slot_empty + s, C::kSepP ? 2 : 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -426,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (q_it > 0) wait_drain(q_full, (q_it - 1) & 1);
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp == kWarpMma || (C::kSepP && warp == kWarpMma2)) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop (waits stay converged); lane 0 issues the
     // products and the commits. Loop state stays in registers and the
@@ -438,91 +455,179 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t dK0 = sdesc_sw128(smem_u32(sSlots), 16, 1024);
     const uint64_t dV0 = sdesc_sw128(smem_u32(sSlots), C::kBoxBytes, 1024);
-    uint32_t slot_it = 0, q_it = 0, p_it0 = 0, p_it1 = 0, o_it0 = 0, o_it1 = 0;
-    bool ok = true;
-    for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
-      const int u = zigzag_unit(r);
-      if (u >= num_units) continue;
-      const Unit U = decode_unit(p, u, nhp);
-      const int n = U.n();
-      if (n == 0) continue;
-      const int nx = U.h[1] >= 0 ? 2 : 1;
-      const bool shared = nx == 1 || (U.h[0] / group == U.h[1] / group);
-      const uint32_t T = shared ? 2u : 4u;  // ring slots per key tile
-      ok = wait_warp(q_full, q_it & 1, wd);
-      if (!ok) break;
-      ++q_it;
-      tc_fence_after();
-      // S_x(0) for both heads
-      for (int x = 0; x < nx && ok; ++x) {
-        const uint32_t seq = slot_it + (shared ? 0u : (uint32_t)x);
-        const uint32_t slot = seq % C::kSlots;
-        if (x == 0 || !shared) {
-          ok = wait_warp(slot_full + slot, (seq / C::kSlots) & 1, wd);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        if (leader) {
-          issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
-                      dK0 + ((slot * C::kTileBytes) >> 4), kIdescQK);
-          mma_commit(s_full + x);
-          if (!shared || x == nx - 1) mma_commit(slot_empty + slot);
-        }
-        __syncwarp();
-      }
-      if (ok && n == 1 && leader) mma_commit(q_empty);
-      for (int j = 0; j < n && ok; ++j) {
+    if constexpr (!C::kSepP) {
+      uint32_t slot_it = 0, q_it = 0, p_it0 = 0, p_it1 = 0, o_it0 = 0, o_it1 = 0;
+      bool ok = true;
+      for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
+        const int u = zigzag_unit(r);
+        if (u >= num_units) continue;
+        const Unit U = decode_unit(p, u, nhp);
+        const int n = U.n();
+        if (n == 0) continue;
+        const int nx = U.h[1] >= 0 ? 2 : 1;
+        const bool shared = nx == 1 || (U.h[0] / group == U.h[1] / group);
+        const uint32_t T = shared ? 2u : 4u;  // ring slots per key tile
+        ok = wait_warp(q_full, q_it & 1, wd);
+        if (!ok) break;
+        ++q_it;
+        tc_fence_after();
+        // S_x(0) for both heads
         for (int x = 0; x < nx && ok; ++x) {
-          // O_x += P_x V_j
-          ok = wait_warp(p_full + x, (x ? p_it1 : p_it0) & 1, wd);
-          if (!ok) break;
-          if (x) ++p_it1; else ++p_it0;
-          if (j == 0) {
-            ok = wait_warp(o_free + x, ((x ? o_it1 : o_it0) & 1) ^ 1, wd);
-            if (!ok) break;
-            if (x) ++o_it1; else ++o_it0;
-          }
-          const uint32_t vseq = slot_it + j * T + (shared ? 1u : 2u + x);
-          const uint32_t vslot = vseq % C::kSlots;
+          const uint32_t seq = slot_it + (shared ? 0u : (uint32_t)x);
+          const uint32_t slot = seq % C::kSlots;
           if (x == 0 || !shared) {
-            ok = wait_warp(slot_full + vslot, (vseq / C::kSlots) & 1, wd);
+            ok = wait_warp(slot_full + slot, (seq / C::kSlots) & 1, wd);
             if (!ok) break;
+            tc_fence_after();
           }
-          tc_fence_after();
           if (leader) {
-            issue_pv<D>(tmem + C::kColO0 + D * x, tmem + 128u * x,
-                        dV0 + ((vslot * C::kTileBytes) >> 4), kIdescPV, j > 0);
-            if (!shared || x == nx - 1) mma_commit(slot_empty + vslot);
+            issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
+                        dK0 + ((slot * C::kTileBytes) >> 4), kIdescQK);
+            mma_commit(s_full + x);
+            if (!shared || x == nx - 1) mma_commit(slot_empty + slot);
           }
           __syncwarp();
-          if (j + 1 < n) {  // S_x(j+1)
-            const uint32_t kseq = slot_it + (j + 1) * T + (shared ? 0u : (uint32_t)x);
-            const uint32_t kslot = kseq % C::kSlots;
-            if (x == 0 || !shared) {
-              ok = wait_warp(slot_full + kslot, (kseq / C::kSlots) & 1, wd);
+        }
+        if (ok && n == 1 && leader) mma_commit(q_empty);
+        for (int j = 0; j < n && ok; ++j) {
+          for (int x = 0; x < nx && ok; ++x) {
+            // O_x += P_x V_j
+            ok = wait_warp(p_full + x, (x ? p_it1 : p_it0) & 1, wd);
+            if (!ok) break;
+            if (x) ++p_it1; else ++p_it0;
+            if (j == 0) {
+              ok = wait_warp(o_free + x, ((x ? o_it1 : o_it0) & 1) ^ 1, wd);
               if (!ok) break;
-              tc_fence_after();
+              if (x) ++o_it1; else ++o_it0;
             }
+            const uint32_t vseq = slot_it + j * T + (shared ? 1u : 2u + x);
+            const uint32_t vslot = vseq % C::kSlots;
+            if (x == 0 || !shared) {
+              ok = wait_warp(slot_full + vslot, (vseq / C::kSlots) & 1, wd);
+              if (!ok) break;
+            }
+            tc_fence_after();
+            if (leader) {
+              issue_pv<D>(tmem + C::kColO0 + D * x, tmem + 128u * x,
+                          dV0 + ((vslot * C::kTileBytes) >> 4), kIdescPV, j > 0);
+              if (!shared || x == nx - 1) mma_commit(slot_empty + vslot);
+            }
+            __syncwarp();
+            if (j + 1 < n) {  // S_x(j+1)
+              const uint32_t kseq = slot_it + (j + 1) * T + (shared ? 0u : (uint32_t)x);
+              const uint32_t kslot = kseq % C::kSlots;
+              if (x == 0 || !shared) {
+                ok = wait_warp(slot_full + kslot, (kseq / C::kSlots) & 1, wd);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              if (leader) {
+                issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
+                            dK0 + ((kslot * C::kTileBytes) >> 4), kIdescQK);
+                mma_commit(s_full + x);
+                if (!shared || x == nx - 1) mma_commit(slot_empty + kslot);
+              }
+              __syncwarp();
+            } else if (leader) {
+              mma_commit(o_done + x);
+            }
+          }
+          if (ok && j + 1 == n - 1 && leader) mma_commit(q_empty);
+        }
+        __syncwarp();
+        slot_it += n * T;
+      }
+    } else {
+      // Separate P, one MMA warp per head: warp kWarpMma serves head A and
+      // kWarpMma2 head B, so neither head's products wait behind the other's.
+      // S_x(j+1) = Q_x K_{j+1}^T is issued as soon as the softmax has read
+      // S_x(j) (s_free), before P_x(j) exists; O_x += P_x(j) V_j follows when
+      // P_x(j) is ready. kq counts this head's Q.K^T products (tile k waits
+      // for s_free phase k-1), kp its P.V products. Every Q tile and ring slot
+      // gets exactly two release commits: one from each warp when both heads
+      // read it, else two from the warp that did.
+      const int x = warp == kWarpMma ? 0 : 1;
+      uint32_t slot_it = 0, q_it = 0, kq = 0, kp = 0, o_it = 0;
+      bool ok = true;
+      for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
+        const int u = zigzag_unit(r);
+        if (u >= num_units) continue;
+        const Unit U = decode_unit(p, u, nhp);
+        const int n = U.n();
+        if (n == 0) continue;
+        const int nx = U.h[1] >= 0 ? 2 : 1;
+        const bool shared = nx == 1 || (U.h[0] / group == U.h[1] / group);
+        const uint32_t T = shared ? 2u : 4u;  // ring slots per key tile
+        const uint32_t base = slot_it;
+        slot_it += n * T;
+        ++q_it;
+        if (x >= nx) continue;  // single-head unit: head B's warp has nothing to do
+        const bool both = nx == 2 && shared;  // the other warp releases the same slots
+        ok = wait_warp(q_full, (q_it - 1) & 1, wd);
+        if (!ok) break;
+        for (int j = -1; j < n && ok; ++j) {
+          if (j + 1 < n) {  // S_x(j+1)
+            if (kq > 0) {
+              ok = wait_warp(s_free + x, (kq - 1) & 1, wd);
+              if (!ok) break;
+            }
+            const uint32_t kseq = base + (j + 1) * T + (shared ? 0u : (uint32_t)x);
+            const uint32_t kslot = kseq % C::kSlots;
+            ok = wait_warp(slot_full + kslot, (kseq / C::kSlots) & 1, wd);
+            if (!ok) break;
+            tc_fence_after();
             if (leader) {
               issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
                           dK0 + ((kslot * C::kTileBytes) >> 4), kIdescQK);
               mma_commit(s_full + x);
-              if (!shared || x == nx - 1) mma_commit(slot_empty + kslot);
+              mma_commit(slot_empty + kslot);
+              if (!both) mma_commit(slot_empty + kslot);
+              if (j + 2 == n) {  // the unit's last Q.K^T for this head
+                mma_commit(q_empty);
+                if (nx == 1) mma_commit(q_empty);
+              }
             }
             __syncwarp();
-          } else if (leader) {
-            mma_commit(o_done + x);
+            ++kq;
           }
+          if (j < 0) continue;
+          // O_x += P_x(j) V_j
+          ok = wait_warp(p_full + x, kp & 1, wd);
+          if (!ok) break;
+          if (j == 0) {
+            ok = wait_warp(o_free + x, (o_it & 1) ^ 1, wd);
+            if (!ok) break;
+            ++o_it;
+          }
+          const uint32_t vseq = base + j * T + (shared ? 1u : 2u + x);
+          const uint32_t vslot = vseq % C::kSlots;
+          ok = wait_warp(slot_full + vslot, (vseq / C::kSlots) & 1, wd);
+          if (!ok) break;
+          tc_fence_after();
+          if (leader) {
+            issue_pv<D>(tmem + C::kColO0 + D * x, tmem + C::kColP + 64u * x,
+                        dV0 + ((vslot * C::kTileBytes) >> 4), kIdescPV, j > 0);
+            mma_commit(pv_done + x);
+            mma_commit(slot_empty + vslot);
+            if (!both) mma_commit(slot_empty + vslot);
+            if (j + 1 == n) mma_commit(o_done + x);
+          }
+          __syncwarp();
+          ++kp;
         }
-        if (ok && j + 1 == n - 1 && leader) mma_commit(q_empty);
       }
+      // all products issued by this warp are complete before TMEM is freed
+      uint64_t* dr = x ? drain2 : drain;
+      if (leader) mma_commit(dr);
       __syncwarp();
-      slot_it += n * T;
+      wait_drain(dr, 0);
     }
-    // all products issued by this warp are complete before TMEM is freed
-    if (leader) mma_commit(drain);
-    __syncwarp();
-    wait_drain(drain, 0);
+    if constexpr (!C::kSepP) {
+      // all products issued by this warp are complete before TMEM is freed
+      if (leader) mma_commit(drain);
+      __syncwarp();
+      wait_drain(drain, 0);
+    }
   } else if (warp < 8) {
     // ------------------------------------------------------------- softmax
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
@@ -638,6 +743,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool need_o = redo && j > 0 && m_ref != -INFINITY && m_new > m_ref;
           if (redo && m_new > m_ref) l *= alpha;
           if (__any_sync(0xffffffffu, need_o)) {
+            if constexpr (C::kSepP) {
+              // S(j) was computed before the previous tile's P.V: let it land in O
+              ok = __all_sync(0xffffffffu, wait_bounded(pv_done + x, s_it & 1, wd));
+              if (!ok) break;
+              tc_fence_after();
+            }
             const float a = need_o ? alpha : 1.0f;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -662,8 +773,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         l += tsum;
-        tmem_st32(colS, *reinterpret_cast<uint32_t(*)[32]>(pk));
-        tmem_st32(colS + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
+        uint32_t colP = colS;  // P overwrites S
+        if constexpr (C::kSepP) {
+          // S(j) is read: the next Q.K^T may overwrite it. P goes to its own
+          // columns once the previous tile's P.V product has consumed them.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_free + x);
+          if (s_it > 1) {
+            ok = __all_sync(0xffffffffu, wait_bounded(pv_done + x, s_it & 1, wd));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          colP = tmem + lane_base + C::kColP + 64u * x;
+        }
+        tmem_st32(colP, *reinterpret_cast<uint32_t(*)[32]>(pk));
+        tmem_st32(colP + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
