@@ -711,21 +711,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         // its true maximum, rescaling l and O.
         uint32_t pk[64];
         float tsum = 0.0f;
-        // A unit's first tile has no reference yet (m_ref = -inf in every row):
-        // it goes straight to the max pass below.
-        bool redo = true;
-        if (j > 0) {
+        bool redo;
+        {
           // the second half's load is in flight while the first half is processed
           float v0[64], v1[64];
           load_cols(colS, v0, 2);
           tmem_ld32(colS + 64, *reinterpret_cast<uint32_t(*)[32]>(v1));
           tmem_ld32(colS + 96, *reinterpret_cast<uint32_t(*)[32]>(v1 + 32));
-          transform_cols<SCORE, 64>(v0, 0, tc, m_ref, partial);
-          tsum = exp2_pack<64>(v0, pk);
-          tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(v1));
-          tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(v1 + 32));
-          transform_cols<SCORE, 64>(v1, 64, tc, m_ref, partial);
-          tsum += exp2_pack<64>(v1, pk + 32);
+          if (j == 0) {
+            // A unit's first tile has no reference yet: both halves are
+            // transformed first and the tile's own row maximum becomes the
+            // reference (0 where the whole row is masked), so the largest
+            // weight is exactly 1 as in the max pass below.
+            transform_cols<SCORE, 64>(v0, 0, tc, 0.0f, partial);
+            tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(v1));
+            tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(v1 + 32));
+            transform_cols<SCORE, 64>(v1, 64, tc, 0.0f, partial);
+            const float mt = fmaxf(row_max<64>(v0), row_max<64>(v1));
+            m_ref = mt == -INFINITY ? 0.0f : mt;
+            const float2 sh = make_float2(-m_ref, -m_ref);
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+              const float2 e0 = fadd2(make_float2(v0[c], v0[c + 1]), sh);
+              v0[c] = e0.x;
+              v0[c + 1] = e0.y;
+              const float2 e1 = fadd2(make_float2(v1[c], v1[c + 1]), sh);
+              v1[c] = e1.x;
+              v1[c + 1] = e1.y;
+            }
+            tsum = exp2_pack<64>(v0, pk);
+            tsum += exp2_pack<64>(v1, pk + 32);
+          } else {
+            transform_cols<SCORE, 64>(v0, 0, tc, m_ref, partial);
+            tsum = exp2_pack<64>(v0, pk);
+            tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(v1));
+            tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(v1 + 32));
+            transform_cols<SCORE, 64>(v1, 64, tc, m_ref, partial);
+            tsum += exp2_pack<64>(v1, pk + 32);
+          }
           redo = !(tsum <= 18446744073709551616.0f);
         }
         if (__any_sync(0xffffffffu, redo)) {
