@@ -462,6 +462,46 @@ def run_ours(args, rank: int, world: int) -> None:
     print(json.dumps(line), flush=True)
 
 
+def run_backward(args) -> None:
+    """Diagnostic: the backward of the bf16 causal training workload (B=8,
+    Hq=Hkv=16, S=4096, D=128) after one forward, timed with CUDA events per
+    launch, in TFLOPS of 2.5 x the forward's unmasked FLOPs."""
+    import torch
+
+    import masked_attention_gb300 as M
+    from synth import make_workload
+
+    w = make_workload(5)
+    dev = torch.device("cuda", 0)
+    variant = variant_of(w, M)
+    flops = 2.5 * 4.0 * w.D * kept_pairs(w) * w.Hq
+    q, k, v, do = (t.to(dev) for t in (w.q, w.k, w.v, w.do))
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(M.attn_bwd_workspace_bytes(w.B, w.Hq, w.Sq), dtype=torch.uint8, device=dev)
+    bm = M.build_block_mask(variant & 0xF, w.B, w.Sq, w.Skv, transposed=True)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    M.attn_fwd(q, k, v, o, lse, variant, block_mask=bm)
+    for _ in range(max(args.warmup, 3)):
+        M.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, variant, block_mask=bm)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for s_ in range(args.steps):
+        flush.fill_(s_ & 0xFF)
+        ev[s_][0].record()
+        M.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, variant, block_mask=bm)
+        ev[s_][1].record()
+    torch.cuda.synchronize()
+    if M.attn_check_status() != M.ATTN_OK:
+        raise RuntimeError("device status error during the backward")
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    print(json.dumps({"diagnostic": "backward", "workload": config_dict(w)["workload"],
+                      "ms_per_launch": ms, "flops_per_launch": flops,
+                      "tflops": flops / ms / 1e9, "source_digest": source_digest()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -474,7 +514,12 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override B (profiling cases only)")
     ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[2, 3, 4, 5],
                     help="diagnostic runs on the other bf16 workloads (forward only)")
+    ap.add_argument("--backward", action="store_true",
+                    help="diagnostic: time the backward of the training workload instead")
     args = ap.parse_args()
+    if args.backward:
+        run_backward(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
