@@ -443,7 +443,8 @@ def run_ours(args, rank: int, world: int) -> None:
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak,
                      "unit": "TFLOP/s", "frac": fwd_tflops / peak,
-                     "traffic": profiled_traffic(digest),
+                     "traffic": (profiled_traffic(digest)
+                                 if args.workload == WORKLOAD and not args.batch else None),
                      "kernel": f"fwd_tc_kernel<D={w.D}>",
                      "peak_source": ("measured bf16 dense burst (MEASURED_PEAKS.json)"
                                      if peak_kind == "measured" else "fallback 1.9 PFLOP/s")},

@@ -94,11 +94,13 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(MaskArgs m, 
     MaskArgs m_nodoc = m;
     m_nodoc.variant &= ~ATTN_MASK_DOCUMENT;
     int st = bounds_state(m_nodoc, b, ri, rj, 0, 0, 0, 0);
+    bool doc_uniform = true;  // one document id over the tile's rows and columns
     if (st != kEmpty && doc) {
       int nmin = 0, nmax = 0;
       warp_doc_minmax(doc, rn, nmin, nmax);
       const int qmin = transposed ? nmin : omin, qmax = transposed ? nmax : omax;
       const int kmin = transposed ? omin : nmin, kmax = transposed ? omax : nmax;
+      doc_uniform = qmin == qmax && kmin == kmax && qmin == kmin;
       st = bounds_state(m, b, ri, rj, qmin, qmax, kmin, kmax);
     }
     if (st >= 8) {  // undecided: look at the pairs
@@ -114,11 +116,27 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(MaskArgs m, 
         valid[k] = c < ncols;
         dj[k] = (doc && valid[k]) ? doc[rj.lo + c] : 0;
       }
+      // The rows' document ids too: lane l holds rows l, l+32, l+64, l+96 and
+      // each row's id is shuffled out, so the row loop never waits on memory.
+      int qd[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = ri.lo + lane + 32 * k;
+        qd[k] = (doc && i <= ri.hi) ? doc[i] : 0;
+      }
       const bool causal = m.variant & ATTN_MASK_CAUSAL, window = m.variant & ATTN_MASK_WINDOW;
       const int P = (m.variant & ATTN_MASK_PREFIX) ? m.prefix_len[b] : INT_MIN;
-      bool any_keep = false, any_drop = false;
+      // Where the causal and window terms keep every pair and the prefix none,
+      // a tile whose rows and columns do not all share one document certainly
+      // drops a pair: only a kept pair has to be found, and the scan stops at
+      // the first one instead of looking for a dropped row far down the tile.
+      const bool range_all = (!causal || rj.hi <= ri.lo) && (!window || ri.hi - rj.lo < m.window);
+      const bool prefix_none = rj.lo >= P;
+      bool any_keep = false, any_drop = range_all && prefix_none && !doc_uniform;
       for (int i = ri.lo; i <= ri.hi; ++i) {
-        const int di = doc ? doc[i] : 0;
+        const int r = i - ri.lo, k = r >> 5;
+        const int mine = k == 0 ? qd[0] : k == 1 ? qd[1] : k == 2 ? qd[2] : qd[3];
+        const int di = __shfl_sync(0xffffffffu, mine, r & 31);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int j = rj.lo + lane + 32 * k;
