@@ -66,6 +66,13 @@ struct Cfg {
   // rest of its work. At D = 128 the 512 columns hold S_A, S_B, O_A, O_B and P
   // overwrites S, so the next Q.K^T waits for the P.V product.
   static constexpr bool kSepP = D == 64;
+  // One MMA warp per head at D = 64: the tensor pipe queues about one product,
+  // so a single issuer leaves it idle whenever it waits or commits; with two,
+  // one head's products run while the other's issuer waits. At D = 128 (P
+  // over S) a single issuer alternating heads keeps the two heads' softmax
+  // phases apart, which matters more there: with two issuers they align and
+  // contend for the special-function unit (soft-cap: 1.38 -> 1.84 ms measured).
+  static constexpr bool kDualMma = kSepP;
   static constexpr uint32_t kColP = 384;
   static_assert(!kSepP || kColP + 128 <= 512, "tensor memory columns");
   static_assert(kOffDoc % 16 == 0 && (kTile * 4) % 16 == 0, "int4 reads of document ids");
@@ -345,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ring slot is released by two commits (one per warp, or two by the one
     // warp that used it).
     mbar_init(q_full, 1);
-    mbar_init(q_empty, C::kSepP ? 2 : 1);
+    mbar_init(q_empty, C::kDualMma ? 2 : 1);
     mbar_init(drain, 1);
     mbar_init(drain2, 1);
     for (int x = 0; x < 2; ++x) {
@@ -358,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(slot_full + s, 1);
-      mbar_init(slot_empty + s, C::kSepP ? 2 : 1);
+      mbar_init(slot_empty + s, C::kDualMma ? 2 : 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -443,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (q_it > 0) wait_drain(q_full, (q_it - 1) & 1);
     }
-  } else if (warp == kWarpMma || (C::kSepP && warp == kWarpMma2)) {
+  } else if (warp == kWarpMma || (C::kDualMma && warp == kWarpMma2)) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop (waits stay converged); lane 0 issues the
     // products and the commits. Loop state stays in registers and the
@@ -455,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t dK0 = sdesc_sw128(smem_u32(sSlots), 16, 1024);
     const uint64_t dV0 = sdesc_sw128(smem_u32(sSlots), C::kBoxBytes, 1024);
-    if constexpr (!C::kSepP) {
+    if constexpr (!C::kDualMma) {
       uint32_t slot_it = 0, q_it = 0, p_it0 = 0, p_it1 = 0, o_it0 = 0, o_it1 = 0;
       bool ok = true;
       for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
@@ -565,55 +572,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool both = nx == 2 && shared;  // the other warp releases the same slots
         ok = wait_warp(q_full, (q_it - 1) & 1, wd);
         if (!ok) break;
-        for (int j = -1; j < n && ok; ++j) {
-          if (j + 1 < n) {  // S_x(j+1)
-            if (kq > 0) {
-              ok = wait_warp(s_free + x, (kq - 1) & 1, wd);
-              if (!ok) break;
-            }
-            const uint32_t kseq = base + (j + 1) * T + (shared ? 0u : (uint32_t)x);
-            const uint32_t kslot = kseq % C::kSlots;
-            ok = wait_warp(slot_full + kslot, (kseq / C::kSlots) & 1, wd);
-            if (!ok) break;
-            tc_fence_after();
-            if (leader) {
-              issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
-                          dK0 + ((kslot * C::kTileBytes) >> 4), kIdescQK);
-              mma_commit(s_full + x);
-              mma_commit(slot_empty + kslot);
-              if (!both) mma_commit(slot_empty + kslot);
-              if (j + 2 == n) {  // the unit's last Q.K^T for this head
-                mma_commit(q_empty);
-                if (nx == 1) mma_commit(q_empty);
-              }
-            }
-            __syncwarp();
-            ++kq;
+        // S_x(jj) = Q_x K_jj^T
+        auto do_qk = [&](int jj) -> bool {
+          if constexpr (C::kSepP) {
+            if (kq > 0 && !wait_warp(s_free + x, (kq - 1) & 1, wd)) return false;
           }
-          if (j < 0) continue;
-          // O_x += P_x(j) V_j
-          ok = wait_warp(p_full + x, kp & 1, wd);
-          if (!ok) break;
-          if (j == 0) {
-            ok = wait_warp(o_free + x, (o_it & 1) ^ 1, wd);
-            if (!ok) break;
-            ++o_it;
-          }
-          const uint32_t vseq = base + j * T + (shared ? 1u : 2u + x);
-          const uint32_t vslot = vseq % C::kSlots;
-          ok = wait_warp(slot_full + vslot, (vseq / C::kSlots) & 1, wd);
-          if (!ok) break;
+          const uint32_t kseq = base + jj * T + (shared ? 0u : (uint32_t)x);
+          const uint32_t kslot = kseq % C::kSlots;
+          if (!wait_warp(slot_full + kslot, (kseq / C::kSlots) & 1, wd)) return false;
           tc_fence_after();
           if (leader) {
-            issue_pv<D>(tmem + C::kColO0 + D * x, tmem + C::kColP + 64u * x,
-                        dV0 + ((vslot * C::kTileBytes) >> 4), kIdescPV, j > 0);
-            mma_commit(pv_done + x);
+            issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
+                        dK0 + ((kslot * C::kTileBytes) >> 4), kIdescQK);
+            mma_commit(s_full + x);
+            mma_commit(slot_empty + kslot);
+            if (!both) mma_commit(slot_empty + kslot);
+            if (jj + 1 == n) {  // the unit's last Q.K^T for this head
+              mma_commit(q_empty);
+              if (nx == 1) mma_commit(q_empty);
+            }
+          }
+          __syncwarp();
+          ++kq;
+          return true;
+        };
+        // O_x += P_x(jj) V_jj
+        auto do_pv = [&](int jj) -> bool {
+          if (!wait_warp(p_full + x, kp & 1, wd)) return false;
+          if (jj == 0) {
+            if (!wait_warp(o_free + x, (o_it & 1) ^ 1, wd)) return false;
+            ++o_it;
+          }
+          const uint32_t vseq = base + jj * T + (shared ? 1u : 2u + x);
+          const uint32_t vslot = vseq % C::kSlots;
+          if (!wait_warp(slot_full + vslot, (vseq / C::kSlots) & 1, wd)) return false;
+          tc_fence_after();
+          if (leader) {
+            const uint32_t pcol = C::kSepP ? C::kColP + 64u * x : 128u * x;
+            issue_pv<D>(tmem + C::kColO0 + D * x, tmem + pcol,
+                        dV0 + ((vslot * C::kTileBytes) >> 4), kIdescPV, jj > 0);
+            if (C::kSepP) mma_commit(pv_done + x);
             mma_commit(slot_empty + vslot);
             if (!both) mma_commit(slot_empty + vslot);
-            if (j + 1 == n) mma_commit(o_done + x);
+            if (jj + 1 == n) mma_commit(o_done + x);
           }
           __syncwarp();
           ++kp;
+          return true;
+        };
+        if constexpr (C::kSepP) {
+          // separate P: S_x(j+1) as soon as S_x(j) is read, then P_x(j) V_j
+          for (int j = -1; j < n && ok; ++j) {
+            if (j + 1 < n) ok = do_qk(j + 1);
+            if (ok && j >= 0) ok = do_pv(j);
+          }
+        } else {
+          // P overwrites S: S_x(j+1) only after P_x(j) V_j has been issued
+          ok = do_qk(0);
+          for (int j = 0; j < n && ok; ++j) {
+            ok = do_pv(j);
+            if (ok && j + 1 < n) ok = do_qk(j + 1);
+          }
         }
       }
       // all products issued by this warp are complete before TMEM is freed
@@ -622,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       wait_drain(dr, 0);
     }
-    if constexpr (!C::kSepP) {
+    if constexpr (!C::kDualMma) {
       // all products issued by this warp are complete before TMEM is freed
       if (leader) mma_commit(drain);
       __syncwarp();
