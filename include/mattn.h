@@ -138,9 +138,11 @@ typedef struct attn_params {
  *   lse fp32 [B,Hq,Sq] (natural log; -inf for a row with no kept key, whose
  *   O row is 0).
  * Supported: D in {64, 128}; Hq % Hkv == 0 (GQA: query head h reads key/value
- * head h / (Hq/Hkv)); ATTN_BF16 needs Sq and Skv multiples of 128 (tcgen05
- * tensor-core kernel); ATTN_F32 takes any Sq, Skv >= 1 (fp32 FFMA kernel).
- * Returns ATTN_ERR_UNSUPPORTED for anything else. */
+ * head h / (Hq/Hkv)); any Sq, Skv >= 1 for both ATTN_BF16 (tcgen05
+ * tensor-core kernel: a last tile that runs past Sq or Skv reads zero-filled
+ * rows, its extra keys are masked and its extra query rows are not stored)
+ * and ATTN_F32 (fp32 FFMA kernel). Returns ATTN_ERR_UNSUPPORTED for anything
+ * else. */
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                      int B, int Hq, int Hkv, int Sq, int Skv, int D,
                      unsigned variant, const attn_params* p, struct CUstream_st* stream);

@@ -243,7 +243,6 @@ MATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void
     return ATTN_ERR_MISALIGNED;
   st = check_block_mask(p->block_mask, variant, p, B, Sq, Skv, false);
   if (st != ATTN_OK) return st;
-  if (p->dtype == ATTN_BF16 && (Sq % kTile != 0 || Skv % kTile != 0)) return ATTN_ERR_UNSUPPORTED;
   st = resolve_status(f);
   if (st != ATTN_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

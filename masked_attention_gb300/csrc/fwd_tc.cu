@@ -109,7 +109,7 @@ __device__ __forceinline__ int zigzag_unit(int r) {
 }
 
 __device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp) {
-  const int nq = p.Sq / kTile, nkv = p.Skv / kTile;
+  const int nq = (p.Sq + kTile - 1) / kTile, nkv = (p.Skv + kTile - 1) / kTile;
   const int rank = u / nhp, hp = u % nhp;
   const bool causal_bound = (p.variant & ATTN_MASK_CAUSAL) && !(p.variant & ATTN_MASK_PREFIX);
   int row;
@@ -138,6 +138,12 @@ __device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp)
     U.lf = U.lp = nullptr;
   }
   return U;
+}
+
+// Document id of key j, or -1 past the end of the keys (those columns are
+// masked by the key-length bound anyway).
+__device__ __forceinline__ int doc_at(const int* docb, int j, int Skv) {
+  return j < Skv ? docb[j] : -1;
 }
 
 // Per-row, per-tile constants of the score transform.
@@ -385,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_base_smem;
 
   const int nhp = (p.Hq + 1) / 2;
-  const int num_units = p.B * (p.Sq / kTile) * nhp;
+  const int num_units = p.B * ((p.Sq + kTile - 1) / kTile) * nhp;
   const int group = p.Hq / p.Hkv;
 
   if (warp >= 8) {
@@ -412,17 +418,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) {
         mbar_arrive_expect_tx(q_full, (two ? 2 : 1) * C::kTileBytes);
         for (int x = 0; x < (two ? 2 : 1); ++x) {
-          const int row = (U.b * p.Hq + U.h[x]) * p.Sq + U.qt * kTile;
+          const int slice = U.b * p.Hq + U.h[x];
           for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_2d(sQ + x * C::kTileBytes + bx * C::kBoxBytes, &tm_q, q_full, bx * 64, row);
+            tma_load_3d(sQ + x * C::kTileBytes + bx * C::kBoxBytes, &tm_q, q_full, bx * 64,
+                        U.qt * kTile, slice);
         }
       }
       __syncwarp();
       ++q_it;
       for (int j = 0; j < n && ok; ++j) {
         const int kt = U.kt(j);
-        const int rows[2] = {(U.b * p.Hkv + hk0) * p.Skv + kt * kTile,
-                             (U.b * p.Hkv + hk1) * p.Skv + kt * kTile};
+        const int slices[2] = {U.b * p.Hkv + hk0, U.b * p.Hkv + hk1};
         // order: K_A, [K_B], V_A, [V_B]
         for (int t = 0; t < (shared ? 2 : 4) && ok; ++t) {
           const int per = shared ? 1 : 2;
@@ -435,8 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (leader) {
             mbar_arrive_expect_tx(slot_full + slot, C::kTileBytes);
             for (int bx = 0; bx < C::kBoxes; ++bx)
-              tma_load_2d(sSlots + slot * C::kTileBytes + bx * C::kBoxBytes, is_v ? &tm_v : &tm_k,
-                          slot_full + slot, bx * 64, rows[x]);
+              tma_load_3d(sSlots + slot * C::kTileBytes + bx * C::kBoxBytes, is_v ? &tm_v : &tm_k,
+                          slot_full + slot, bx * 64, kt * kTile, slices[x]);
           }
           __syncwarp();
           ++slot_it;
@@ -669,19 +675,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (h < 0) continue;
       const int n = U.n();
       const int i = U.qt * kTile + t;
+      const bool row_in = i < p.Sq;  // a last query tile may run past Sq
       const size_t orow = ((size_t)(U.b * p.Hq + h) * p.Sq + i);
       __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + orow * D;
       if (n == 0) {
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(O)[c] = z;
-        p.lse[orow] = -INFINITY;
+        if (row_in) {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(O)[c] = z;
+          p.lse[orow] = -INFINITY;
+        }
         continue;
       }
       const float slope = (SCORE & 1) ? alibi_slope(p.score, h) : 0.0f;
       const float slope2 = slope * kLog2e;
       const int* docb = (p.variant & ATTN_MASK_DOCUMENT)
                             ? p.mask.doc_id + (size_t)U.b * p.mask.doc_len : nullptr;
-      const int doc_i = docb ? docb[i] : 0;
+      const int doc_i = (docb && row_in) ? docb[i] : 0;
       const int P = (p.variant & ATTN_MASK_PREFIX) ? p.mask.prefix_len[U.b] : INT_MIN;
       float m_ref = -INFINITY, l = 0.0f;
       // Key-tile indices are read two tiles ahead and the document ids of a
@@ -691,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int dcur[4] = {0, 0, 0, 0};
       if (docb && U.partial(0)) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) dcur[c] = docb[kt_cur * kTile + lane + 32 * c];
+        for (int c = 0; c < 4; ++c) dcur[c] = doc_at(docb, kt_cur * kTile + lane + 32 * c, p.Skv);
       }
 
       for (int j = 0; j < n; ++j) {
@@ -700,10 +709,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         int dnext[4] = {0, 0, 0, 0};
         if (docb && j + 1 < n && U.partial(j + 1)) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) dnext[c] = docb[kt_n1 * kTile + lane + 32 * c];
+          for (int c = 0; c < 4; ++c) dnext[c] = doc_at(docb, kt_n1 * kTile + lane + 32 * c, p.Skv);
         }
         const int j0 = kt * kTile;
-        const bool partial = U.partial(j);
+        // a key tile that runs past Skv is masked like a partial tile: its
+        // columns from Skv - j0 on hold zero-filled keys
+        const bool tail = j0 + kTile > p.Skv;
+        const bool partial = U.partial(j) || tail;
         if (partial && docb) {
           __syncwarp();
 #pragma unroll
@@ -715,9 +727,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) dcur[c] = dnext[c];
         TileCtx tc{sl2, sc, cl2, slope, slope2, p.score.scale, 1.0f / p.score.softcap,
-                   float(j0 - i), (p.variant & ATTN_MASK_CAUSAL) ? i - j0 : INT_MAX,
+                   float(j0 - i),
+                   min((p.variant & ATTN_MASK_CAUSAL) ? i - j0 : INT_MAX, p.Skv - 1 - j0),
                    (p.variant & ATTN_MASK_WINDOW) ? i - j0 - p.mask.window : INT_MIN,
-                   P == INT_MIN ? INT_MIN : P - j0, docb ? wdoc : nullptr, doc_i, 0u};
+                   P == INT_MIN ? INT_MIN : min(P, p.Skv) - j0, docb ? wdoc : nullptr, doc_i,
+                   0u};
         if (partial) tc.modes = chunk_modes(tc);  // before the wait: off the critical path
         ok = __all_sync(0xffffffffu, wait_bounded(s_full + x, s_it & 1, wd));
         if (!ok) break;
@@ -853,14 +867,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e)
           pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
         uint4* dst = reinterpret_cast<uint4*>(O + 32 * c);
+        if (row_in) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free + x);
-      p.lse[orow] = l > 0.0f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      if (row_in) p.lse[orow] = l > 0.0f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -878,9 +894,9 @@ template <int D, int SCORE>
 cudaError_t launch_typed(const FwdProblem& p, cudaStream_t stream) {
   using C = Cfg<D>;
   CUtensorMap mq, mk, mv;
-  if (!make_map_bf16(&mq, p.q, (long long)p.B * p.Hq * p.Sq, D) ||
-      !make_map_bf16(&mk, p.k, (long long)p.B * p.Hkv * p.Skv, D) ||
-      !make_map_bf16(&mv, p.v, (long long)p.B * p.Hkv * p.Skv, D))
+  if (!make_map_bf16_3d(&mq, p.q, (long long)p.B * p.Hq, p.Sq, D) ||
+      !make_map_bf16_3d(&mk, p.k, (long long)p.B * p.Hkv, p.Skv, D) ||
+      !make_map_bf16_3d(&mv, p.v, (long long)p.B * p.Hkv, p.Skv, D))
     return cudaErrorInvalidValue;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -889,7 +905,7 @@ cudaError_t launch_typed(const FwdProblem& p, cudaStream_t stream) {
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const int units = p.B * (p.Sq / kTile) * ((p.Hq + 1) / 2);
+  const int units = p.B * ((p.Sq + kTile - 1) / kTile) * ((p.Hq + 1) / 2);
   const int grid = units < sm_count() ? units : sm_count();
   if (grid == 0) return cudaSuccess;
   fwd_tc_kernel<D, SCORE><<<grid, kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, p);

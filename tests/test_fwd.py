@@ -111,6 +111,35 @@ BF16_CASES = {
 }
 
 
+# bf16 with sequence lengths that are not multiples of the 128-row tile: the
+# last query tile runs past Sq (rows not stored) and the last key tile past
+# Skv (zero-filled keys masked), for every mask term and score_mod.
+BF16_RAGGED = {
+    "causal_alibi_d64_s300": dict(B=2, Hq=2, Hkv=2, S=300, D=64, causal=True, alibi=True),
+    "full_d128_q100_k389": dict(B=1, Hq=2, Hkv=1, Sq=100, Skv=389, D=128),
+    "doc_window_d128_s333": dict(B=1, Hq=2, Hkv=2, S=333, D=128, causal=True, window=90,
+                                 document=True, doc_lo=20, doc_hi=150),
+    "prefix_softcap_gqa_d64_q257_k129": dict(B=2, Hq=4, Hkv=2, Sq=257, Skv=129, D=64,
+                                             causal=True, prefix=True, softcap=5.0,
+                                             prefix_lo=60, prefix_hi=300),
+    "single_row_d128": dict(B=1, Hq=1, Hkv=1, Sq=1, Skv=1, D=128, causal=True),
+    "window_empty_rows_d64": dict(B=1, Hq=2, Hkv=2, Sq=140, Skv=7, D=64, causal=True,
+                                  window=3),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BF16_RAGGED))
+def test_bf16_ragged(name):
+    w = make_workload(0, seed=400 + sorted(BF16_RAGGED).index(name), **BF16_RAGGED[name])
+    run_and_check(w)
+
+
+@pytest.mark.parametrize("name", ["causal_alibi_d64_s300", "full_d128_q100_k389"])
+def test_bf16_ragged_without_block_mask(name):
+    w = make_workload(0, seed=400 + sorted(BF16_RAGGED).index(name), **BF16_RAGGED[name])
+    run_and_check(w, use_block_mask=False)
+
+
 @pytest.mark.parametrize("name", sorted(BF16_CASES))
 def test_bf16_reduced(name):
     w = make_workload(0, seed=300 + sorted(BF16_CASES).index(name), **BF16_CASES[name])
