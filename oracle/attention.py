@@ -55,6 +55,10 @@ class Spec:
     alibi_slopes: Optional[np.ndarray] = None  # [Hq]; None -> 2**(-8(h+1)/Hq)
     softcap: Optional[float] = None
     scale: Optional[float] = None           # None -> 1/sqrt(D)
+    # relative-position bias table [Hq, Sq + Skv - 1]; entry d + rel_bias_zero
+    # is added for query-key distance d = i - j (rel_bias_zero = Skv - 1)
+    rel_bias: Optional[np.ndarray] = None
+    rel_bias_zero: int = 0
 
 
 def alibi_slopes(Hq: int) -> np.ndarray:
@@ -92,10 +96,21 @@ def score_mod(spec: Spec, s: np.ndarray, h: int, Hq: int, i: np.ndarray,
     if spec.alibi:
         slopes = spec.alibi_slopes if spec.alibi_slopes is not None else alibi_slopes(Hq)
         out = out - float(slopes[h]) * (np.asarray(i, np.float64) - np.asarray(j, np.float64))
+    if spec.rel_bias is not None:
+        out = out + rel_bias_term(spec, h, i, j)
     if spec.softcap is not None:
         c = float(spec.softcap)
         out = c * np.tanh(out / c)
     return out
+
+
+def rel_bias_term(spec: Spec, h: int, i: np.ndarray, j: np.ndarray) -> np.ndarray:
+    """Relative-position bias: a per-head table indexed by the query-key
+    distance i - j (FlexAttention page, relative position encoding: the score
+    is adjusted by the distance between query and key, computed in the kernel
+    without an S x S tensor). The table is a captured buffer of the call."""
+    d = np.asarray(i, np.int64) - np.asarray(j, np.int64)
+    return np.asarray(spec.rel_bias[h], np.float64)[d + spec.rel_bias_zero]
 
 
 def score_mod_grad(spec: Spec, s: np.ndarray, h: int, Hq: int, i: np.ndarray,
@@ -108,6 +123,8 @@ def score_mod_grad(spec: Spec, s: np.ndarray, h: int, Hq: int, i: np.ndarray,
     if spec.alibi:
         slopes = spec.alibi_slopes if spec.alibi_slopes is not None else alibi_slopes(Hq)
         x = x - float(slopes[h]) * (np.asarray(i, np.float64) - np.asarray(j, np.float64))
+    if spec.rel_bias is not None:
+        x = x + rel_bias_term(spec, h, i, j)
     t = np.tanh(x / float(spec.softcap))
     return 1.0 - t * t
 

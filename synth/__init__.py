@@ -65,6 +65,7 @@ class Workload:
     alibi: bool = False
     softcap: Optional[float] = None
     backward: bool = False
+    relbias: bool = False                    # relative-position bias table on
     seed: int = 0
     doc_lengths: Optional[list] = None       # per batch element
     doc_id: Optional[np.ndarray] = None      # int32 [B, max(Sq, Skv)]
@@ -73,11 +74,12 @@ class Workload:
     k: Optional[torch.Tensor] = None
     v: Optional[torch.Tensor] = None
     do: Optional[torch.Tensor] = None
+    rel_bias: Optional[torch.Tensor] = None  # fp32 [Hq, Sq + Skv - 1], entry i - j + Skv - 1
 
     def describe(self) -> dict:
         out = dict(name=self.name, dtype=self.dtype, B=self.B, Hq=self.Hq, Hkv=self.Hkv,
                    Sq=self.Sq, Skv=self.Skv, D=self.D, seed=self.seed)
-        for key in ("causal", "document", "prefix", "alibi", "backward"):
+        for key in ("causal", "document", "prefix", "alibi", "backward", "relbias"):
             if getattr(self, key):
                 out[key] = True
         if self.window is not None:
@@ -135,7 +137,8 @@ def make_workload(number: int = 0, *, seed: Optional[int] = None, with_tensors: 
                  Hkv=Hkv, Sq=Sq, Skv=Skv, D=D, causal=spec.get("causal", False),
                  window=spec.get("window"), document=spec.get("document", False),
                  prefix=spec.get("prefix", False), alibi=spec.get("alibi", False),
-                 softcap=spec.get("softcap"), backward=spec.get("backward", False), seed=seed)
+                 softcap=spec.get("softcap"), backward=spec.get("backward", False),
+                 relbias=spec.get("relbias", False), seed=seed)
     rng = np.random.default_rng(seed)
     L = max(Sq, Skv)
     if w.document:
@@ -161,5 +164,7 @@ def make_workload(number: int = 0, *, seed: Optional[int] = None, with_tensors: 
         w.v = torch.randn(B, Hkv, Skv, D, dtype=torch.float32, generator=g).to(tdtype)
         if w.backward:
             w.do = torch.randn(B, Hq, Sq, D, dtype=torch.float32, generator=g).to(tdtype)
+        if w.relbias:  # drawn last: the other tensors do not depend on it
+            w.rel_bias = torch.randn(Hq, Sq + Skv - 1, dtype=torch.float32, generator=g)
     return w
 

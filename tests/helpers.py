@@ -9,7 +9,9 @@ def oracle_spec(w, **extra) -> Spec:
     return Spec(causal=w.causal, window=w.window,
                 doc_id=w.doc_id if w.document else None,
                 prefix_len=w.prefix_len if w.prefix else None,
-                alibi=w.alibi, softcap=w.softcap, **extra)
+                alibi=w.alibi, softcap=w.softcap,
+                rel_bias=w.rel_bias.double().numpy() if w.rel_bias is not None else None,
+                rel_bias_zero=w.Skv - 1, **extra)
 
 
 def max_abs(a, b) -> float:
@@ -36,6 +38,8 @@ def variant_bits(w) -> int:
         v |= M.SCORE_ALIBI
     if w.softcap is not None:
         v |= M.SCORE_SOFTCAP
+    if w.relbias:
+        v |= M.SCORE_RELBIAS
     return v
 
 
@@ -55,6 +59,7 @@ class GpuRun:
         self.variant = variant_bits(w)
         self.window = w.window or 0
         self.softcap = w.softcap or 0.0
+        self.rel_bias = w.rel_bias.to(dev).contiguous() if w.rel_bias is not None else None
         self.bm = None
         if use_block_mask:
             self.bm = M.build_block_mask(self.variant & 0xF, w.B, w.Sq, w.Skv,
@@ -62,8 +67,11 @@ class GpuRun:
                                          prefix_len=self.prefix_len, transposed=transposed)
 
     def kwargs(self):
-        return dict(window=self.window, softcap=self.softcap, doc_id=self.doc_id,
-                    prefix_len=self.prefix_len, block_mask=self.bm)
+        kw = dict(window=self.window, softcap=self.softcap, doc_id=self.doc_id,
+                  prefix_len=self.prefix_len, block_mask=self.bm)
+        if self.rel_bias is not None:
+            kw["rel_bias"] = self.rel_bias
+        return kw
 
     def fwd(self, o=None, lse=None):
         import torch

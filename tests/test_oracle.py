@@ -34,7 +34,7 @@ def rnd(shape, seed):
 # ---------------------------------------------------------------------------
 
 def brute_force(q, k, v, causal=False, window=None, doc=None, prefix=None, alibi=False,
-                softcap=None):
+                softcap=None, table=None):
     B, Hq, Sq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
     group = Hq // Hkv
@@ -54,6 +54,8 @@ def brute_force(q, k, v, causal=False, window=None, doc=None, prefix=None, alibi
                     sc = dot * scale
                     if alibi:
                         sc = sc + slope * (kj - qi)
+                    if table is not None:  # bias by the query-key distance
+                        sc = sc + float(table[h][qi - kj + Skv - 1])
                     if softcap is not None:
                         sc = softcap * math.tanh(sc / softcap)
                     ok = True
@@ -89,6 +91,8 @@ BF_CASES = [
     dict(causal=True, prefix=[4, 7], softcap=2.0),
     dict(alibi=True, softcap=1.5),
     dict(window=2),
+    dict(causal=True, table="rel"),
+    dict(alibi=True, softcap=2.5, table="rel", window=5),
 ]
 
 
@@ -100,11 +104,16 @@ def test_oracle_matches_brute_force(case, heads):
     q = rnd((B, Hq, S, D), 1)
     k = rnd((B, Hkv, S, D), 2)
     v = rnd((B, Hkv, S, D), 3)
-    O_ref, L_ref = brute_force(q, k, v, **case)
+    case = dict(case)
+    table = None
+    if case.pop("table", None):
+        table = rnd((Hq, 2 * S - 1), 11)
+    O_ref, L_ref = brute_force(q, k, v, table=table, **case)
     spec = Spec(causal=case.get("causal", False), window=case.get("window"),
                 doc_id=np.array(case["doc"]) if "doc" in case else None,
                 prefix_len=np.array(case["prefix"]) if "prefix" in case else None,
-                alibi=case.get("alibi", False), softcap=case.get("softcap"))
+                alibi=case.get("alibi", False), softcap=case.get("softcap"),
+                rel_bias=table, rel_bias_zero=S - 1)
     O, L = attention_forward(q, k, v, spec)
     assert np.max(np.abs(O - O_ref)) < 1e-12
     assert np.max(np.abs(L - L_ref)) < 1e-12
@@ -468,3 +477,57 @@ def test_workload_recipe_shapes():
     assert all(256 <= n <= 4096 for n in w.doc_lengths[0][:-1])
     w4 = make_workload(4, with_tensors=False)
     assert w4.prefix_len.shape == (2,) and all(512 <= p <= 4096 for p in w4.prefix_len)
+
+
+# ---------------------------------------------------------------------------
+# Relative-position bias (FlexAttention page, relative position encoding):
+# special cases and invariants of the distance-indexed table.
+# ---------------------------------------------------------------------------
+
+def test_rel_bias_table_of_alibi_equals_alibi():
+    """ALiBi is the table T[h][d] = -slope_h * d over the distance d = i - j."""
+    B, Hq, Sq, Skv, D = 1, 4, 23, 31, 8
+    q, k, v = rnd((B, Hq, Sq, D), 21), rnd((B, Hq, Skv, D), 22), rnd((B, Hq, Skv, D), 23)
+    d = np.arange(-(Skv - 1), Sq)
+    table = -alibi_slopes(Hq)[:, None] * d[None, :]
+    for causal in (False, True):
+        O1, L1 = attention_forward(q, k, v, Spec(causal=causal, alibi=True))
+        O2, L2 = attention_forward(q, k, v, Spec(causal=causal, rel_bias=table,
+                                                 rel_bias_zero=Skv - 1))
+        assert np.max(np.abs(O1 - O2)) < 1e-12
+        assert np.max(np.abs(L1 - L2)) < 1e-12
+
+
+def test_rel_bias_constant_table_shifts_lse_only():
+    """A constant bias c leaves O unchanged and adds c to the LSE (softmax is
+    shift-invariant)."""
+    q, k, v = rnd((2, 2, 17, 8), 24), rnd((2, 2, 17, 8), 25), rnd((2, 2, 17, 8), 26)
+    c = 1.75
+    O1, L1 = attention_forward(q, k, v, Spec(causal=True))
+    O2, L2 = attention_forward(q, k, v, Spec(causal=True, rel_bias=np.full((2, 33), c),
+                                             rel_bias_zero=16))
+    assert np.max(np.abs(O1 - O2)) < 1e-12
+    assert np.max(np.abs(L2 - L1 - c)) < 1e-12
+
+
+def test_rel_bias_gradient_matches_finite_differences():
+    """The table is a constant of the call: dQ, dK, dV follow from the biased
+    scores (central differences of the forward)."""
+    B, H, S, D = 1, 2, 6, 3
+    q, k, v, do = (rnd((B, H, S, D), 30 + t) for t in range(4))
+    spec = Spec(causal=True, softcap=2.0, rel_bias=rnd((H, 2 * S - 1), 34), rel_bias_zero=S - 1)
+    dq, dk, dv, _, _ = attention_backward(q, k, v, do, spec)
+
+    def loss(q_, k_, v_):
+        O, _ = attention_forward(q_, k_, v_, spec)
+        return float(np.sum(O * do))
+
+    h = 1e-6
+    for X, G, idx in ((q, dq, (0, 1, 4, 2)), (k, dk, (0, 0, 2, 1)), (v, dv, (0, 1, 3, 0))):
+        Xp, Xm = X.copy(), X.copy()
+        Xp[idx] += h
+        Xm[idx] -= h
+        args_p = [Xp if Y is X else Y for Y in (q, k, v)]
+        args_m = [Xm if Y is X else Y for Y in (q, k, v)]
+        fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        assert abs(fd - G[idx]) < 1e-6 * max(1.0, abs(fd))
