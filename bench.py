@@ -69,7 +69,7 @@ def read_peaks():
 
 def source_digest() -> str:
     h = hashlib.sha256()
-    for name in ("fwd_tc.cu", "common.cuh"):
+    for name in ("fwd_tc_kernel.cuh", "fwd_tc.cu", "common.cuh"):
         with open(os.path.join(ROOT, "masked_attention_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -310,6 +310,7 @@ def variant_of(w, M):
     v |= M.MASK_PREFIX if w.prefix else 0
     v |= M.SCORE_ALIBI if w.alibi else 0
     v |= M.SCORE_SOFTCAP if w.softcap is not None else 0
+    v |= M.SCORE_RELBIAS if w.relbias else 0
     return v
 
 
@@ -317,7 +318,8 @@ def config_dict(w):
     terms = [t for t, on in (("causal", w.causal), (f"window {w.window}", w.window is not None),
                              ("document", w.document), ("prefix", w.prefix),
                              ("ALiBi slope_h = 2^(-8(h+1)/H)", w.alibi),
-                             (f"soft-cap {w.softcap}", w.softcap is not None)) if on]
+                             (f"soft-cap {w.softcap}", w.softcap is not None),
+                             ("relative-position bias table", w.relbias)) if on]
     return {"workload": f"{w.name} attention forward, B={w.B} Hq={w.Hq} Hkv={w.Hkv} "
                         f"S={w.Sq} D={w.D}",
             "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.Sq, "D": w.D,
@@ -336,7 +338,10 @@ def run_ours(args, rank: int, world: int) -> None:
     local = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = make_workload(args.workload, **({"B": args.batch} if args.batch else {}))
+    over = {"B": args.batch} if args.batch else {}
+    if args.relbias:
+        over["relbias"] = True
+    w = make_workload(args.workload, **over)
     variant = variant_of(w, M)
     pairs = kept_pairs(w)
     flops = 4.0 * w.D * pairs * w.Hq  # per step, whole batch
@@ -353,6 +358,8 @@ def run_ours(args, rank: int, world: int) -> None:
     pre = torch.from_numpy(w.prefix_len).to(dev) if w.prefix else None
     mkw = dict(window=w.window or 0, doc_id=doc, prefix_len=pre)
     fkw = dict(mkw, softcap=w.softcap or 0.0)
+    if w.relbias:
+        fkw["rel_bias"] = w.rel_bias.to(dev)
 
     def step():
         bm = M.build_block_mask(variant & 0xF, w.B, w.Sq, w.Skv, buf=bm_buf, stream=stream, **mkw)
@@ -444,7 +451,8 @@ def run_ours(args, rank: int, world: int) -> None:
         "roofline": {"bound": "tensor", "achieved": fwd_tflops, "peak": peak,
                      "unit": "TFLOP/s", "frac": fwd_tflops / peak,
                      "traffic": (profiled_traffic(digest)
-                                 if args.workload == WORKLOAD and not args.batch else None),
+                                 if args.workload == WORKLOAD and not args.batch
+                                 and not args.relbias else None),
                      "kernel": f"fwd_tc_kernel<D={w.D}>",
                      "peak_source": ("measured bf16 dense burst (MEASURED_PEAKS.json)"
                                      if peak_kind == "measured" else "fallback 1.9 PFLOP/s")},
@@ -515,6 +523,8 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override B (profiling cases only)")
     ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[2, 3, 4, 5],
                     help="diagnostic runs on the other bf16 workloads (forward only)")
+    ap.add_argument("--relbias", action="store_true",
+                    help="diagnostic: add a relative-position bias table to the workload")
     ap.add_argument("--backward", action="store_true",
                     help="diagnostic: time the backward of the training workload instead")
     args = ap.parse_args()

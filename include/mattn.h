@@ -61,17 +61,21 @@ typedef enum attn_status {
  * with absent AND-terms true and an absent PREFIX false. i and j are absolute
  * positions (query row i, key column j), aligned at 0.
  * Score terms apply in this order: s <- scale * q.k; ALIBI: s <- s - slope_h
- * * (i - j); SOFTCAP: s <- softcap * tanh(s / softcap). */
+ * * (i - j); RELBIAS: s <- s + rel_bias[h][i - j + Skv - 1]; SOFTCAP:
+ * s <- softcap * tanh(s / softcap). */
 enum {
   ATTN_MASK_CAUSAL = 1u << 0,   /* FlexAttention page, "Causal Mask" */
   ATTN_MASK_WINDOW = 1u << 1,   /* "Sliding Window + Causal" (1024 tokens there) */
   ATTN_MASK_DOCUMENT = 1u << 2, /* variant list: document masking */
   ATTN_MASK_PREFIX = 1u << 3,   /* variant list: PrefixLM (prefix is bidirectional) */
   ATTN_SCORE_ALIBI = 1u << 8,   /* variant list: ALiBi; slope_h = 2^(-8(h+1)/Hq) */
-  ATTN_SCORE_SOFTCAP = 1u << 9  /* "Soft-capping" section (Gemma 2, Grok-1) */
+  ATTN_SCORE_SOFTCAP = 1u << 9, /* "Soft-capping" section (Gemma 2, Grok-1) */
+  ATTN_SCORE_RELBIAS = 1u << 10 /* relative position encoding: the score is adjusted by
+                                   the query-key distance, from a per-head table the
+                                   call captures (no S x S tensor); forward only */
 };
 #define ATTN_MASK_BITS 0x0Fu
-#define ATTN_SCORE_BITS 0x300u
+#define ATTN_SCORE_BITS 0x700u
 
 enum { ATTN_BF16 = 0, ATTN_F32 = 1 };
 
@@ -124,6 +128,10 @@ typedef struct attn_params {
                                         visited with the mask evaluated per element */
   int* status;                 /* device int32 status word, or NULL for the library's own */
   unsigned long long timeout_ns; /* limit of each device-side wait; 0 = 4 s */
+  const float* rel_bias;       /* ATTN_SCORE_RELBIAS: device fp32 [Hq][Sq + Skv - 1]; entry
+                                  d + Skv - 1 is added to the score of a query-key pair at
+                                  distance d = i - j (4-byte aligned). Not differentiated:
+                                  attn_bwd returns ATTN_ERR_UNSUPPORTED with this bit */
   unsigned fault_inject;       /* 0 in normal use. ATTN_FAULT_NO_LOADS: the tensor-core
                                   kernels' load warp issues no copy, so every wait for data
                                   runs out after timeout_ns and the call reports

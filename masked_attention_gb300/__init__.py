@@ -28,7 +28,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmattn.so
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_MISALIGNED = 0, 1, 2, 3
 ATTN_ERR_WORKSPACE_TOO_SMALL, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = 4, 5, 6
 MASK_CAUSAL, MASK_WINDOW, MASK_DOCUMENT, MASK_PREFIX = 1 << 0, 1 << 1, 1 << 2, 1 << 3
-SCORE_ALIBI, SCORE_SOFTCAP = 1 << 8, 1 << 9
+SCORE_ALIBI, SCORE_SOFTCAP, SCORE_RELBIAS = 1 << 8, 1 << 9, 1 << 10
 BF16, F32 = 0, 1
 TILE = 128
 FAULT_NO_LOADS = 1
@@ -51,7 +51,8 @@ class attn_params(ctypes.Structure):
                 ("softcap", ctypes.c_float), ("alibi_slopes", ctypes.c_void_p),
                 ("doc_id", ctypes.c_void_p), ("prefix_len", ctypes.c_void_p),
                 ("block_mask", ctypes.POINTER(attn_block_mask)), ("status", ctypes.c_void_p),
-                ("timeout_ns", ctypes.c_ulonglong), ("fault_inject", ctypes.c_uint)]
+                ("timeout_ns", ctypes.c_ulonglong), ("rel_bias", ctypes.c_void_p),
+                ("fault_inject", ctypes.c_uint)]
 
 
 _lib = None
@@ -166,7 +167,7 @@ class BlockMask:
 
 def _params(dtype: int, scale: float, window: int, softcap: float, alibi_slopes, doc_id,
             prefix_len, block_mask: Optional[BlockMask], status, timeout_ns: int,
-            fault_inject: int = 0) -> attn_params:
+            fault_inject: int = 0, rel_bias=None) -> attn_params:
     p = attn_params()
     p.dtype = dtype
     p.scale = scale
@@ -179,6 +180,7 @@ def _params(dtype: int, scale: float, window: int, softcap: float, alibi_slopes,
     p.status = _ptr(status)
     p.timeout_ns = timeout_ns
     p.fault_inject = fault_inject
+    p.rel_bias = _ptr(rel_bias)
     return p
 
 
@@ -212,7 +214,7 @@ def attn_fwd(q, k, v, o, lse, variant: int = 0, *, B=None, Hq=None, Hkv=None, Sq
              Skv=None, D=None, dtype: Optional[int] = None, scale: float = 0.0, window: int = 0,
              softcap: float = 0.0, alibi_slopes=None, doc_id=None, prefix_len=None,
              block_mask: Optional[BlockMask] = None, status=None, timeout_ns: int = 0,
-             fault_inject: int = 0, stream=None) -> None:
+             fault_inject: int = 0, rel_bias=None, stream=None) -> None:
     """O and LSE of masked attention; writes ``o`` and ``lse`` in place.
 
     ``q`` [B,Hq,Sq,D], ``k``/``v`` [B,Hkv,Skv,D], ``o`` like ``q``, ``lse`` fp32
@@ -225,7 +227,7 @@ def attn_fwd(q, k, v, o, lse, variant: int = 0, *, B=None, Hq=None, Hkv=None, Sq
         import torch
         dtype = F32 if q.dtype == torch.float32 else BF16
     p = _params(dtype, scale, window, softcap, alibi_slopes, doc_id, prefix_len, block_mask,
-                status, timeout_ns, fault_inject)
+                status, timeout_ns, fault_inject, rel_bias)
     st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
                         variant, ctypes.byref(p), _stream(stream))
     _check(st, "attn_fwd")

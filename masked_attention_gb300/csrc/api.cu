@@ -83,6 +83,9 @@ attn_status check_mask_params(unsigned variant, const attn_params* p, int B) {
   if ((variant & ATTN_MASK_DOCUMENT) && !p->doc_id) return ATTN_ERR_INVALID_ARG;
   if ((variant & ATTN_MASK_PREFIX) && !p->prefix_len) return ATTN_ERR_INVALID_ARG;
   if ((variant & ATTN_SCORE_SOFTCAP) && !(p->softcap > 0.0f)) return ATTN_ERR_INVALID_ARG;
+  if ((variant & ATTN_SCORE_RELBIAS) &&
+      (!p->rel_bias || (reinterpret_cast<uintptr_t>(p->rel_bias) & 3)))
+    return ATTN_ERR_INVALID_ARG;
   (void)B;
   return ATTN_OK;
 }
@@ -144,6 +147,9 @@ attn_status fill_problem(FwdProblem& f, const void* q, const void* k, const void
   f.score.softcap = p->softcap;
   f.score.slopes = p->alibi_slopes;
   f.score.Hq = Hq;
+  f.score.rel_bias = (variant & ATTN_SCORE_RELBIAS) ? p->rel_bias : nullptr;
+  f.score.rb_len = Sq + Skv - 1;
+  f.score.rb_zero = Skv - 1;
   if (p->block_mask) {
     const attn_block_mask* bm = p->block_mask;
     f.lists = BlockLists{bm->full_cnt, bm->part_cnt, bm->full_idx, bm->part_idx, bm->order,
@@ -275,6 +281,7 @@ MATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, cons
                                 Hq, Hkv, Sq, Skv, D, variant, p);
   if (st != ATTN_OK) return st;
   if (p->dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (variant & ATTN_SCORE_RELBIAS) return ATTN_ERR_UNSUPPORTED;  // forward only
   if (Sq % kTile != 0 || Skv % kTile != 0) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || Sq == 0 || Skv == 0) return ATTN_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)

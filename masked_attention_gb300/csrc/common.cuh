@@ -32,6 +32,9 @@ struct ScoreArgs {
   float softcap;
   const float* slopes;    // [Hq] or nullptr -> 2^(-8(h+1)/Hq)
   int Hq;
+  const float* rel_bias;  // [Hq][rb_len] distance-indexed bias, or nullptr
+  int rb_len;             // Sq + Skv - 1
+  int rb_zero;            // index of distance 0: Skv - 1
 };
 
 struct BlockLists {       // device view of attn_block_mask (nullptr full_cnt = none)
@@ -174,6 +177,21 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared (cp.async), its group commit and
+// the wait for all groups but the newest `n` (n = 0 or 1).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Plain bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).

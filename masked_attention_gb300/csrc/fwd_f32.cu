@@ -42,6 +42,8 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(FwdProblem p) {
     acc[d] = 0.0f;
   }
   const float slope = (p.variant & ATTN_SCORE_ALIBI) ? alibi_slope(p.score, h) : 0.0f;
+  // distance-indexed bias of this head (relative position encoding), or nullptr
+  const float* rb = p.score.rel_bias ? p.score.rel_bias + (size_t)h * p.score.rb_len : nullptr;
   float m = -INFINITY, l = 0.0f;
 
   // Which key tiles to visit: the block-mask lists of this 128-row tile, or
@@ -86,8 +88,9 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(FwdProblem p) {
         float x = (part + __shfl_xor_sync(0xffffffffu, part, 1)) * p.score.scale;
         const int j = j0 + jj;
         if (p.variant & ATTN_SCORE_ALIBI) x -= slope * float(i - j);
-        if (p.variant & ATTN_SCORE_SOFTCAP) x = p.score.softcap * tanhf(x / p.score.softcap);
         bool keep = row_ok && j < p.Skv;
+        if (rb && keep) x += rb[i - j + p.score.rb_zero];
+        if (p.variant & ATTN_SCORE_SOFTCAP) x = p.score.softcap * tanhf(x / p.score.softcap);
         if (partial && keep) keep = mask_keep(p.mask, b, i, j);
         s[jj] = keep ? x : -INFINITY;
         cmax = fmaxf(cmax, s[jj]);

@@ -1,920 +1,12 @@
-// bf16 forward on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
-//
-// Algorithm: the 1-pass FlashAttention recurrence named on the
-// Online-Softmax/FlashAttention page (online softmax: running max m, running
-// sum l, accumulator rescaled when m grows), with score_mod applied per element
-// before the softmax and the mask applied only on partial tiles (FlexAttention
-// page: "FlexAttention" section, the variant list, and the item on exploiting
-// mask sparsity). The score matrix never leaves the SM.
-//
-// Work unit: one 128-row query tile of two query heads (2h, 2h+1) of one batch
-// element; both heads see the same key-tile list because the mask does not
-// depend on the head. Units are taken longest-first (block-mask `order`) by a
-// persistent grid of one CTA per SM.
-//
-// Warp roles (384 threads, three warpgroups):
-//   warps 0-3  softmax for head A (thread t owns query row t: TMEM lane t)
-//   warps 4-7  softmax for head B
-//   warp  8    TMA producer: Q tiles once per unit, then K/V tiles into a ring
-//   warp  9    MMA issuer (one thread) and TMEM owner
-//   warps 10-11 idle
-// The third warpgroup hands registers to the softmax warpgroups (setmaxnreg).
-// Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A, O_B (D columns
-// each) from 256. P (bf16) overwrites the first 64 columns of its S tile and
-// is the A operand of the P.V product, read straight from TMEM.
-//
-// Per key tile j and head X:  S_X = Q_X K_j^T (SS MMA) -> softmax warps read
-// S_X, write P_X -> O_X += P_X V_j (TS MMA). The MMA warp alternates heads so
-// one head's softmax overlaps the other head's products.
-#include <cmath>
-#include <mutex>
-
-#include "host_util.h"
-#include "launch.h"
+// Launches of the bf16 tensor-core forward (kernel in fwd_tc_kernel.cuh) for
+// the score_mod variants without the relative-position bias; the variants
+// with it are compiled in fwd_tc_rb.cu, so the two builds run in parallel.
+#include "fwd_tc_kernel.cuh"
 
 namespace mattn {
-namespace {
-
-constexpr int kThreads = 384;
-constexpr int kRegsSoftmax = 208;  // 2 x 128 x 208 + 128 x 88 = 64512 = 384 x 168
-constexpr int kRegsOther = 88;
-constexpr int kSoftmaxThreads = 128;
-constexpr int kWarpProducer = 8;
-constexpr int kWarpMma = 9;
-constexpr int kWarpMma2 = 10;  // second MMA issuer (separate-P kernels: head B)
-
-template <int D>
-struct Cfg {
-  static constexpr int kTileBytes = kTile * D * 2;  // one 128-row bf16 tile
-  static constexpr int kBoxes = D / 64;             // 64-column (128-byte) TMA boxes
-  static constexpr int kBoxBytes = kTile * 128;
-  static constexpr int kSlots = D == 128 ? 4 : 8;   // K/V ring
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffSlots = 2 * kTileBytes;
-  static constexpr int kOffBars = kOffSlots + kSlots * kTileBytes;
-  // barriers: q_full, q_empty, drain, s_full[2], p_full[2], o_done[2], o_free[2],
-  // s_free[2], pv_done[2], drain2, slot_full[kSlots], slot_empty[kSlots]
-  static constexpr int kNumBars = 16 + 2 * kSlots;
-  // per-warp document ids, read as int4: 16-byte aligned
-  static constexpr int kOffDoc = (kOffBars + kNumBars * 8 + 15) & ~15;
-  static constexpr int kOffMisc = kOffDoc + 8 * kTile * 4;
-  static constexpr int kSmemBytes = kOffMisc + 16;
-  static constexpr int kSmemAlloc = kSmemBytes + 1024;     // slack for 1024-byte alignment
-  static constexpr uint32_t kColO0 = 256;
-  // D = 64 leaves TMEM room for P apart from S (columns 384 + 64x): the
-  // softmax frees S as soon as it has read it and the next Q.K^T overlaps the
-  // rest of its work. At D = 128 the 512 columns hold S_A, S_B, O_A, O_B and P
-  // overwrites S, so the next Q.K^T waits for the P.V product.
-  static constexpr bool kSepP = D == 64;
-  // One MMA warp per head at D = 64: the tensor pipe queues about one product,
-  // so a single issuer leaves it idle whenever it waits or commits; with two,
-  // one head's products run while the other's issuer waits. At D = 128 (P
-  // over S) a single issuer alternating heads keeps the two heads' softmax
-  // phases apart, which matters more there: with two issuers they align and
-  // contend for the special-function unit (soft-cap: 1.38 -> 1.84 ms measured).
-  static constexpr bool kDualMma = kSepP;
-  static constexpr uint32_t kColP = 384;
-  static_assert(!kSepP || kColP + 128 <= 512, "tensor memory columns");
-  static_assert(kOffDoc % 16 == 0 && (kTile * 4) % 16 == 0, "int4 reads of document ids");
-  static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
-};
-
-struct Unit {
-  int b, qt, h[2];  // h[1] < 0: single-head unit
-  int n_full, n_part;
-  const int* lf;
-  const int* lp;
-  __device__ __forceinline__ int n() const { return n_full + n_part; }
-  // Visiting order: partial tiles, then full tiles, each from the largest key
-  // index down. Keys near the query usually carry the largest scores (causal
-  // diagonal, ALiBi), so the running maximum settles early and the
-  // accumulator is rarely rescaled. The softmax result does not depend on it.
-  __device__ __forceinline__ bool partial(int j) const { return j < n_part; }
-  __device__ __forceinline__ int kt(int j) const {
-    if (j < n_part) {
-      const int a = n_part - 1 - j;
-      return lp ? lp[a] : a;
-    }
-    const int a = n_full - 1 - (j - n_part);
-    return lf ? lf[a] : a;
-  }
-};
-
-// Static schedule of a persistent CTA: round r takes unit r*G + c for even r
-// and r*G + (G-1-c) for odd r (G CTAs, c = blockIdx.x). On a longest-first
-// unit order this zigzag evens out the total work per CTA.
-__device__ __forceinline__ int zigzag_unit(int r) {
-  const int c = (r & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x;
-  return r * (int)gridDim.x + c;
-}
-
-__device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp) {
-  const int nq = (p.Sq + kTile - 1) / kTile, nkv = (p.Skv + kTile - 1) / kTile;
-  const int rank = u / nhp, hp = u % nhp;
-  const bool causal_bound = (p.variant & ATTN_MASK_CAUSAL) && !(p.variant & ATTN_MASK_PREFIX);
-  int row;
-  if (p.lists.full_cnt) {
-    row = p.lists.order[rank];
-  } else if (causal_bound) {
-    row = (rank % p.B) * nq + (nq - 1 - rank / p.B);  // longest first
-  } else {
-    row = rank;
-  }
-  Unit U;
-  U.b = row / nq;
-  U.qt = row % nq;
-  U.h[0] = 2 * hp;
-  U.h[1] = 2 * hp + 1 < p.Hq ? 2 * hp + 1 : -1;
-  if (p.lists.full_cnt) {
-    U.n_full = p.lists.full_cnt[row];
-    U.n_part = p.lists.part_cnt[row];
-    U.lf = p.lists.full_idx + (size_t)row * p.lists.nkv;
-    U.lp = p.lists.part_idx + (size_t)row * p.lists.nkv;
-  } else {
-    const int last = causal_bound ? min(nkv, U.qt + 1) : nkv;
-    const bool masked = (p.variant & ATTN_MASK_BITS) != 0;
-    U.n_full = masked ? 0 : last;
-    U.n_part = masked ? last : 0;
-    U.lf = U.lp = nullptr;
-  }
-  return U;
-}
-
-// Document id of key j, or -1 past the end of the keys (those columns are
-// masked by the key-length bound anyway).
-__device__ __forceinline__ int doc_at(const int* docb, int j, int Skv) {
-  return j < Skv ? docb[j] : -1;
-}
-
-// Per-row, per-tile constants of the score transform.
-struct TileCtx {
-  float sl2, sc, cl2, slope, slope2, scale, inv_cap;
-  float base;        // j0 - i: (j - i) = base + c
-  int hi, lo, pre;   // mask bounds on the column c (see transform_tile)
-  const int* wdoc;   // document ids of the key tile (shared memory), or nullptr
-  int doc_i;
-  uint32_t modes;    // per 32-column chunk of a partial tile (chunk_modes)
-};
-
-constexpr uint32_t kChunkKept = 0, kChunkMasked = 1, kChunkMixed = 2;
-
-// Whole-warp bounded wait (every lane polls; the result is the same for all).
-__device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
-  return __all_sync(0xffffffffu, wait_bounded(bar, parity, wd));
-}
-
-// S = Q K^T over D (K-major operands, 128-byte swizzle): K-step kk advances
-// 32 bytes inside a 64-column box and moves to the next box every 4 steps.
-template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc) {
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint64_t off = (uint64_t)(((kk / 4) * kTile * 128 + (kk % 4) * 32) >> 4);
-    mma_bf16_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0);
-  }
-}
-
-// O += P V: P (bf16, 8 TMEM columns per 16 keys) times V (MN-major); K-step kk
-// advances 16 key rows = 2048 bytes.
-template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t b_desc,
-                                         uint32_t idesc, bool accumulate) {
-#pragma unroll
-  for (int kk = 0; kk < kTile / 16; ++kk)
-    mma_bf16_ts(d_tmem, p_tmem + kk * 8, b_desc + (uint64_t)((kk * 16 * 128) >> 4), idesc,
-                (accumulate || kk > 0) ? 1u : 0u);
-}
-
-// Loads n32 x 32 columns of this thread's TMEM lane into s (one wait for all).
-__device__ __forceinline__ void load_cols(uint32_t col, float* s, int n32) {
-  uint32_t* r = reinterpret_cast<uint32_t*>(s);
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-    if (c < n32) tmem_ld32(col + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-    if (c < n32) tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(r + 32 * c));
-}
-
-// s[0..N) <- score_mod(s) in log2 units minus `shift` for the columns
-// c0 .. c0+N-1 of the tile; masked entries -inf.
-template <int SCORE, int N>
-__device__ __forceinline__ void transform_cols(float* s, int c0, const TileCtx& t, float shift,
-                                               bool partial) {
-  if constexpr (SCORE == 0) {
-    const float2 m2 = make_float2(t.sl2, t.sl2), sh2 = make_float2(-shift, -shift);
-#pragma unroll
-    for (int c = 0; c < N; c += 2) {
-      const float2 e = ffma2(make_float2(s[c], s[c + 1]), m2, sh2);
-      s[c] = e.x;
-      s[c + 1] = e.y;
-    }
-  } else if constexpr (SCORE == 1) {
-    const float b0 = fmaf(t.slope2, t.base + float(c0), -shift);
-#pragma unroll
-    for (int c = 0; c < N; ++c) s[c] = fmaf(s[c], t.sl2, fmaf(t.slope2, float(c), b0));
-  } else {
-    const float b0 = t.slope * (t.base + float(c0));
-    const float2 cl = make_float2(t.cl2, t.cl2), sh2 = make_float2(-shift, -shift);
-#pragma unroll
-    for (int c = 0; c < N; c += 2) {
-      float2 y;
-      if constexpr (SCORE == 2) {
-        y = fmul2(make_float2(s[c], s[c + 1]), make_float2(t.sc, t.sc));
-      } else {
-        y.x = fmaf(s[c], t.scale, fmaf(t.slope, float(c), b0)) * t.inv_cap;
-        y.y = fmaf(s[c + 1], t.scale, fmaf(t.slope, float(c + 1), b0)) * t.inv_cap;
-      }
-      const float2 e = ffma2(make_float2(tanh_approx(y.x), tanh_approx(y.y)), cl, sh2);
-      s[c] = e.x;
-      s[c + 1] = e.y;
-    }
-  }
-  // mask_mod on a partial tile: keep (lo < c <= hi and same document) or
-  // c < pre. Chunks of 32 columns that every row of the warp keeps need no
-  // work and chunks no row keeps become -inf (t.modes, see chunk_modes); only
-  // mixed chunks are masked element by element. There the terms are combined
-  // with bitwise operators and the document ids are read unconditionally, four
-  // at a time: a short-circuit form would make every element a divergent
-  // branch around a load.
-  if (partial) {
-#pragma unroll
-    for (int q = 0; q < N / 32; ++q) {
-      const int a = c0 + 32 * q;  // first column of the chunk
-      const uint32_t mode = (t.modes >> (2 * (a >> 5))) & 3u;
-      if (mode == kChunkKept) continue;
-      float* sq = s + 32 * q;
-      if (mode == kChunkMasked) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) sq[c] = -INFINITY;
-        continue;
-      }
-      if (t.wdoc) {
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const int4 dv = *reinterpret_cast<const int4*>(t.wdoc + a + c);
-          const int d4[4] = {dv.x, dv.y, dv.z, dv.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int cc = a + c + e;
-            const bool keep =
-                ((cc <= t.hi) & (cc > t.lo) & (d4[e] == t.doc_i)) | (cc < t.pre);
-            sq[c + e] = keep ? sq[c + e] : -INFINITY;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int cc = a + c;
-          const bool keep = ((cc <= t.hi) & (cc > t.lo)) | (cc < t.pre);
-          sq[c] = keep ? sq[c] : -INFINITY;
-        }
-      }
-    }
-  }
-}
-
-// Warp-uniform mode of each 32-column chunk of a partial tile, two bits per
-// chunk: kept by every row of the warp, masked for every row, or mixed. From
-// the rows' column bounds and the min/max document id of the chunk's keys;
-// exact for "kept" and "masked", conservative ("mixed") otherwise. Integer
-// compares run at half rate, so deciding whole chunks saves most of the
-// per-element mask work on diagonal, window-edge and document-edge tiles.
-__device__ __forceinline__ uint32_t chunk_modes(const TileCtx& t) {
-  const int lane = threadIdx.x & 31;
-  uint32_t modes = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int a = 32 * q;
-    const bool pre_all = a + 31 < t.pre, pre_none = a >= t.pre;
-    bool all = ((a + 31 <= t.hi) & (a > t.lo)) | pre_all;
-    bool none = ((a > t.hi) | (a + 31 <= t.lo)) & pre_none;
-    if (t.wdoc) {
-      const int dl = t.wdoc[a + lane];
-      const int dmin = __reduce_min_sync(0xffffffffu, dl);
-      const int dmax = __reduce_max_sync(0xffffffffu, dl);
-      const bool d_all = (dmin == t.doc_i) & (dmax == t.doc_i);
-      const bool d_none = (t.doc_i < dmin) | (t.doc_i > dmax);
-      all = (all & d_all) | pre_all;
-      none = none | (d_none & pre_none);
-    }
-    const uint32_t m = __all_sync(0xffffffffu, all)    ? kChunkKept
-                       : __all_sync(0xffffffffu, none) ? kChunkMasked
-                                                       : kChunkMixed;
-    modes |= m << (2 * q);
-  }
-  return modes;
-}
-
-// pk[0..N/2) <- bf16 pairs of 2^s; returns the fp32 sum.
-template <int N>
-__device__ __forceinline__ float exp2_pack(const float* s, uint32_t* pk) {
-  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                   make_float2(0.f, 0.f)};
-#pragma unroll
-  for (int c = 0; c < N; c += 2) {
-    const float2 pr = make_float2(ex2_approx(s[c]), ex2_approx(s[c + 1]));
-    acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], pr);
-    pk[c >> 1] = pack_bf16x2(pr.x, pr.y);
-  }
-  const float2 a = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
-  return a.x + a.y;
-}
-
-template <int D, int SCORE>
-__global__ void __launch_bounds__(kThreads, 1)
-    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
-                  const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const FwdProblem p) {
-  using C = Cfg<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  uint8_t* sQ = smem + C::kOffQ;
-  uint8_t* sSlots = smem + C::kOffSlots;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
-  uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* drain = bars + 2;
-  uint64_t* s_full = bars + 3;   // [2]
-  uint64_t* p_full = bars + 5;   // [2]
-  uint64_t* o_done = bars + 7;   // [2]
-  uint64_t* o_free = bars + 9;   // [2]
-  uint64_t* s_free = bars + 11;  // [2] (separate P only) S read by the softmax
-  uint64_t* pv_done = bars + 13; // [2] (separate P only) P.V product complete
-  uint64_t* drain2 = bars + 15;  // (separate P only) second MMA warp's products
-  uint64_t* slot_full = bars + 16;
-  uint64_t* slot_empty = bars + 16 + C::kSlots;
-  int* sdoc = reinterpret_cast<int*>(smem + C::kOffDoc);
-  uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Watchdog wd{abort_flag, p.status, p.timeout_ns};
-
-  if (threadIdx.x == 0) {
-    // With separate P each head has its own MMA warp and every Q tile and
-    // ring slot is released by two commits (one per warp, or two by the one
-    // warp that used it).
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, C::kDualMma ? 2 : 1);
-    mbar_init(drain, 1);
-    mbar_init(drain2, 1);
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(s_full + x, 1);
-      mbar_init(p_full + x, kSoftmaxThreads / 32);  // one arrive per softmax warp
-      mbar_init(o_done + x, 1);
-      mbar_init(o_free + x, kSoftmaxThreads / 32);
-      mbar_init(s_free + x, kSoftmaxThreads / 32);
-      mbar_init(pv_done + x, 1);
-    }
-    for (int s = 0; s < C::kSlots; ++s) {
-      mbar_init(slot_full + s, 1);
-      mbar_init(slot_empty + s, C::kDualMma ? 2 : 1);
-    }
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == kWarpMma) {
-    tmem_alloc(tmem_base_smem, 512);
-    tmem_relinquish();
-  }
-  if (warp == kWarpProducer && lane == 0) {
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_v);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_base_smem;
-
-  const int nhp = (p.Hq + 1) / 2;
-  const int num_units = p.B * ((p.Sq + kTile - 1) / kTile) * nhp;
-  const int group = p.Hq / p.Hkv;
-
-  if (warp >= 8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
-  }
-  if (warp == kWarpProducer) {
-    // ------------------------------------------------------------- producer
-    // The whole warp runs the loop (waits stay converged); lane 0 issues.
-    // With ATTN_FAULT_NO_LOADS nothing is issued and the consumers' waits run out.
-    const bool leader = lane == 0 && !(p.fault_inject & ATTN_FAULT_NO_LOADS);
-    uint32_t slot_it = 0, q_it = 0;
-    bool ok = true;
-    for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
-      const int u = zigzag_unit(r);
-      if (u >= num_units) continue;
-      const Unit U = decode_unit(p, u, nhp);
-      const int n = U.n();
-      if (n == 0) continue;
-      const bool two = U.h[1] >= 0;
-      const int hk0 = U.h[0] / group, hk1 = two ? U.h[1] / group : hk0;
-      const bool shared = !two || hk0 == hk1;
-      ok = __all_sync(0xffffffffu, wait_bounded(q_empty, (q_it & 1) ^ 1, wd));
-      if (!ok) break;
-      if (leader) {
-        mbar_arrive_expect_tx(q_full, (two ? 2 : 1) * C::kTileBytes);
-        for (int x = 0; x < (two ? 2 : 1); ++x) {
-          const int slice = U.b * p.Hq + U.h[x];
-          for (int bx = 0; bx < C::kBoxes; ++bx)
-            tma_load_3d(sQ + x * C::kTileBytes + bx * C::kBoxBytes, &tm_q, q_full, bx * 64,
-                        U.qt * kTile, slice);
-        }
-      }
-      __syncwarp();
-      ++q_it;
-      for (int j = 0; j < n && ok; ++j) {
-        const int kt = U.kt(j);
-        const int slices[2] = {U.b * p.Hkv + hk0, U.b * p.Hkv + hk1};
-        // order: K_A, [K_B], V_A, [V_B]
-        for (int t = 0; t < (shared ? 2 : 4) && ok; ++t) {
-          const int per = shared ? 1 : 2;
-          const bool is_v = t >= per;
-          const int x = shared ? 0 : (t % 2);
-          const int slot = slot_it % C::kSlots;
-          ok = __all_sync(0xffffffffu,
-                          wait_bounded(slot_empty + slot, ((slot_it / C::kSlots) & 1) ^ 1, wd));
-          if (!ok) break;
-          if (leader) {
-            mbar_arrive_expect_tx(slot_full + slot, C::kTileBytes);
-            for (int bx = 0; bx < C::kBoxes; ++bx)
-              tma_load_3d(sSlots + slot * C::kTileBytes + bx * C::kBoxBytes, is_v ? &tm_v : &tm_k,
-                          slot_full + slot, bx * 64, kt * kTile, slices[x]);
-          }
-          __syncwarp();
-          ++slot_it;
-        }
-      }
-    }
-    if (!ok && !(p.fault_inject & ATTN_FAULT_NO_LOADS)) {  // let copies in flight land
-      for (uint32_t k = 0; k < C::kSlots && k < slot_it; ++k) {
-        const uint32_t it = slot_it - 1 - k;
-        wait_drain(slot_full + it % C::kSlots, (it / C::kSlots) & 1);
-      }
-      if (q_it > 0) wait_drain(q_full, (q_it - 1) & 1);
-    }
-  } else if (warp == kWarpMma || (C::kDualMma && warp == kWarpMma2)) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the loop (waits stay converged); lane 0 issues the
-    // products and the commits. Loop state stays in registers and the
-    // shared-memory descriptors are precomputed: the start-address field is
-    // in 16-byte units, so an offset is added as (bytes >> 4).
-    const bool leader = lane == 0;
-    constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false);
-    constexpr uint32_t kIdescPV = idesc_bf16(128, D, true);
-    const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
-    const uint64_t dK0 = sdesc_sw128(smem_u32(sSlots), 16, 1024);
-    const uint64_t dV0 = sdesc_sw128(smem_u32(sSlots), C::kBoxBytes, 1024);
-    if constexpr (!C::kDualMma) {
-      uint32_t slot_it = 0, q_it = 0, p_it0 = 0, p_it1 = 0, o_it0 = 0, o_it1 = 0;
-      bool ok = true;
-      for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
-        const int u = zigzag_unit(r);
-        if (u >= num_units) continue;
-        const Unit U = decode_unit(p, u, nhp);
-        const int n = U.n();
-        if (n == 0) continue;
-        const int nx = U.h[1] >= 0 ? 2 : 1;
-        const bool shared = nx == 1 || (U.h[0] / group == U.h[1] / group);
-        const uint32_t T = shared ? 2u : 4u;  // ring slots per key tile
-        ok = wait_warp(q_full, q_it & 1, wd);
-        if (!ok) break;
-        ++q_it;
-        tc_fence_after();
-        // S_x(0) for both heads
-        for (int x = 0; x < nx && ok; ++x) {
-          const uint32_t seq = slot_it + (shared ? 0u : (uint32_t)x);
-          const uint32_t slot = seq % C::kSlots;
-          if (x == 0 || !shared) {
-            ok = wait_warp(slot_full + slot, (seq / C::kSlots) & 1, wd);
-            if (!ok) break;
-            tc_fence_after();
-          }
-          if (leader) {
-            issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
-                        dK0 + ((slot * C::kTileBytes) >> 4), kIdescQK);
-            mma_commit(s_full + x);
-            if (!shared || x == nx - 1) mma_commit(slot_empty + slot);
-          }
-          __syncwarp();
-        }
-        if (ok && n == 1 && leader) mma_commit(q_empty);
-        for (int j = 0; j < n && ok; ++j) {
-          for (int x = 0; x < nx && ok; ++x) {
-            // O_x += P_x V_j
-            ok = wait_warp(p_full + x, (x ? p_it1 : p_it0) & 1, wd);
-            if (!ok) break;
-            if (x) ++p_it1; else ++p_it0;
-            if (j == 0) {
-              ok = wait_warp(o_free + x, ((x ? o_it1 : o_it0) & 1) ^ 1, wd);
-              if (!ok) break;
-              if (x) ++o_it1; else ++o_it0;
-            }
-            const uint32_t vseq = slot_it + j * T + (shared ? 1u : 2u + x);
-            const uint32_t vslot = vseq % C::kSlots;
-            if (x == 0 || !shared) {
-              ok = wait_warp(slot_full + vslot, (vseq / C::kSlots) & 1, wd);
-              if (!ok) break;
-            }
-            tc_fence_after();
-            if (leader) {
-              issue_pv<D>(tmem + C::kColO0 + D * x, tmem + 128u * x,
-                          dV0 + ((vslot * C::kTileBytes) >> 4), kIdescPV, j > 0);
-              if (!shared || x == nx - 1) mma_commit(slot_empty + vslot);
-            }
-            __syncwarp();
-            if (j + 1 < n) {  // S_x(j+1)
-              const uint32_t kseq = slot_it + (j + 1) * T + (shared ? 0u : (uint32_t)x);
-              const uint32_t kslot = kseq % C::kSlots;
-              if (x == 0 || !shared) {
-                ok = wait_warp(slot_full + kslot, (kseq / C::kSlots) & 1, wd);
-                if (!ok) break;
-                tc_fence_after();
-              }
-              if (leader) {
-                issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
-                            dK0 + ((kslot * C::kTileBytes) >> 4), kIdescQK);
-                mma_commit(s_full + x);
-                if (!shared || x == nx - 1) mma_commit(slot_empty + kslot);
-              }
-              __syncwarp();
-            } else if (leader) {
-              mma_commit(o_done + x);
-            }
-          }
-          if (ok && j + 1 == n - 1 && leader) mma_commit(q_empty);
-        }
-        __syncwarp();
-        slot_it += n * T;
-      }
-    } else {
-      // Separate P, one MMA warp per head: warp kWarpMma serves head A and
-      // kWarpMma2 head B, so neither head's products wait behind the other's.
-      // S_x(j+1) = Q_x K_{j+1}^T is issued as soon as the softmax has read
-      // S_x(j) (s_free), before P_x(j) exists; O_x += P_x(j) V_j follows when
-      // P_x(j) is ready. kq counts this head's Q.K^T products (tile k waits
-      // for s_free phase k-1), kp its P.V products. Every Q tile and ring slot
-      // gets exactly two release commits: one from each warp when both heads
-      // read it, else two from the warp that did.
-      const int x = warp == kWarpMma ? 0 : 1;
-      uint32_t slot_it = 0, q_it = 0, kq = 0, kp = 0, o_it = 0;
-      bool ok = true;
-      for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
-        const int u = zigzag_unit(r);
-        if (u >= num_units) continue;
-        const Unit U = decode_unit(p, u, nhp);
-        const int n = U.n();
-        if (n == 0) continue;
-        const int nx = U.h[1] >= 0 ? 2 : 1;
-        const bool shared = nx == 1 || (U.h[0] / group == U.h[1] / group);
-        const uint32_t T = shared ? 2u : 4u;  // ring slots per key tile
-        const uint32_t base = slot_it;
-        slot_it += n * T;
-        ++q_it;
-        if (x >= nx) continue;  // single-head unit: head B's warp has nothing to do
-        const bool both = nx == 2 && shared;  // the other warp releases the same slots
-        ok = wait_warp(q_full, (q_it - 1) & 1, wd);
-        if (!ok) break;
-        // S_x(jj) = Q_x K_jj^T
-        auto do_qk = [&](int jj) -> bool {
-          if constexpr (C::kSepP) {
-            if (kq > 0 && !wait_warp(s_free + x, (kq - 1) & 1, wd)) return false;
-          }
-          const uint32_t kseq = base + jj * T + (shared ? 0u : (uint32_t)x);
-          const uint32_t kslot = kseq % C::kSlots;
-          if (!wait_warp(slot_full + kslot, (kseq / C::kSlots) & 1, wd)) return false;
-          tc_fence_after();
-          if (leader) {
-            issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
-                        dK0 + ((kslot * C::kTileBytes) >> 4), kIdescQK);
-            mma_commit(s_full + x);
-            mma_commit(slot_empty + kslot);
-            if (!both) mma_commit(slot_empty + kslot);
-            if (jj + 1 == n) {  // the unit's last Q.K^T for this head
-              mma_commit(q_empty);
-              if (nx == 1) mma_commit(q_empty);
-            }
-          }
-          __syncwarp();
-          ++kq;
-          return true;
-        };
-        // O_x += P_x(jj) V_jj
-        auto do_pv = [&](int jj) -> bool {
-          if (!wait_warp(p_full + x, kp & 1, wd)) return false;
-          if (jj == 0) {
-            if (!wait_warp(o_free + x, (o_it & 1) ^ 1, wd)) return false;
-            ++o_it;
-          }
-          const uint32_t vseq = base + jj * T + (shared ? 1u : 2u + x);
-          const uint32_t vslot = vseq % C::kSlots;
-          if (!wait_warp(slot_full + vslot, (vseq / C::kSlots) & 1, wd)) return false;
-          tc_fence_after();
-          if (leader) {
-            const uint32_t pcol = C::kSepP ? C::kColP + 64u * x : 128u * x;
-            issue_pv<D>(tmem + C::kColO0 + D * x, tmem + pcol,
-                        dV0 + ((vslot * C::kTileBytes) >> 4), kIdescPV, jj > 0);
-            if (C::kSepP) mma_commit(pv_done + x);
-            mma_commit(slot_empty + vslot);
-            if (!both) mma_commit(slot_empty + vslot);
-            if (jj + 1 == n) mma_commit(o_done + x);
-          }
-          __syncwarp();
-          ++kp;
-          return true;
-        };
-        if constexpr (C::kSepP) {
-          // separate P: S_x(j+1) as soon as S_x(j) is read, then P_x(j) V_j
-          for (int j = -1; j < n && ok; ++j) {
-            if (j + 1 < n) ok = do_qk(j + 1);
-            if (ok && j >= 0) ok = do_pv(j);
-          }
-        } else {
-          // P overwrites S: S_x(j+1) only after P_x(j) V_j has been issued
-          ok = do_qk(0);
-          for (int j = 0; j < n && ok; ++j) {
-            ok = do_pv(j);
-            if (ok && j + 1 < n) ok = do_qk(j + 1);
-          }
-        }
-      }
-      // all products issued by this warp are complete before TMEM is freed
-      uint64_t* dr = x ? drain2 : drain;
-      if (leader) mma_commit(dr);
-      __syncwarp();
-      wait_drain(dr, 0);
-    }
-    if constexpr (!C::kDualMma) {
-      // all products issued by this warp are complete before TMEM is freed
-      if (leader) mma_commit(drain);
-      __syncwarp();
-      wait_drain(drain, 0);
-    }
-  } else if (warp < 8) {
-    // ------------------------------------------------------------- softmax
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
-    const int x = warp / 4;            // head slot 0 or 1
-    const int t = threadIdx.x & 127;   // query row within the tile == TMEM lane
-    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
-    const uint32_t colS = tmem + lane_base + 128u * x;
-    const uint32_t colO = tmem + lane_base + C::kColO0 + D * x;
-    int* wdoc = sdoc + warp * kTile;   // this warp's copy of the key tile's document ids
-    const float sl2 = p.score.scale * kLog2e;              // raw score -> log2 units
-    const float sc = p.score.scale / p.score.softcap;      // raw score -> tanh argument
-    const float cl2 = p.score.softcap * kLog2e;            // tanh -> log2 units
-    uint32_t s_it = 0, o_it = 0;
-    bool ok = true;
-    for (int rr = 0; rr * (int)gridDim.x < num_units && ok; ++rr) {
-      const int u = zigzag_unit(rr);
-      if (u >= num_units) continue;
-      const Unit U = decode_unit(p, u, nhp);
-      const int h = U.h[x];
-      if (h < 0) continue;
-      const int n = U.n();
-      const int i = U.qt * kTile + t;
-      const bool row_in = i < p.Sq;  // a last query tile may run past Sq
-      const size_t orow = ((size_t)(U.b * p.Hq + h) * p.Sq + i);
-      __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + orow * D;
-      if (n == 0) {
-        if (row_in) {
-          const uint4 z = make_uint4(0, 0, 0, 0);
-          for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(O)[c] = z;
-          p.lse[orow] = -INFINITY;
-        }
-        continue;
-      }
-      const float slope = (SCORE & 1) ? alibi_slope(p.score, h) : 0.0f;
-      const float slope2 = slope * kLog2e;
-      const int* docb = (p.variant & ATTN_MASK_DOCUMENT)
-                            ? p.mask.doc_id + (size_t)U.b * p.mask.doc_len : nullptr;
-      const int doc_i = (docb && row_in) ? docb[i] : 0;
-      const int P = (p.variant & ATTN_MASK_PREFIX) ? p.mask.prefix_len[U.b] : INT_MIN;
-      float m_ref = -INFINITY, l = 0.0f;
-      // Key-tile indices are read two tiles ahead and the document ids of a
-      // partial tile one tile ahead, so neither global read waits on the
-      // critical path (lane l holds ids l, l+32, l+64, l+96).
-      int kt_cur = U.kt(0), kt_n1 = n > 1 ? U.kt(1) : 0;
-      int dcur[4] = {0, 0, 0, 0};
-      if (docb && U.partial(0)) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) dcur[c] = doc_at(docb, kt_cur * kTile + lane + 32 * c, p.Skv);
-      }
-
-      for (int j = 0; j < n; ++j) {
-        const int kt = kt_cur;
-        const int kt_n2 = j + 2 < n ? U.kt(j + 2) : 0;
-        int dnext[4] = {0, 0, 0, 0};
-        if (docb && j + 1 < n && U.partial(j + 1)) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) dnext[c] = doc_at(docb, kt_n1 * kTile + lane + 32 * c, p.Skv);
-        }
-        const int j0 = kt * kTile;
-        // a key tile that runs past Skv is masked like a partial tile: its
-        // columns from Skv - j0 on hold zero-filled keys
-        const bool tail = j0 + kTile > p.Skv;
-        const bool partial = U.partial(j) || tail;
-        if (partial && docb) {
-          __syncwarp();
-#pragma unroll
-          for (int c = 0; c < 4; ++c) wdoc[lane + 32 * c] = dcur[c];
-          __syncwarp();
-        }
-        kt_cur = kt_n1;
-        kt_n1 = kt_n2;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) dcur[c] = dnext[c];
-        TileCtx tc{sl2, sc, cl2, slope, slope2, p.score.scale, 1.0f / p.score.softcap,
-                   float(j0 - i),
-                   min((p.variant & ATTN_MASK_CAUSAL) ? i - j0 : INT_MAX, p.Skv - 1 - j0),
-                   (p.variant & ATTN_MASK_WINDOW) ? i - j0 - p.mask.window : INT_MIN,
-                   P == INT_MIN ? INT_MIN : min(P, p.Skv) - j0, docb ? wdoc : nullptr, doc_i,
-                   0u};
-        if (partial) tc.modes = chunk_modes(tc);  // before the wait: off the critical path
-        ok = __all_sync(0xffffffffu, wait_bounded(s_full + x, s_it & 1, wd));
-        if (!ok) break;
-        ++s_it;
-        tc_fence_after();
-        // Steady state: exponentiate against the current reference max with no
-        // max pass, 64 columns at a time, keeping P as packed bf16. A tile whose
-        // sum is not finite or exceeds 2^64 (the first tile, or a tile whose
-        // scores outgrow the reference) is redone from S (still in TMEM) with
-        // its true maximum, rescaling l and O.
-        uint32_t pk[64];
-        float tsum = 0.0f;
-        bool redo;
-        {
-          // the second half's load is in flight while the first half is processed
-          float v0[64], v1[64];
-          load_cols(colS, v0, 2);
-          tmem_ld32(colS + 64, *reinterpret_cast<uint32_t(*)[32]>(v1));
-          tmem_ld32(colS + 96, *reinterpret_cast<uint32_t(*)[32]>(v1 + 32));
-          if (j == 0) {
-            // A unit's first tile has no reference yet: both halves are
-            // transformed first and the tile's own row maximum becomes the
-            // reference (0 where the whole row is masked), so the largest
-            // weight is exactly 1 as in the max pass below.
-            transform_cols<SCORE, 64>(v0, 0, tc, 0.0f, partial);
-            tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(v1));
-            tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(v1 + 32));
-            transform_cols<SCORE, 64>(v1, 64, tc, 0.0f, partial);
-            const float mt = fmaxf(row_max<64>(v0), row_max<64>(v1));
-            m_ref = mt == -INFINITY ? 0.0f : mt;
-            const float2 sh = make_float2(-m_ref, -m_ref);
-#pragma unroll
-            for (int c = 0; c < 64; c += 2) {
-              const float2 e0 = fadd2(make_float2(v0[c], v0[c + 1]), sh);
-              v0[c] = e0.x;
-              v0[c + 1] = e0.y;
-              const float2 e1 = fadd2(make_float2(v1[c], v1[c + 1]), sh);
-              v1[c] = e1.x;
-              v1[c + 1] = e1.y;
-            }
-            tsum = exp2_pack<64>(v0, pk);
-            tsum += exp2_pack<64>(v1, pk + 32);
-          } else {
-            transform_cols<SCORE, 64>(v0, 0, tc, m_ref, partial);
-            tsum = exp2_pack<64>(v0, pk);
-            tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(v1));
-            tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(v1 + 32));
-            transform_cols<SCORE, 64>(v1, 64, tc, m_ref, partial);
-            tsum += exp2_pack<64>(v1, pk + 32);
-          }
-          redo = !(tsum <= 18446744073709551616.0f);
-        }
-        if (__any_sync(0xffffffffu, redo)) {
-          // pass 1: the tile's maximum, 32 columns at a time
-          float mt = -INFINITY;
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            float v[32];
-            load_cols(colS + 32 * qq, v, 1);
-            transform_cols<SCORE, 32>(v, 32 * qq, tc, 0.0f, partial);
-            mt = fmaxf(mt, row_max<32>(v));
-          }
-          const float m_new = redo ? fmaxf(m_ref, mt) : m_ref;
-          const float alpha = ex2_approx(m_ref - m_new);  // m_ref = -inf gives 0
-          const bool need_o = redo && j > 0 && m_ref != -INFINITY && m_new > m_ref;
-          if (redo && m_new > m_ref) l *= alpha;
-          if (__any_sync(0xffffffffu, need_o)) {
-            if constexpr (C::kSepP) {
-              // S(j) was computed before the previous tile's P.V: let it land in O
-              ok = __all_sync(0xffffffffu, wait_bounded(pv_done + x, s_it & 1, wd));
-              if (!ok) break;
-              tc_fence_after();
-            }
-            const float a = need_o ? alpha : 1.0f;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(colO + 32 * c, r);
-              tmem_ld_wait_regs(r);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * a);
-              tmem_st32(colO + 32 * c, r);
-            }
-          }
-          m_ref = m_new;
-          // pass 2: exponentiate against the new reference
-          const float m_use = m_ref == -INFINITY ? 0.0f : m_ref;
-          tsum = 0.0f;
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            float v[32];
-            load_cols(colS + 32 * qq, v, 1);
-            transform_cols<SCORE, 32>(v, 32 * qq, tc, m_use, partial);
-            tsum += exp2_pack<32>(v, pk + 16 * qq);
-          }
-        }
-        l += tsum;
-        uint32_t colP = colS;  // P overwrites S
-        if constexpr (C::kSepP) {
-          // S(j) is read: the next Q.K^T may overwrite it. P goes to its own
-          // columns once the previous tile's P.V product has consumed them.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(s_free + x);
-          if (s_it > 1) {
-            ok = __all_sync(0xffffffffu, wait_bounded(pv_done + x, s_it & 1, wd));
-            if (!ok) break;
-            tc_fence_after();
-          }
-          colP = tmem + lane_base + C::kColP + 64u * x;
-        }
-        tmem_st32(colP, *reinterpret_cast<uint32_t(*)[32]>(pk));
-        tmem_st32(colP + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(p_full + x);
-      }
-      if (!ok) break;
-      // epilogue: O / l -> bf16, LSE = ln(sum exp)
-      ok = __all_sync(0xffffffffu, wait_bounded(o_done + x, o_it & 1, wd));
-      if (!ok) break;
-      ++o_it;
-      tc_fence_after();
-      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(colO + 32 * c, r);
-        tmem_ld_wait_regs(r);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
-        uint4* dst = reinterpret_cast<uint4*>(O + 32 * c);
-        if (row_in) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_free + x);
-      if (row_in) p.lse[orow] = l > 0.0f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kWarpMma) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
-// ----------------------------------------------------------------- host side
-template <int D, int SCORE>
-cudaError_t launch_typed(const FwdProblem& p, cudaStream_t stream) {
-  using C = Cfg<D>;
-  CUtensorMap mq, mk, mv;
-  if (!make_map_bf16_3d(&mq, p.q, (long long)p.B * p.Hq, p.Sq, D) ||
-      !make_map_bf16_3d(&mk, p.k, (long long)p.B * p.Hkv, p.Skv, D) ||
-      !make_map_bf16_3d(&mv, p.v, (long long)p.B * p.Hkv, p.Skv, D))
-    return cudaErrorInvalidValue;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(fwd_tc_kernel<D, SCORE>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
-  const int units = p.B * ((p.Sq + kTile - 1) / kTile) * ((p.Hq + 1) / 2);
-  const int grid = units < sm_count() ? units : sm_count();
-  if (grid == 0) return cudaSuccess;
-  fwd_tc_kernel<D, SCORE><<<grid, kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, p);
-  return cudaGetLastError();
-}
-
-}  // namespace
 
 cudaError_t launch_fwd_tc(const FwdProblem& p, cudaStream_t stream) {
+  if (p.variant & ATTN_SCORE_RELBIAS) return launch_fwd_tc_rb(p, stream);
   const int score = ((p.variant & ATTN_SCORE_ALIBI) ? 1 : 0) |
                     ((p.variant & ATTN_SCORE_SOFTCAP) ? 2 : 0);
   if (p.D == 64) {

@@ -128,6 +128,33 @@ BF16_RAGGED = {
 }
 
 
+# Relative-position bias (a per-head table indexed by the query-key distance),
+# alone and with every other term, at both head dims and a ragged length.
+BF16_RELBIAS = {
+    "causal_d64": dict(B=2, Hq=2, Hkv=2, S=512, D=64, causal=True, relbias=True),
+    "doc_window_d128": dict(B=1, Hq=2, Hkv=2, S=768, D=128, causal=True, window=200,
+                            document=True, doc_lo=60, doc_hi=400, relbias=True),
+    "gqa_prefix_softcap_d128": dict(B=1, Hq=4, Hkv=2, S=512, D=128, causal=True, prefix=True,
+                                    softcap=20.0, prefix_lo=50, prefix_hi=300, relbias=True),
+    "alibi_softcap_full_d64": dict(B=1, Hq=2, Hkv=1, S=384, D=64, alibi=True, softcap=5.0,
+                                   relbias=True),
+    "ragged_causal_d128_q200_k333": dict(B=1, Hq=2, Hkv=2, Sq=200, Skv=333, D=128,
+                                         causal=True, relbias=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BF16_RELBIAS))
+def test_bf16_rel_bias(name):
+    w = make_workload(0, seed=500 + sorted(BF16_RELBIAS).index(name), **BF16_RELBIAS[name])
+    run_and_check(w)
+
+
+def test_fp32_rel_bias():
+    w = make_workload(0, seed=520, dtype="f32", B=1, Hq=2, Hkv=1, Sq=150, Skv=211, D=64,
+                      causal=True, window=90, alibi=True, relbias=True)
+    run_and_check(w)
+
+
 @pytest.mark.parametrize("name", sorted(BF16_RAGGED))
 def test_bf16_ragged(name):
     w = make_workload(0, seed=400 + sorted(BF16_RAGGED).index(name), **BF16_RAGGED[name])
