@@ -155,6 +155,19 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
                      int B, int Hq, int Hkv, int Sq, int Skv, int D,
                      unsigned variant, const attn_params* p, struct CUstream_st* stream);
 
+/* Jagged batches (FlexAttention page, variant list: irregular tensors): n
+ * sequences packed back to back with no padding, cu_seqlens (device int32
+ * [n + 1]: 0 = cu[0] <= cu[1] <= ... <= cu[n] = total) their cumulative
+ * lengths. Writes doc_id (device int32 [total]) = the index of the sequence
+ * each packed position belongs to. With B = 1, S = total and
+ * ATTN_MASK_DOCUMENT (plus ATTN_MASK_CAUSAL etc.) the forward, backward and
+ * block mask then attend within each sequence only. Asynchronous on
+ * `stream`; ATTN_ERR_INVALID_ARG for n < 1, total < 0 or null pointers. The
+ * lengths are not validated on the device: non-monotone input gives
+ * undefined ids. */
+attn_status attn_doc_ids_from_seqlens(const int* cu_seqlens, int n, int total, int* doc_id,
+                                      struct CUstream_st* stream);
+
 /* Bytes of device buffer build_block_mask() needs (256-byte aligned pieces). */
 size_t attn_block_mask_bytes(int B, int Sq, int Skv, int transposed);
 

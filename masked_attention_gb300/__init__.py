@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, u,
                                        P, vp]
         L.attn_bwd_noalloc.restype = i
+        L.attn_doc_ids_from_seqlens.argtypes = [vp, i, i, vp, vp]
+        L.attn_doc_ids_from_seqlens.restype = i
         L.attn_check_status.argtypes = [vp, vp]
         L.attn_check_status.restype = i
         L.attn_status_str.argtypes = [i]
@@ -231,6 +233,24 @@ def attn_fwd(q, k, v, o, lse, variant: int = 0, *, B=None, Hq=None, Hkv=None, Sq
     st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
                         variant, ctypes.byref(p), _stream(stream))
     _check(st, "attn_fwd")
+
+
+def doc_ids_from_seqlens(cu_seqlens, total: Optional[int] = None, doc_id=None,
+                         stream=None):
+    """Jagged batches: per-position sequence index of ``total`` packed
+    positions from the cumulative lengths ``cu_seqlens`` (int32 CUDA tensor,
+    n + 1 entries starting at 0). Use the result as ``doc_id`` ([1, total])
+    with ``MASK_DOCUMENT`` and B = 1 to attend within each sequence only."""
+    import torch
+    n = cu_seqlens.numel() - 1
+    if total is None:
+        total = int(cu_seqlens[-1].item())
+    if doc_id is None:
+        doc_id = torch.empty(1, total, dtype=torch.int32, device=cu_seqlens.device)
+    st = lib().attn_doc_ids_from_seqlens(_ptr(cu_seqlens), n, total, _ptr(doc_id),
+                                         _stream(stream))
+    _check(st, "attn_doc_ids_from_seqlens")
+    return doc_id
 
 
 def attn_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, variant: int = 0, *,
