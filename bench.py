@@ -360,6 +360,24 @@ def run_ours(args, rank: int, world: int) -> None:
     fkw = dict(mkw, softcap=w.softcap or 0.0)
     if w.relbias:
         fkw["rel_bias"] = w.rel_bias.to(dev)
+    if args.paged:
+        # the same K/V in a paged pool [B * pages, Hkv, page, D] under a shuffled page table
+        ps = args.paged
+        pps = (w.Skv + ps - 1) // ps
+        pad = pps * ps - w.Skv
+        gen = torch.Generator().manual_seed(w.seed)
+        perm = torch.randperm(w.B * pps, generator=gen)
+
+        def pool(t):
+            t = torch.nn.functional.pad(t, (0, 0, 0, pad)) if pad else t
+            pages = t.reshape(w.B, w.Hkv, pps, ps, w.D).permute(0, 2, 1, 3, 4)
+            out = torch.empty(w.B * pps, w.Hkv, ps, w.D, dtype=t.dtype, device=dev)
+            out[perm.to(dev)] = pages.reshape(w.B * pps, w.Hkv, ps, w.D)
+            return out
+
+        k, v = pool(k), pool(v)
+        fkw.update(page_table=perm.reshape(w.B, pps).to(torch.int32).to(dev), page_size=ps,
+                   Skv=w.Skv)
 
     def step():
         bm = M.build_block_mask(variant & 0xF, w.B, w.Sq, w.Skv, buf=bm_buf, stream=stream, **mkw)
@@ -403,7 +421,7 @@ def run_ours(args, rank: int, world: int) -> None:
     total_s, fwd_s = max_over_ranks(total_s, fwd_s)
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.paged:
         # end to end through the public API: pinned host inputs in, O and LSE out
         hq, hk, hv = (t.pin_memory() for t in (w.q, w.k, w.v))
         ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
@@ -452,7 +470,7 @@ def run_ours(args, rank: int, world: int) -> None:
                      "unit": "TFLOP/s", "frac": fwd_tflops / peak,
                      "traffic": (profiled_traffic(digest)
                                  if args.workload == WORKLOAD and not args.batch
-                                 and not args.relbias else None),
+                                 and not args.relbias and not args.paged else None),
                      "kernel": f"fwd_tc_kernel<D={w.D}>",
                      "peak_source": ("measured bf16 dense burst (MEASURED_PEAKS.json)"
                                      if peak_kind == "measured" else "fallback 1.9 PFLOP/s")},
@@ -523,6 +541,8 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override B (profiling cases only)")
     ap.add_argument("--workload", type=int, default=WORKLOAD, choices=[2, 3, 4, 5],
                     help="diagnostic runs on the other bf16 workloads (forward only)")
+    ap.add_argument("--paged", type=int, default=0, choices=[0, 16, 32, 64, 128],
+                    help="diagnostic: read K/V from a paged cache with this page size")
     ap.add_argument("--relbias", action="store_true",
                     help="diagnostic: add a relative-position bias table to the workload")
     ap.add_argument("--backward", action="store_true",

@@ -137,6 +137,17 @@ typedef struct attn_params {
                                   runs out after timeout_ns and the call reports
                                   ATTN_ERR_TIMEOUT (tests the bounded-wait path; no GPU
                                   fault is involved) */
+  /* Paged K/V cache (variant list: PagedAttention), bf16 forward only. NULL
+   * page_table: k and v are contiguous [B,Hkv,Skv,D]. Otherwise k and v are
+   * page pools [num_pages][Hkv][page_size][D] and key j of batch b is row
+   * j % page_size of page page_table[b * pages_per_seq + j / page_size].
+   * page_size is 16, 32, 64 or 128; pages_per_seq * page_size >= Skv. Rows
+   * of the last page past Skv are read (and masked): they must hold finite
+   * values. A page index outside [0, num_pages) reads zeros. */
+  const int* page_table;       /* device int32 [B][pages_per_seq], or NULL */
+  int page_size;
+  int pages_per_seq;
+  int num_pages;
 } attn_params;
 
 #define ATTN_FAULT_NO_LOADS 1u

@@ -52,7 +52,9 @@ class attn_params(ctypes.Structure):
                 ("doc_id", ctypes.c_void_p), ("prefix_len", ctypes.c_void_p),
                 ("block_mask", ctypes.POINTER(attn_block_mask)), ("status", ctypes.c_void_p),
                 ("timeout_ns", ctypes.c_ulonglong), ("rel_bias", ctypes.c_void_p),
-                ("fault_inject", ctypes.c_uint)]
+                ("fault_inject", ctypes.c_uint), ("page_table", ctypes.c_void_p),
+                ("page_size", ctypes.c_int), ("pages_per_seq", ctypes.c_int),
+                ("num_pages", ctypes.c_int)]
 
 
 _lib = None
@@ -216,20 +218,32 @@ def attn_fwd(q, k, v, o, lse, variant: int = 0, *, B=None, Hq=None, Hkv=None, Sq
              Skv=None, D=None, dtype: Optional[int] = None, scale: float = 0.0, window: int = 0,
              softcap: float = 0.0, alibi_slopes=None, doc_id=None, prefix_len=None,
              block_mask: Optional[BlockMask] = None, status=None, timeout_ns: int = 0,
-             fault_inject: int = 0, rel_bias=None, stream=None) -> None:
+             fault_inject: int = 0, rel_bias=None, page_table=None, page_size: int = 0,
+             stream=None) -> None:
     """O and LSE of masked attention; writes ``o`` and ``lse`` in place.
+
+    Paged K/V cache: ``k``/``v`` are page pools [num_pages, Hkv, page_size, D]
+    and ``page_table`` [B, pages_per_seq] int32 maps logical to physical pages;
+    pass ``Skv`` (the shapes cannot tell it).
 
     ``q`` [B,Hq,Sq,D], ``k``/``v`` [B,Hkv,Skv,D], ``o`` like ``q``, ``lse`` fp32
     [B,Hq,Sq]. Shapes come from the tensors unless given explicitly (needed
     when raw addresses are passed)."""
     if B is None:
         B, Hq, Sq, D = q.shape
-        Hkv, Skv = k.shape[1], k.shape[2]
+        Hkv = k.shape[1]
+        if Skv is None:
+            Skv = k.shape[2]
     if dtype is None:
         import torch
         dtype = F32 if q.dtype == torch.float32 else BF16
     p = _params(dtype, scale, window, softcap, alibi_slopes, doc_id, prefix_len, block_mask,
                 status, timeout_ns, fault_inject, rel_bias)
+    if page_table is not None:
+        p.page_table = _ptr(page_table)
+        p.page_size = page_size
+        p.pages_per_seq = page_table.shape[1]
+        p.num_pages = k.shape[0]
     st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
                         variant, ctypes.byref(p), _stream(stream))
     _check(st, "attn_fwd")

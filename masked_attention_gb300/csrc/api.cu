@@ -160,6 +160,10 @@ attn_status fill_problem(FwdProblem& f, const void* q, const void* k, const void
   f.status = p->status;  // resolved by resolve_status() once every check has passed
   f.timeout_ns = p->timeout_ns ? p->timeout_ns : 4000000000ull;
   f.fault_inject = p->fault_inject;
+  f.page_table = p->page_table;
+  f.page_size = p->page_size;
+  f.pages_per_seq = p->pages_per_seq;
+  f.num_pages = p->num_pages;
   return ATTN_OK;
 }
 
@@ -249,6 +253,16 @@ MATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void
     return ATTN_ERR_MISALIGNED;
   st = check_block_mask(p->block_mask, variant, p, B, Sq, Skv, false);
   if (st != ATTN_OK) return st;
+  if (p->page_table) {  // paged K/V cache: bf16 tensor-core forward only
+    if (p->dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+    const int ps = p->page_size;
+    if (ps != 16 && ps != 32 && ps != 64 && ps != 128) return ATTN_ERR_UNSUPPORTED;
+    if (p->num_pages < 1 || p->pages_per_seq < 1 ||
+        (long long)p->pages_per_seq * ps < (long long)Skv)
+      return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(p->page_table) && (reinterpret_cast<uintptr_t>(p->page_table) & 3))
+      return ATTN_ERR_MISALIGNED;
+  }
   st = resolve_status(f);
   if (st != ATTN_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -282,6 +296,7 @@ MATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, cons
   if (st != ATTN_OK) return st;
   if (p->dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   if (variant & ATTN_SCORE_RELBIAS) return ATTN_ERR_UNSUPPORTED;  // forward only
+  if (p->page_table) return ATTN_ERR_UNSUPPORTED;                 // forward only
   if (Sq % kTile != 0 || Skv % kTile != 0) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || Sq == 0 || Skv == 0) return ATTN_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)

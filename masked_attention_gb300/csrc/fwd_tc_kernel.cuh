@@ -152,6 +152,30 @@ __device__ __forceinline__ int doc_at(const int* docb, int j, int Skv) {
   return j < Skv ? docb[j] : -1;
 }
 
+// TMA loads of one 128-row K or V tile of (b, kv head hk) at key tile kt:
+// one box per 64 columns, or, from a paged cache, one box per page and 64
+// columns (pages past the last one holding keys repeat it: their rows are
+// masked). The boxes of page q land q * page_size rows into the tile, a
+// multiple of the 8-row swizzle period.
+template <int kBoxes, int kBoxBytes>
+__device__ __forceinline__ void load_kv_tile(uint8_t* dst, const CUtensorMap* map,
+                                             uint64_t* bar, const FwdProblem& p, int b, int hk,
+                                             int kt) {
+  if (!p.page_table) {
+    for (int bx = 0; bx < kBoxes; ++bx)
+      tma_load_3d(dst + bx * kBoxBytes, map, bar, bx * 64, kt * kTile, b * p.Hkv + hk);
+    return;
+  }
+  const int ps = p.page_size, per = kTile / ps;
+  const int last = (p.Skv + ps - 1) / ps - 1;
+  for (int q = 0; q < per; ++q) {
+    const int lp = min(kt * per + q, last);
+    const int phys = p.page_table[(size_t)b * p.pages_per_seq + lp];
+    for (int bx = 0; bx < kBoxes; ++bx)
+      tma_load_3d(dst + bx * kBoxBytes + q * ps * 128, map, bar, bx * 64, 0, phys * p.Hkv + hk);
+  }
+}
+
 // Per-row, per-tile constants of the score transform.
 struct TileCtx {
   float sl2, sc, cl2, slope, slope2, scale, inv_cap;
@@ -473,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++q_it;
       for (int j = 0; j < n && ok; ++j) {
         const int kt = U.kt(j);
-        const int slices[2] = {U.b * p.Hkv + hk0, U.b * p.Hkv + hk1};
+        const int hks[2] = {hk0, hk1};
         // order: K_A, [K_B], V_A, [V_B]
         for (int t = 0; t < (shared ? 2 : 4) && ok; ++t) {
           const int per = shared ? 1 : 2;
@@ -485,9 +509,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           if (leader) {
             mbar_arrive_expect_tx(slot_full + slot, C::kTileBytes);
-            for (int bx = 0; bx < C::kBoxes; ++bx)
-              tma_load_3d(sSlots + slot * C::kTileBytes + bx * C::kBoxBytes, is_v ? &tm_v : &tm_k,
-                          slot_full + slot, bx * 64, kt * kTile, slices[x]);
+            load_kv_tile<C::kBoxes, C::kBoxBytes>(sSlots + slot * C::kTileBytes,
+                                                  is_v ? &tm_v : &tm_k, slot_full + slot, p,
+                                                  U.b, hks[x], kt);
           }
           __syncwarp();
           ++slot_it;
@@ -959,9 +983,12 @@ template <int D, int SCORE>
 cudaError_t launch_typed(const FwdProblem& p, cudaStream_t stream) {
   using C = Cfg<D>;
   CUtensorMap mq, mk, mv;
+  const bool paged = p.page_table != nullptr;
+  const long long kv_slices = paged ? (long long)p.num_pages * p.Hkv : (long long)p.B * p.Hkv;
+  const int kv_rows = paged ? p.page_size : p.Skv;
   if (!make_map_bf16_3d(&mq, p.q, (long long)p.B * p.Hq, p.Sq, D) ||
-      !make_map_bf16_3d(&mk, p.k, (long long)p.B * p.Hkv, p.Skv, D) ||
-      !make_map_bf16_3d(&mv, p.v, (long long)p.B * p.Hkv, p.Skv, D))
+      !make_map_bf16_3d(&mk, p.k, kv_slices, kv_rows, D, paged ? p.page_size : kTile) ||
+      !make_map_bf16_3d(&mv, p.v, kv_slices, kv_rows, D, paged ? p.page_size : kTile))
     return cudaErrorInvalidValue;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;

@@ -46,12 +46,14 @@ inline bool make_map_bf16(CUtensorMap* map, const void* base, long long rows, in
 
 // 3-D view [B*H][S][D] of the same tensor (box 64 columns x 128 rows x 1
 // slice): a tile that runs past S reads zeros instead of the next slice.
-inline bool make_map_bf16_3d(CUtensorMap* map, const void* base, long long slices, int S, int D) {
+// box_rows < 128 serves a paged K/V cache: one box per page of box_rows rows.
+inline bool make_map_bf16_3d(CUtensorMap* map, const void* base, long long slices, int S, int D,
+                             int box_rows = 128) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)slices};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

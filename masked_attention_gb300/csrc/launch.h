@@ -22,6 +22,8 @@ struct FwdProblem {
   int* status;
   uint64_t timeout_ns;
   unsigned fault_inject;  // ATTN_FAULT_NO_LOADS: the load warp issues nothing
+  const int* page_table;  // paged K/V cache [B][pages_per_seq], or nullptr (contiguous)
+  int page_size, pages_per_seq, num_pages;
 };
 
 struct BwdProblem {
