@@ -143,7 +143,8 @@ typedef struct attn_params {
    * j % page_size of page page_table[b * pages_per_seq + j / page_size].
    * page_size is 16, 32, 64 or 128; pages_per_seq * page_size >= Skv. Rows
    * of the last page past Skv are read (and masked): they must hold finite
-   * values. A page index outside [0, num_pages) reads zeros. */
+   * values. A page index outside [0, num_pages) reads zeros. Not combined
+   * with ATTN_SCORE_RELBIAS (ATTN_ERR_UNSUPPORTED). */
   const int* page_table;       /* device int32 [B][pages_per_seq], or NULL */
   int page_size;
   int pages_per_seq;

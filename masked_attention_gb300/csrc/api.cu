@@ -255,6 +255,7 @@ MATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void
   if (st != ATTN_OK) return st;
   if (p->page_table) {  // paged K/V cache: bf16 tensor-core forward only
     if (p->dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+    if (variant & ATTN_SCORE_RELBIAS) return ATTN_ERR_UNSUPPORTED;
     const int ps = p->page_size;
     if (ps != 16 && ps != 32 && ps != 64 && ps != 128) return ATTN_ERR_UNSUPPORTED;
     if (p->num_pages < 1 || p->pages_per_seq < 1 ||

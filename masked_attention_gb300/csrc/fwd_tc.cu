@@ -1,11 +1,14 @@
 // Launches of the bf16 tensor-core forward (kernel in fwd_tc_kernel.cuh) for
-// the score_mod variants without the relative-position bias; the variants
-// with it are compiled in fwd_tc_rb.cu, so the two builds run in parallel.
+// the score_mod variants without the relative-position bias over contiguous
+// K/V; the variants with the bias (fwd_tc_rb.cu) and over a paged cache
+// (fwd_tc_paged.cu) are compiled in their own files, so the builds run in
+// parallel.
 #include "fwd_tc_kernel.cuh"
 
 namespace mattn {
 
 cudaError_t launch_fwd_tc(const FwdProblem& p, cudaStream_t stream) {
+  if (p.page_table) return launch_fwd_tc_paged(p, stream);
   if (p.variant & ATTN_SCORE_RELBIAS) return launch_fwd_tc_rb(p, stream);
   const int score = ((p.variant & ATTN_SCORE_ALIBI) ? 1 : 0) |
                     ((p.variant & ATTN_SCORE_SOFTCAP) ? 2 : 0);

@@ -157,22 +157,25 @@ __device__ __forceinline__ int doc_at(const int* docb, int j, int Skv) {
 // columns (pages past the last one holding keys repeat it: their rows are
 // masked). The boxes of page q land q * page_size rows into the tile, a
 // multiple of the 8-row swizzle period.
-template <int kBoxes, int kBoxBytes>
+template <int kBoxes, int kBoxBytes, bool kPaged>
 __device__ __forceinline__ void load_kv_tile(uint8_t* dst, const CUtensorMap* map,
-                                             uint64_t* bar, const FwdProblem& p, int b, int hk,
+                                             uint64_t* bar, const int* page_table, int ps,
+                                             int pages_per_seq, int Skv, int Hkv, int b, int hk,
                                              int kt) {
-  if (!p.page_table) {
+  if constexpr (!kPaged) {
+#pragma unroll
     for (int bx = 0; bx < kBoxes; ++bx)
-      tma_load_3d(dst + bx * kBoxBytes, map, bar, bx * 64, kt * kTile, b * p.Hkv + hk);
+      tma_load_3d(dst + bx * kBoxBytes, map, bar, bx * 64, kt * kTile, b * Hkv + hk);
     return;
   }
-  const int ps = p.page_size, per = kTile / ps;
-  const int last = (p.Skv + ps - 1) / ps - 1;
+  const int per = kTile / ps;
+  const int last = (Skv + ps - 1) / ps - 1;
   for (int q = 0; q < per; ++q) {
     const int lp = min(kt * per + q, last);
-    const int phys = p.page_table[(size_t)b * p.pages_per_seq + lp];
+    const int phys = page_table[(size_t)b * pages_per_seq + lp];
+#pragma unroll
     for (int bx = 0; bx < kBoxes; ++bx)
-      tma_load_3d(dst + bx * kBoxBytes + q * ps * 128, map, bar, bx * 64, 0, phys * p.Hkv + hk);
+      tma_load_3d(dst + bx * kBoxBytes + q * ps * 128, map, bar, bx * 64, 0, phys * Hkv + hk);
   }
 }
 
@@ -390,7 +393,9 @@ __device__ __forceinline__ float exp2_pack(const float* s, uint32_t* pk) {
   return a.x + a.y;
 }
 
-template <int D, int SCORE>
+// PAGED: K/V come from a paged cache (a separate instantiation: the page-table
+// code in the load warp measurably slowed the contiguous kernel).
+template <int D, int SCORE, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
@@ -509,9 +514,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           if (leader) {
             mbar_arrive_expect_tx(slot_full + slot, C::kTileBytes);
-            load_kv_tile<C::kBoxes, C::kBoxBytes>(sSlots + slot * C::kTileBytes,
-                                                  is_v ? &tm_v : &tm_k, slot_full + slot, p,
-                                                  U.b, hks[x], kt);
+            load_kv_tile<C::kBoxes, C::kBoxBytes, PAGED>(sSlots + slot * C::kTileBytes,
+                                                  is_v ? &tm_v : &tm_k, slot_full + slot,
+                                                  p.page_table, p.page_size, p.pages_per_seq,
+                                                  p.Skv, p.Hkv, U.b, hks[x], kt);
           }
           __syncwarp();
           ++slot_it;
@@ -979,11 +985,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ----------------------------------------------------------------- host side
-template <int D, int SCORE>
+template <int D, int SCORE, bool PAGED = false>
 cudaError_t launch_typed(const FwdProblem& p, cudaStream_t stream) {
   using C = Cfg<D>;
   CUtensorMap mq, mk, mv;
-  const bool paged = p.page_table != nullptr;
+  const bool paged = PAGED;
   const long long kv_slices = paged ? (long long)p.num_pages * p.Hkv : (long long)p.B * p.Hkv;
   const int kv_rows = paged ? p.page_size : p.Skv;
   if (!make_map_bf16_3d(&mq, p.q, (long long)p.B * p.Hq, p.Sq, D) ||
@@ -993,14 +999,14 @@ cudaError_t launch_typed(const FwdProblem& p, cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(fwd_tc_kernel<D, SCORE>,
+    attr_err = cudaFuncSetAttribute(fwd_tc_kernel<D, SCORE, PAGED>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int units = p.B * ((p.Sq + kTile - 1) / kTile) * ((p.Hq + 1) / 2);
   const int grid = units < sm_count() ? units : sm_count();
   if (grid == 0) return cudaSuccess;
-  fwd_tc_kernel<D, SCORE><<<grid, kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, p);
+  fwd_tc_kernel<D, SCORE, PAGED><<<grid, kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 

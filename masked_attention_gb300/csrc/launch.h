@@ -45,7 +45,8 @@ cudaError_t launch_block_mask(const MaskArgs& m, int B, int Sq, int Skv, int tra
 
 cudaError_t launch_fwd_f32(const FwdProblem& p, cudaStream_t stream);
 cudaError_t launch_fwd_tc(const FwdProblem& p, cudaStream_t stream);
-cudaError_t launch_fwd_tc_rb(const FwdProblem& p, cudaStream_t stream);  // relative bias
+cudaError_t launch_fwd_tc_rb(const FwdProblem& p, cudaStream_t stream);     // relative bias
+cudaError_t launch_fwd_tc_paged(const FwdProblem& p, cudaStream_t stream);  // paged K/V
 cudaError_t launch_bwd_tc(const BwdProblem& p, cudaStream_t stream);
 
 }  // namespace mattn
