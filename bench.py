@@ -328,6 +328,20 @@ def config_dict(w):
             "step": "build_block_mask + attn_fwd"}
 
 
+def reduce_max(vals, world: int, device) -> tuple:
+    """Element-wise maximum of ``vals`` over the ranks (each rank's timed
+    seconds, so the slowest rank sets the job's time); ``vals`` itself when
+    there is one rank. ``device``: where the collective runs (the GPU under
+    NCCL, the CPU under gloo)."""
+    if world == 1:
+        return tuple(vals)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(vals, device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return tuple(float(x) for x in t)
+
+
 def run_ours(args, rank: int, world: int) -> None:
     import torch
     import torch.distributed as dist
@@ -389,11 +403,7 @@ def run_ours(args, rank: int, world: int) -> None:
         torch.cuda.synchronize()
 
     def max_over_ranks(*vals):
-        if world == 1:
-            return vals
-        t = torch.tensor(vals, device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return tuple(float(x) for x in t)
+        return reduce_max(vals, world, dev)
 
     for _ in range(max(args.warmup, 3)):
         flush.fill_(1)
