@@ -17,7 +17,8 @@
 //   warps 4-7  softmax for head B
 //   warp  8    TMA producer: Q tiles once per unit, then K/V tiles into a ring
 //   warp  9    MMA issuer (one thread) and TMEM owner
-//   warps 10-11 idle
+//   warp  10   second MMA issuer at D = 64 (head B), idle at D = 128
+//   warp  11   idle
 // The third warpgroup hands registers to the softmax warpgroups (setmaxnreg).
 // Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A, O_B (D columns
 // each) from 256. P (bf16) overwrites the first 64 columns of its S tile and
@@ -59,11 +60,16 @@ struct Cfg {
   static constexpr int kNumBars = 16 + 2 * kSlots;
   // per-warp document ids, read as int4: 16-byte aligned
   static constexpr int kOffDoc = (kOffBars + kNumBars * 8 + 15) & ~15;
-  // per-warp windows of the relative-position bias, double-buffered by tile:
-  // float [8 warps][2][kRbWindow]
+  // Per-warp area of kWarpArea bytes, used in the key-tile loop for the two
+  // windows of the relative-position bias (float [2][kRbWindow], double-
+  // buffered by tile) and in the epilogue to stage 32 rows x 32 bf16 columns
+  // of the output.
   static constexpr int kRbWindow = 160;
-  static constexpr int kOffRb = kOffDoc + 8 * kTile * 4;
-  static constexpr int kOffMisc = kOffRb + 8 * 2 * kRbWindow * 4;
+  static constexpr int kStageBytes = 32 * 32 * 2;
+  static constexpr int kWarpArea = kStageBytes;
+  static_assert(2 * kRbWindow * 4 <= kWarpArea, "bias windows fit the per-warp area");
+  static constexpr int kOffArea = kOffDoc + 8 * kTile * 4;
+  static constexpr int kOffMisc = kOffArea + 8 * kWarpArea;
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;     // slack for 1024-byte alignment
   static constexpr uint32_t kColO0 = 256;
@@ -82,6 +88,7 @@ struct Cfg {
   static constexpr uint32_t kColP = 384;
   static_assert(!kSepP || kColP + 128 <= 512, "tensor memory columns");
   static_assert(kOffDoc % 16 == 0 && (kTile * 4) % 16 == 0, "int4 reads of document ids");
+  static_assert(kOffArea % 16 == 0, "uint4 staging of the output");
   static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -150,6 +157,12 @@ __device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp)
 // masked by the key-length bound anyway).
 __device__ __forceinline__ int doc_at(const int* docb, int j, int Skv) {
   return j < Skv ? docb[j] : -1;
+}
+
+// A key tile is masked element by element when the lists call it partial or
+// it runs past Skv (its columns from Skv - j0 on hold zero-filled keys).
+__device__ __forceinline__ bool elementwise_tile(const Unit& U, int j, int kt, int Skv) {
+  return U.partial(j) || (kt + 1) * kTile > Skv;
 }
 
 // TMA loads of one 128-row K or V tile of (b, kv head hk) at key tile kt:
@@ -420,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* slot_full = bars + 16;
   uint64_t* slot_empty = bars + 16 + C::kSlots;
   int* sdoc = reinterpret_cast<int*>(smem + C::kOffDoc);
-  float* srb = reinterpret_cast<float*>(smem + C::kOffRb);
+  uint8_t* sarea = smem + C::kOffArea;  // per-warp bias windows / output staging
   uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -737,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t colS = tmem + lane_base + 128u * x;
     const uint32_t colO = tmem + lane_base + C::kColO0 + D * x;
     int* wdoc = sdoc + warp * kTile;   // this warp's copy of the key tile's document ids
-    float* wrb = srb + warp * 2 * C::kRbWindow;  // this warp's two bias windows
+    float* wrb = reinterpret_cast<float*>(sarea + warp * C::kWarpArea);  // two bias windows
     const float sl2 = p.score.scale * kLog2e;              // raw score -> log2 units
     const float sc = p.score.scale / p.score.softcap;      // raw score -> tanh argument
     const float cl2 = p.score.softcap * kLog2e;            // tanh -> log2 units
@@ -779,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rb_first = U.qt * kTile + (warp & 3) * 32 - 127 + p.score.rb_zero;  // minus j0
       if (rtab) rb_fill<C::kRbWindow>(wrb, rtab, p.score.rb_len, rb_first - kt_cur * kTile);
       int dcur[4] = {0, 0, 0, 0};
-      if (docb && U.partial(0)) {
+      if (docb && elementwise_tile(U, 0, kt_cur, p.Skv)) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) dcur[c] = doc_at(docb, kt_cur * kTile + lane + 32 * c, p.Skv);
       }
@@ -788,15 +801,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kt = kt_cur;
         const int kt_n2 = j + 2 < n ? U.kt(j + 2) : 0;
         int dnext[4] = {0, 0, 0, 0};
-        if (docb && j + 1 < n && U.partial(j + 1)) {
+        if (docb && j + 1 < n && elementwise_tile(U, j + 1, kt_n1, p.Skv)) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) dnext[c] = doc_at(docb, kt_n1 * kTile + lane + 32 * c, p.Skv);
         }
         const int j0 = kt * kTile;
-        // a key tile that runs past Skv is masked like a partial tile: its
-        // columns from Skv - j0 on hold zero-filled keys
-        const bool tail = j0 + kTile > p.Skv;
-        const bool partial = U.partial(j) || tail;
+        const bool partial = elementwise_tile(U, j, kt, p.Skv);
         if (partial && docb) {
           __syncwarp();
 #pragma unroll
@@ -946,32 +956,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(p_full + x);
       }
       if (!ok) break;
-      // epilogue: O / l -> bf16, LSE = ln(sum exp)
+      // epilogue: O / l -> bf16, LSE = ln(sum exp); the LSE store goes first
+      // so that it does not queue behind the output's
+      if (row_in) p.lse[orow] = l > 0.0f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
       ok = __all_sync(0xffffffffu, wait_bounded(o_done + x, o_it & 1, wd));
       if (!ok) break;
       ++o_it;
       tc_fence_after();
+      // O is written through shared memory so that the global stores are
+      // coalesced: per 32 columns, each thread puts its row's 64 bytes in the
+      // warp's staging area (16-byte units swizzled by (row >> 1) & 3: no bank
+      // conflicts either way), then a store instruction covers 8 whole
+      // 64-byte row segments instead of one 16-byte piece of 32 rows.
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+      uint4* stg = reinterpret_cast<uint4*>(sarea + warp * C::kWarpArea);
+      const int row0 = U.qt * kTile + (warp & 3) * 32;  // the warp's first row
+      __nv_bfloat16* Oh = static_cast<__nv_bfloat16*>(p.o) + (size_t)(U.b * p.Hq + h) * p.Sq * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(colO + 32 * c, r);
-        tmem_ld_wait_regs(r);
-        uint32_t pk[16];
+      for (int cc = 0; cc < D / 64; ++cc) {
+        uint32_t r[64];
+        tmem_ld32(colO + 64 * cc, *reinterpret_cast<uint32_t(*)[32]>(r));
+        tmem_ld32(colO + 64 * cc + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+        tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(r));
+        tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(r + 32));
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
-        uint4* dst = reinterpret_cast<uint4*>(O + 32 * c);
-        if (row_in) {
+        for (int hh = 0; hh < 2; ++hh) {
+          const int c = 2 * cc + hh;  // 32-column chunk
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(r[32 * hh + 2 * e]) * inv,
+                                __uint_as_float(r[32 * hh + 2 * e + 1]) * inv);
+          __syncwarp();  // the previous chunk's reads of the staging area are done
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            stg[lane * 4 + (e ^ ((lane >> 1) & 3))] =
+                make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int rr = 8 * k + (lane >> 2), e = lane & 3;
+            const uint4 v = stg[rr * 4 + (e ^ ((rr >> 1) & 3))];
+            if (row0 + rr < p.Sq)
+              *reinterpret_cast<uint4*>(Oh + (size_t)(row0 + rr) * D + 32 * c + 8 * e) = v;
+          }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_free + x);
-      if (row_in) p.lse[orow] = l > 0.0f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
 

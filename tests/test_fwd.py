@@ -125,6 +125,14 @@ BF16_RAGGED = {
     "single_row_d128": dict(B=1, Hq=1, Hkv=1, Sq=1, Skv=1, D=128, causal=True),
     "window_empty_rows_d64": dict(B=1, Hq=2, Hkv=2, Sq=140, Skv=7, D=64, causal=True,
                                   window=3),
+    # Document masking alone with a last key tile that the block mask calls
+    # full (one document over its keys and the last query tile's rows) but
+    # that runs past Skv: the kernel masks it element by element and needs
+    # its keys' document ids, which differ from 0 here.
+    "doc_full_tail_d64_s200": dict(B=2, Hq=2, Hkv=2, S=200, D=64, document=True,
+                                   doc_lengths=[[128, 72], [50, 78, 72]]),
+    "doc_full_tail_gqa_d128_q300_k200": dict(B=1, Hq=4, Hkv=2, Sq=300, Skv=200, D=128,
+                                             document=True, doc_lengths=[[100, 28, 172]]),
 }
 
 
