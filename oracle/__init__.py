@@ -8,8 +8,8 @@ invariants, brute force and a library special case.
 """
 from .attention import (Spec, alibi_slopes, mask_mod, score_mod, score_mod_grad,
                         attention_forward, attention_backward, block_mask, BlockMask,
-                        kept_per_row)
+                        kept_per_row, combine_partials)
 
 __all__ = ["Spec", "alibi_slopes", "mask_mod", "score_mod", "score_mod_grad",
            "attention_forward", "attention_backward", "block_mask", "BlockMask",
-           "kept_per_row"]
+           "kept_per_row", "combine_partials"]

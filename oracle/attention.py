@@ -59,6 +59,12 @@ class Spec:
     # is added for query-key distance d = i - j (rel_bias_zero = Skv - 1)
     rel_bias: Optional[np.ndarray] = None
     rel_bias_zero: int = 0
+    # Absolute position of query row 0 and of key 0 (a shard of a longer
+    # sequence, as in context-parallel attention): every mask term, the ALiBi
+    # bias and the document ids use absolute positions q_offset + i and
+    # kv_offset + j; doc_id then covers max(q_offset + Sq, kv_offset + Skv).
+    q_offset: int = 0
+    kv_offset: int = 0
 
 
 def alibi_slopes(Hq: int) -> np.ndarray:
@@ -165,14 +171,16 @@ def attention_forward(q, k, v, spec: Spec, rows: Optional[Sequence[int]] = None,
     row_idx = np.arange(Sq) if rows is None else np.asarray(rows, dtype=np.int64)
     pairs = [(b, h) for b in range(B) for h in range(Hq)] if heads is None else heads
     j = np.arange(Skv)[None, :]
+    ja = j + spec.kv_offset  # absolute key positions
     slab = _slab_rows(Skv)
     for b, h in pairs:
         hk = h // group
         for start in range(0, len(row_idx), slab):
             i = row_idx[start:start + slab][:, None]
+            ia = i + spec.q_offset  # absolute query positions
             s = scale * (q[b, h, i[:, 0], :] @ k[b, hk].T)
-            s = score_mod(spec, s, h, Hq, i, j)
-            keep = mask_mod(spec, b, i, j)
+            s = score_mod(spec, s, h, Hq, ia, ja)
+            keep = mask_mod(spec, b, ia, ja)
             # pass 1: row maximum over kept entries
             m = np.where(keep, s, NEG_INF).max(axis=1)
             m_safe = np.where(np.isfinite(m), m, 0.0)
@@ -217,8 +225,8 @@ def attention_backward(q, k, v, do, spec: Spec, heads: Optional[Sequence[tuple]]
     dK = np.zeros_like(k)
     dV = np.zeros_like(v)
     pairs = [(b, h) for b in range(B) for h in range(Hq)] if heads is None else heads
-    i = np.arange(Sq)[:, None]
-    j = np.arange(Skv)[None, :]
+    i = np.arange(Sq)[:, None] + spec.q_offset   # absolute positions
+    j = np.arange(Skv)[None, :] + spec.kv_offset
     for b, h in pairs:
         hk = h // group
         s = scale * (q[b, h] @ k[b, hk].T)
@@ -262,8 +270,8 @@ def block_mask(spec: Spec, B: int, Sq: int, Skv: int, BM: int = 128, BN: int = 1
     state = np.zeros((B, nq, nkv), dtype=np.int8)
     for b in range(B):
         for qt in range(nq):
-            i = np.arange(qt * BM, min((qt + 1) * BM, Sq))[:, None]
-            j = np.arange(Skv)[None, :]
+            i = np.arange(qt * BM, min((qt + 1) * BM, Sq))[:, None] + spec.q_offset
+            j = np.arange(Skv)[None, :] + spec.kv_offset
             keep = mask_mod(spec, b, i, j)
             for kt in range(nkv):
                 tile = keep[:, kt * BN:min((kt + 1) * BN, Skv)]
@@ -287,10 +295,40 @@ def block_mask(spec: Spec, B: int, Sq: int, Skv: int, BM: int = 128, BN: int = 1
 def kept_per_row(spec: Spec, B: int, Sq: int, Skv: int) -> np.ndarray:
     """Number of kept keys of every query row, int64 [B, Sq]."""
     out = np.zeros((B, Sq), dtype=np.int64)
-    j = np.arange(Skv)[None, :]
+    j = np.arange(Skv)[None, :] + spec.kv_offset
     slab = _slab_rows(Skv, 64 << 20)
     for b in range(B):
         for start in range(0, Sq, slab):
-            i = np.arange(start, min(start + slab, Sq))[:, None]
+            i = np.arange(start, min(start + slab, Sq))[:, None] + spec.q_offset
             out[b, start:start + slab] = mask_mod(spec, b, i, j).sum(axis=1)
     return out
+
+
+def combine_partials(parts):
+    """Merges attention results over disjoint key sets into the result over
+    their union. ``parts`` is a sequence of ``(O_k, LSE_k)``, each the output
+    and log-sum-exp of the same queries against one key shard (fp64 or
+    widened to it; LSE_k = -inf where a row kept no key of that shard).
+
+    This is the merge step of the online softmax (Online-Softmax/FlashAttention
+    page, the 2-pass online softmax: two partial maxima and sums combine as
+    m = max(m1, m2), l = l1 e^(m1-m) + l2 e^(m2-m)) applied to whole partial
+    results, as context-parallel attention does with key/value shards
+    (FlexAttention page, variant list: sliding window + document masking +
+    causal + context parallel). Because O_k is normalised by its own sum,
+    O = sum_k e^(LSE_k - LSE) O_k with LSE = ln sum_k e^(LSE_k). A row with no
+    kept key in any shard gets O = 0 and LSE = -inf.
+    """
+    Os = [_as_f64(o) for o, _ in parts]
+    Ls = [_as_f64(l) for _, l in parts]
+    L = np.stack(Ls)                       # [K, ...rows]
+    m = L.max(axis=0)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    w = np.exp(L - m_safe)                 # e^(LSE_k - m); 0 for empty parts
+    tot = w.sum(axis=0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        lse = np.where(tot > 0, m_safe + np.log(np.where(tot > 0, tot, 1.0)), NEG_INF)
+        frac = np.where(tot > 0, w / np.where(tot > 0, tot, 1.0), 0.0)
+    # a part with weight 0 contributes nothing (its O row may be anything)
+    O = sum(np.where(frac[k][..., None] > 0, frac[k][..., None] * Os[k], 0.0) for k in range(len(Os)))
+    return O, lse

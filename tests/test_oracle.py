@@ -17,7 +17,7 @@ import pytest
 import torch
 
 from oracle import (Spec, alibi_slopes, attention_backward, attention_forward, block_mask,
-                    kept_per_row)
+                    combine_partials, kept_per_row)
 from synth import doc_ids_from_lengths, make_workload
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -531,3 +531,80 @@ def test_rel_bias_gradient_matches_finite_differences():
         args_m = [Xm if Y is X else Y for Y in (q, k, v)]
         fd = (loss(*args_p) - loss(*args_m)) / (2 * h)
         assert abs(fd - G[idx]) < 1e-6 * max(1.0, abs(fd))
+
+
+# ---------------------------------------------------------------------------
+# Shards of a longer sequence (absolute positions) and the merge of partial
+# results: together they must reproduce attention over the whole sequence.
+# ---------------------------------------------------------------------------
+
+def _shard_spec(spec: Spec, q_off: int, kv_off: int) -> Spec:
+    import dataclasses
+    return dataclasses.replace(spec, q_offset=q_off, kv_offset=kv_off)
+
+
+SHARD_SPECS = {
+    "doc_window_causal_alibi_softcap": lambda doc, pre: Spec(
+        causal=True, window=23, doc_id=doc, alibi=True, softcap=3.0),
+    "prefix_causal": lambda doc, pre: Spec(causal=True, prefix_len=pre),
+    "full_alibi": lambda doc, pre: Spec(alibi=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHARD_SPECS))
+def test_sharded_attention_merges_to_full_attention(name):
+    """Queries and keys cut into shards at uneven points: each (query shard,
+    key shard) pair computed with its absolute offsets, the key shards merged
+    by the log-sum-exp rule, equals attention over the whole sequence (the
+    merge is exact in real arithmetic: the online-softmax merge of partial
+    maxima and sums). A missing or mis-signed offset moves the mask or the
+    ALiBi bias; a wrong merge weight changes O or LSE."""
+    B, Hq, Hkv, S, D = 2, 4, 2, 90, 8
+    q, k, v = rnd((B, Hq, S, D), 71), rnd((B, Hkv, S, D), 72), rnd((B, Hkv, S, D), 73)
+    doc = np.stack([doc_ids_from_lengths([17, 40, 33], S), doc_ids_from_lengths([60, 30], S)])
+    pre = np.array([12, 47])
+    spec = SHARD_SPECS[name](doc, pre)
+    O_ref, L_ref = attention_forward(q, k, v, spec)
+    q_cuts, kv_cuts = [0, 41, 90], [0, 25, 61, 90]
+    for qa, qb in zip(q_cuts[:-1], q_cuts[1:]):
+        parts = []
+        for ka, kb in zip(kv_cuts[:-1], kv_cuts[1:]):
+            parts.append(attention_forward(q[:, :, qa:qb], k[:, :, ka:kb], v[:, :, ka:kb],
+                                           _shard_spec(spec, qa, ka)))
+        O, L = combine_partials(parts)
+        assert np.allclose(O, O_ref[:, :, qa:qb], atol=1e-12, rtol=0)
+        fin = np.isfinite(L_ref[:, :, qa:qb])
+        assert np.array_equal(np.isfinite(L), fin)
+        assert np.allclose(L[fin], L_ref[:, :, qa:qb][fin], atol=1e-12, rtol=0)
+
+
+def test_merge_special_cases():
+    """Merging: one part is the identity; a part with no kept key (O = 0,
+    LSE = -inf) contributes nothing; only empty parts give O = 0, LSE = -inf;
+    two parts with equal LSE average their outputs, and the merged LSE is
+    ln 2 larger."""
+    rng = np.random.default_rng(5)
+    O1, L1 = rng.standard_normal((3, 4)), rng.standard_normal(3)
+    O0, L0 = np.zeros((3, 4)), np.full(3, -np.inf)
+    O, L = combine_partials([(O1, L1)])
+    assert np.array_equal(O, O1) and np.array_equal(L, L1)
+    O, L = combine_partials([(O0, L0), (O1, L1), (O0, L0)])
+    assert np.allclose(O, O1, atol=1e-15) and np.allclose(L, L1, atol=1e-15)
+    O, L = combine_partials([(O0, L0), (O0, L0)])
+    assert np.array_equal(O, O0) and np.all(L == -np.inf)
+    O2 = rng.standard_normal((3, 4))
+    O, L = combine_partials([(O1, L1), (O2, L1)])
+    assert np.allclose(O, (O1 + O2) / 2, atol=1e-15)
+    assert np.allclose(L, L1 + math.log(2.0), atol=1e-15)
+
+
+def test_block_mask_of_a_shard_is_a_window_of_the_full_block_mask():
+    """With offsets that are multiples of the tile size, the tiles of a
+    (query shard, key shard) pair are the full problem's tiles at the shifted
+    tile indices."""
+    S = 640
+    doc = np.array([doc_ids_from_lengths([200, 300, 140], S)])
+    spec = Spec(causal=True, window=300, doc_id=doc)
+    full = block_mask(spec, 1, S, S)
+    shard = block_mask(_shard_spec(spec, 256, 128), 1, 384, 256)
+    assert np.array_equal(shard.state[0], full.state[0, 2:5, 1:3])
