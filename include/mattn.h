@@ -59,7 +59,9 @@ typedef enum attn_status {
  *                 AND (DOCUMENT: doc_id[b][i] == doc_id[b][j])
  *                 OR  (PREFIX: j < prefix_len[b])
  * with absent AND-terms true and an absent PREFIX false. i and j are absolute
- * positions (query row i, key column j), aligned at 0.
+ * positions: i = q_offset + query row, j = kv_offset + key column (both
+ * offsets 0 unless the call is one shard of a longer sequence, see
+ * attn_params and attn_combine).
  * Score terms apply in this order: s <- scale * q.k; ALIBI: s <- s - slope_h
  * * (i - j); RELBIAS: s <- s + rel_bias[h][i - j + Skv - 1]; SOFTCAP:
  * s <- softcap * tanh(s / softcap). */
@@ -112,6 +114,8 @@ typedef struct attn_block_mask {
   const int* t_full_idx;
   const int* t_part_idx;
   const int* t_order;
+  int q_offset, kv_offset;  /* position offsets it was built for */
+  int doc_len;              /* row length of doc_id it was built for */
 } attn_block_mask;
 
 /* Parameters of a call (host struct). */
@@ -121,7 +125,8 @@ typedef struct attn_params {
   int window;                  /* ATTN_MASK_WINDOW: keys with i - j < window; >= 1 */
   float softcap;               /* ATTN_SCORE_SOFTCAP: cap c > 0 */
   const float* alibi_slopes;   /* ATTN_SCORE_ALIBI: device fp32 [Hq], or NULL for 2^(-8(h+1)/Hq) */
-  const int* doc_id;           /* ATTN_MASK_DOCUMENT: device int32 [B][max(Sq,Skv)] */
+  const int* doc_id;           /* ATTN_MASK_DOCUMENT: device int32 [B][doc_len], indexed
+                                  by absolute position */
   const int* prefix_len;       /* ATTN_MASK_PREFIX: device int32 [B] */
   const attn_block_mask* block_mask; /* from build_block_mask() for the same mask, or NULL:
                                         then every key tile allowed by the causal bound is
@@ -149,6 +154,19 @@ typedef struct attn_params {
   int page_size;
   int pages_per_seq;
   int num_pages;
+  /* Shards of a longer sequence (FlexAttention page, variant list: sliding
+   * window + document masking + causal + context parallel): query row r and
+   * key column c of this call sit at absolute positions q_offset + r and
+   * kv_offset + c, which every mask term, the ALiBi bias and the document ids
+   * use. Results over disjoint key shards merge with attn_combine(). >= 0.
+   * Forward and block mask only (attn_bwd: ATTN_ERR_UNSUPPORTED when either
+   * is nonzero), not combined with ATTN_SCORE_RELBIAS. */
+  int q_offset;
+  int kv_offset;
+  /* Row length of doc_id: 0 selects L = max(q_offset + Sq, kv_offset + Skv);
+   * otherwise >= L (e.g. the whole sequence's length when the call is one
+   * shard of it). */
+  int doc_len;
 } attn_params;
 
 #define ATTN_FAULT_NO_LOADS 1u
@@ -166,6 +184,28 @@ typedef struct attn_params {
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                      int B, int Hq, int Hkv, int Sq, int Skv, int D,
                      unsigned variant, const attn_params* p, struct CUstream_st* stream);
+
+/* Merge of partial results over disjoint key sets, e.g. the key/value shards
+ * of context-parallel attention (FlexAttention page, variant list: ... +
+ * context parallel). It is the merge step of the online softmax
+ * (Online-Softmax/FlashAttention page, 2-pass online softmax: partial maxima
+ * and sums combine as m = max(m1, m2), l = l1 e^(m1-m) + l2 e^(m2-m)) applied
+ * to whole results, each normalised by its own sum:
+ *   LSE = ln sum_k exp(LSE_k),   O = sum_k exp(LSE_k - LSE) O_k
+ * and a row with no kept key in any part (every LSE_k = -inf) gets O = 0 and
+ * LSE = -inf. A part whose LSE_k is -inf is not read.
+ *   o_parts   device [n_parts][rows][D] of `dtype` (ATTN_BF16 or ATTN_F32),
+ *             part k = the forward output of the same queries against key
+ *             set k (rows = B * H * S in [B, H, S, D] order)
+ *   lse_parts device fp32 [n_parts][rows]
+ *   o, lse    device [rows][D] of `dtype` and fp32 [rows]; they must not
+ *             overlap the parts.
+ * D is 64 or 128; n_parts >= 1; 16-byte aligned tensors. Asynchronous on
+ * `stream`. ATTN_ERR_INVALID_ARG / ATTN_ERR_UNSUPPORTED / ATTN_ERR_MISALIGNED
+ * before any launch. */
+attn_status attn_combine(const void* o_parts, const float* lse_parts, int n_parts,
+                         long long rows, int D, int dtype, void* o, float* lse,
+                         struct CUstream_st* stream);
 
 /* Jagged batches (FlexAttention page, variant list: irregular tensors): n
  * sequences packed back to back with no padding, cu_seqlens (device int32

@@ -19,7 +19,7 @@ __all__ = [
     "MASK_CAUSAL", "MASK_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX", "SCORE_ALIBI",
     "SCORE_SOFTCAP", "BF16", "F32", "AttnError", "BlockMask", "attn_fwd", "attn_bwd",
     "build_block_mask", "attn_block_mask_bytes", "attn_bwd_workspace_bytes", "attn_bwd_noalloc",
-    "attn_check_status", "attn_status_str", "lib", "LIB_PATH",
+    "attn_check_status", "attn_status_str", "attn_combine", "lib", "LIB_PATH",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmattn.so")
@@ -43,7 +43,8 @@ class attn_block_mask(ctypes.Structure):
                 ("part_idx", ctypes.c_void_p), ("order", ctypes.c_void_p),
                 ("t_full_cnt", ctypes.c_void_p), ("t_part_cnt", ctypes.c_void_p),
                 ("t_full_idx", ctypes.c_void_p), ("t_part_idx", ctypes.c_void_p),
-                ("t_order", ctypes.c_void_p)]
+                ("t_order", ctypes.c_void_p), ("q_offset", ctypes.c_int),
+                ("kv_offset", ctypes.c_int), ("doc_len", ctypes.c_int)]
 
 
 class attn_params(ctypes.Structure):
@@ -54,7 +55,8 @@ class attn_params(ctypes.Structure):
                 ("timeout_ns", ctypes.c_ulonglong), ("rel_bias", ctypes.c_void_p),
                 ("fault_inject", ctypes.c_uint), ("page_table", ctypes.c_void_p),
                 ("page_size", ctypes.c_int), ("pages_per_seq", ctypes.c_int),
-                ("num_pages", ctypes.c_int)]
+                ("num_pages", ctypes.c_int), ("q_offset", ctypes.c_int),
+                ("kv_offset", ctypes.c_int), ("doc_len", ctypes.c_int)]
 
 
 _lib = None
@@ -87,6 +89,8 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd_noalloc.restype = i
         L.attn_doc_ids_from_seqlens.argtypes = [vp, i, i, vp, vp]
         L.attn_doc_ids_from_seqlens.restype = i
+        L.attn_combine.argtypes = [vp, vp, i, ctypes.c_longlong, i, i, vp, vp, vp]
+        L.attn_combine.restype = i
         L.attn_check_status.argtypes = [vp, vp]
         L.attn_check_status.restype = i
         L.attn_status_str.argtypes = [i]
@@ -171,7 +175,8 @@ class BlockMask:
 
 def _params(dtype: int, scale: float, window: int, softcap: float, alibi_slopes, doc_id,
             prefix_len, block_mask: Optional[BlockMask], status, timeout_ns: int,
-            fault_inject: int = 0, rel_bias=None) -> attn_params:
+            fault_inject: int = 0, rel_bias=None, q_offset: int = 0,
+            kv_offset: int = 0) -> attn_params:
     p = attn_params()
     p.dtype = dtype
     p.scale = scale
@@ -185,6 +190,10 @@ def _params(dtype: int, scale: float, window: int, softcap: float, alibi_slopes,
     p.timeout_ns = timeout_ns
     p.fault_inject = fault_inject
     p.rel_bias = _ptr(rel_bias)
+    p.q_offset = q_offset
+    p.kv_offset = kv_offset
+    # the row length of the document ids, from the tensor ([B, L] or [L])
+    p.doc_len = int(doc_id.shape[-1]) if doc_id is not None and hasattr(doc_id, "shape") else 0
     return p
 
 
@@ -198,14 +207,18 @@ def attn_bwd_workspace_bytes(B: int, Hq: int, Sq: int) -> int:
 
 def build_block_mask(variant: int, B: int, Sq: int, Skv: int, *, window: int = 0, doc_id=None,
                      prefix_len=None, transposed: bool = False, device="cuda",
-                     buf=None, stream=None) -> BlockMask:
+                     buf=None, q_offset: int = 0, kv_offset: int = 0,
+                     stream=None) -> BlockMask:
     """Builds the block mask on the device (``buf``: optional caller buffer,
-    a uint8 CUDA tensor of at least ``attn_block_mask_bytes`` bytes)."""
+    a uint8 CUDA tensor of at least ``attn_block_mask_bytes`` bytes).
+    ``q_offset``/``kv_offset``: absolute positions of query row 0 and key 0
+    (one shard of a longer sequence)."""
     import torch
     nbytes = attn_block_mask_bytes(B, Sq, Skv, transposed)
     if buf is None:
         buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
-    p = _params(BF16, 0.0, window, 0.0, None, doc_id, prefix_len, None, None, 0)
+    p = _params(BF16, 0.0, window, 0.0, None, doc_id, prefix_len, None, None, 0,
+                q_offset=q_offset, kv_offset=kv_offset)
     out = attn_block_mask()
     st = lib().build_block_mask(variant, ctypes.byref(p), B, Sq, Skv, _ptr(buf),
                                 buf.numel() if hasattr(buf, "numel") else nbytes,
@@ -219,12 +232,17 @@ def attn_fwd(q, k, v, o, lse, variant: int = 0, *, B=None, Hq=None, Hkv=None, Sq
              softcap: float = 0.0, alibi_slopes=None, doc_id=None, prefix_len=None,
              block_mask: Optional[BlockMask] = None, status=None, timeout_ns: int = 0,
              fault_inject: int = 0, rel_bias=None, page_table=None, page_size: int = 0,
-             stream=None) -> None:
+             q_offset: int = 0, kv_offset: int = 0, stream=None) -> None:
     """O and LSE of masked attention; writes ``o`` and ``lse`` in place.
 
     Paged K/V cache: ``k``/``v`` are page pools [num_pages, Hkv, page_size, D]
     and ``page_table`` [B, pages_per_seq] int32 maps logical to physical pages;
     pass ``Skv`` (the shapes cannot tell it).
+
+    One shard of a longer sequence: ``q_offset``/``kv_offset`` are the
+    absolute positions of query row 0 and key 0 (mask terms, ALiBi and
+    document ids use absolute positions); merge the results over key shards
+    with ``attn_combine``.
 
     ``q`` [B,Hq,Sq,D], ``k``/``v`` [B,Hkv,Skv,D], ``o`` like ``q``, ``lse`` fp32
     [B,Hq,Sq]. Shapes come from the tensors unless given explicitly (needed
@@ -238,7 +256,7 @@ def attn_fwd(q, k, v, o, lse, variant: int = 0, *, B=None, Hq=None, Hkv=None, Sq
         import torch
         dtype = F32 if q.dtype == torch.float32 else BF16
     p = _params(dtype, scale, window, softcap, alibi_slopes, doc_id, prefix_len, block_mask,
-                status, timeout_ns, fault_inject, rel_bias)
+                status, timeout_ns, fault_inject, rel_bias, q_offset, kv_offset)
     if page_table is not None:
         p.page_table = _ptr(page_table)
         p.page_size = page_size
@@ -247,6 +265,21 @@ def attn_fwd(q, k, v, o, lse, variant: int = 0, *, B=None, Hq=None, Hkv=None, Sq
     st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
                         variant, ctypes.byref(p), _stream(stream))
     _check(st, "attn_fwd")
+
+
+def attn_combine(o_parts, lse_parts, o, lse, stream=None) -> None:
+    """Merges results over disjoint key sets (e.g. key/value shards):
+    ``o_parts`` [n, ...rows..., D] (bf16 or fp32 CUDA tensor), ``lse_parts``
+    fp32 [n, ...rows...]; writes ``o`` [...rows..., D] and ``lse``
+    [...rows...] in place: LSE = ln sum_k exp(LSE_k), O = sum_k
+    exp(LSE_k - LSE) O_k."""
+    import torch
+    n, D = o_parts.shape[0], o_parts.shape[-1]
+    rows = lse_parts[0].numel()
+    dtype = F32 if o_parts.dtype == torch.float32 else BF16
+    st = lib().attn_combine(_ptr(o_parts), _ptr(lse_parts), n, rows, D, dtype, _ptr(o),
+                            _ptr(lse), _stream(stream))
+    _check(st, "attn_combine")
 
 
 def doc_ids_from_seqlens(cu_seqlens, total: Optional[int] = None, doc_id=None,

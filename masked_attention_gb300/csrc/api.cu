@@ -1,6 +1,8 @@
 // The exported C ABI (include/mattn.h): argument checks, block-mask buffer
 // layout, and dispatch to the kernels. Every check returns before anything
 // is launched; nothing here allocates device memory.
+#include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -77,7 +79,7 @@ MaskLayout mask_layout(int B, int Sq, int Skv, int transposed) {
   return L;
 }
 
-attn_status check_mask_params(unsigned variant, const attn_params* p, int B) {
+attn_status check_mask_params(unsigned variant, const attn_params* p, int B, int Sq, int Skv) {
   if (variant & ~kKnownBits) return ATTN_ERR_INVALID_ARG;
   if ((variant & ATTN_MASK_WINDOW) && p->window < 1) return ATTN_ERR_INVALID_ARG;
   if ((variant & ATTN_MASK_DOCUMENT) && !p->doc_id) return ATTN_ERR_INVALID_ARG;
@@ -86,6 +88,13 @@ attn_status check_mask_params(unsigned variant, const attn_params* p, int B) {
   if ((variant & ATTN_SCORE_RELBIAS) &&
       (!p->rel_bias || (reinterpret_cast<uintptr_t>(p->rel_bias) & 3)))
     return ATTN_ERR_INVALID_ARG;
+  if (p->q_offset < 0 || p->kv_offset < 0) return ATTN_ERR_INVALID_ARG;
+  if ((long long)p->q_offset + Sq > INT_MAX || (long long)p->kv_offset + Skv > INT_MAX)
+    return ATTN_ERR_INVALID_ARG;  // absolute positions are int
+  if ((variant & ATTN_SCORE_RELBIAS) && (p->q_offset || p->kv_offset))
+    return ATTN_ERR_UNSUPPORTED;
+  const long long need = std::max((long long)p->q_offset + Sq, (long long)p->kv_offset + Skv);
+  if (p->doc_len != 0 && p->doc_len < need) return ATTN_ERR_INVALID_ARG;
   (void)B;
   return ATTN_OK;
 }
@@ -95,7 +104,10 @@ MaskArgs mask_args(unsigned variant, const attn_params* p, int Sq, int Skv) {
   m.variant = variant & ATTN_MASK_BITS;
   m.window = p->window;
   m.doc_id = p->doc_id;
-  m.doc_len = Sq > Skv ? Sq : Skv;
+  m.q_off = p->q_offset;
+  m.kv_off = p->kv_offset;
+  const long long lq = (long long)p->q_offset + Sq, lk = (long long)p->kv_offset + Skv;
+  m.doc_len = p->doc_len ? p->doc_len : (int)(lq > lk ? lq : lk);
   m.prefix_len = p->prefix_len;
   return m;
 }
@@ -110,6 +122,9 @@ attn_status check_block_mask(const attn_block_mask* bm, unsigned variant, const 
   if ((mbits & ATTN_MASK_WINDOW) && bm->window != p->window) return ATTN_ERR_INVALID_ARG;
   if ((mbits & ATTN_MASK_DOCUMENT) && bm->doc_id != p->doc_id) return ATTN_ERR_INVALID_ARG;
   if ((mbits & ATTN_MASK_PREFIX) && bm->prefix_len != p->prefix_len) return ATTN_ERR_INVALID_ARG;
+  if (bm->q_offset != p->q_offset || bm->kv_offset != p->kv_offset) return ATTN_ERR_INVALID_ARG;
+  if ((mbits & ATTN_MASK_DOCUMENT) && bm->doc_len != mask_args(variant, p, Sq, Skv).doc_len)
+    return ATTN_ERR_INVALID_ARG;
   if (!bm->full_cnt || !bm->part_cnt || !bm->full_idx || !bm->part_idx || !bm->order)
     return ATTN_ERR_INVALID_ARG;
   if (need_transposed && (!bm->t_full_cnt || !bm->t_part_cnt || !bm->t_full_idx ||
@@ -126,7 +141,7 @@ attn_status fill_problem(FwdProblem& f, const void* q, const void* k, const void
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if (p->dtype != ATTN_BF16 && p->dtype != ATTN_F32) return ATTN_ERR_UNSUPPORTED;
-  attn_status st = check_mask_params(variant, p, B);
+  attn_status st = check_mask_params(variant, p, B, Sq, Skv);
   if (st != ATTN_OK) return st;
   if (!std::isfinite(p->scale) || p->scale < 0.0f) return ATTN_ERR_INVALID_ARG;
   f = FwdProblem{};
@@ -199,7 +214,7 @@ MATTN_API attn_status build_block_mask(unsigned variant, const attn_params* p, i
                                        int Skv, void* buf, size_t bytes, int transposed,
                                        attn_block_mask* out, struct CUstream_st* stream) {
   if (!p || !out || B < 1 || Sq < 1 || Skv < 1) return ATTN_ERR_INVALID_ARG;
-  attn_status st = check_mask_params(variant, p, B);
+  attn_status st = check_mask_params(variant, p, B, Sq, Skv);
   if (st != ATTN_OK) return st;
   if (!buf) return ATTN_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(buf) & 255u) return ATTN_ERR_MISALIGNED;
@@ -222,6 +237,9 @@ MATTN_API attn_status build_block_mask(unsigned variant, const attn_params* p, i
   r.window = p->window;
   r.doc_id = (variant & ATTN_MASK_DOCUMENT) ? p->doc_id : nullptr;
   r.prefix_len = (variant & ATTN_MASK_PREFIX) ? p->prefix_len : nullptr;
+  r.q_offset = p->q_offset;
+  r.kv_offset = p->kv_offset;
+  r.doc_len = m.doc_len;
   r.full_cnt = at(L.full_cnt);
   r.part_cnt = at(L.part_cnt);
   r.full_idx = at(L.full_idx);
@@ -297,6 +315,7 @@ MATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, cons
   if (st != ATTN_OK) return st;
   if (p->dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
   if (variant & ATTN_SCORE_RELBIAS) return ATTN_ERR_UNSUPPORTED;  // forward only
+  if (p->q_offset || p->kv_offset) return ATTN_ERR_UNSUPPORTED;   // forward only
   if (p->page_table) return ATTN_ERR_UNSUPPORTED;                 // forward only
   if (Sq % kTile != 0 || Skv % kTile != 0) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || Sq == 0 || Skv == 0) return ATTN_ERR_UNSUPPORTED;

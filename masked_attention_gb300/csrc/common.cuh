@@ -22,9 +22,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 struct MaskArgs {
   unsigned variant;       // mask bits (ATTN_MASK_*)
   int window;
-  const int* doc_id;      // [B][doc_len]
-  int doc_len;            // max(Sq, Skv)
+  const int* doc_id;      // [B][doc_len], indexed by absolute position
+  int doc_len;            // max(q_off + Sq, kv_off + Skv)
   const int* prefix_len;  // [B]
+  int q_off, kv_off;      // absolute position of query row 0 / key 0
 };
 
 struct ScoreArgs {
@@ -50,9 +51,20 @@ __device__ __forceinline__ float alibi_slope(const ScoreArgs& s, int h) {
   return s.slopes ? s.slopes[h] : exp2f(-8.0f * float(h + 1) / float(s.Hq));
 }
 
-// keep(b, i, j) exactly as the mask bits define it (used by the fp32 kernel,
-// the block-mask builder, and as the reference for partial tiles).
+// Number of leading key tiles the causal term allows for query rows up to
+// `last_row` (rows and key columns of the call; absolute positions add the
+// offsets): tiles past the one holding absolute key position q_off+last_row.
+__device__ __forceinline__ int causal_tiles(const MaskArgs& m, int last_row, int nkv) {
+  const int jmax = last_row + m.q_off - m.kv_off;  // last key column with j <= i
+  return jmax < 0 ? 0 : min(nkv, jmax / kTile + 1);
+}
+
+// keep(b, i, j) exactly as the mask bits define it, for query row i and key
+// column j of the call (their absolute positions add the offsets). Used by
+// the fp32 kernel.
 __device__ __forceinline__ bool mask_keep(const MaskArgs& m, int b, int i, int j) {
+  i += m.q_off;
+  j += m.kv_off;
   bool keep = true;
   if (m.variant & ATTN_MASK_CAUSAL) keep = keep && (j <= i);
   if (m.variant & ATTN_MASK_WINDOW) keep = keep && (i - j < m.window);

@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(FwdProblem p) {
   } else {
     int last = nkv;
     if ((p.variant & ATTN_MASK_CAUSAL) && !(p.variant & ATTN_MASK_PREFIX))
-      last = min(nkv, (min(q0 + kRows, p.Sq) - 1) / kTile + 1);
+      last = causal_tiles(p.mask, min(q0 + kRows, p.Sq) - 1, nkv);
     n_full = (p.variant & ATTN_MASK_BITS) ? 0 : last;
     n_part = (p.variant & ATTN_MASK_BITS) ? last : 0;
   }
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(FwdProblem p) {
         for (int d = 0; d < DH; ++d) part = fmaf(q[d], sK[jj][half * DH + d], part);
         float x = (part + __shfl_xor_sync(0xffffffffu, part, 1)) * p.score.scale;
         const int j = j0 + jj;
-        if (p.variant & ATTN_SCORE_ALIBI) x -= slope * float(i - j);
+        if (p.variant & ATTN_SCORE_ALIBI) x -= slope * float(i - j + p.mask.q_off - p.mask.kv_off);
         bool keep = row_ok && j < p.Skv;
         if (rb && keep) x += rb[i - j + p.score.rb_zero];
         if (p.variant & ATTN_SCORE_SOFTCAP) x = p.score.softcap * tanhf(x / p.score.softcap);

@@ -144,7 +144,8 @@ __device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp)
     U.lf = p.lists.full_idx + (size_t)row * p.lists.nkv;
     U.lp = p.lists.part_idx + (size_t)row * p.lists.nkv;
   } else {
-    const int last = causal_bound ? min(nkv, U.qt + 1) : nkv;
+    const int last = causal_bound ? causal_tiles(p.mask, min((U.qt + 1) * kTile, p.Sq) - 1, nkv)
+                                  : nkv;
     const bool masked = (p.variant & ATTN_MASK_BITS) != 0;
     U.n_full = masked ? 0 : last;
     U.n_part = masked ? last : 0;
@@ -777,9 +778,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float slope = (SCORE & 1) ? alibi_slope(p.score, h) : 0.0f;
       const float slope2 = slope * kLog2e;
+      // document ids by key column and query row of this call (the row of
+      // doc_id is indexed by absolute position)
       const int* docb = (p.variant & ATTN_MASK_DOCUMENT)
-                            ? p.mask.doc_id + (size_t)U.b * p.mask.doc_len : nullptr;
-      const int doc_i = (docb && row_in) ? docb[i] : 0;
+                            ? p.mask.doc_id + (size_t)U.b * p.mask.doc_len + p.mask.kv_off
+                            : nullptr;
+      const int doc_i =
+          (docb && row_in) ? p.mask.doc_id[(size_t)U.b * p.mask.doc_len + p.mask.q_off + i] : 0;
+      const int dqk = p.mask.q_off - p.mask.kv_off;  // absolute i - j = (i - j) + dqk
       const int P = (p.variant & ATTN_MASK_PREFIX) ? p.mask.prefix_len[U.b] : INT_MIN;
       float m_ref = -INFINITY, l = 0.0f;
       // Key-tile indices are read two tiles ahead and the document ids of a
@@ -832,11 +838,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) dcur[c] = dnext[c];
         TileCtx tc{sl2, sc, cl2, slope, slope2, p.score.scale, 1.0f / p.score.softcap,
-                   float(j0 - i),
-                   min((p.variant & ATTN_MASK_CAUSAL) ? i - j0 : INT_MAX, p.Skv - 1 - j0),
-                   (p.variant & ATTN_MASK_WINDOW) ? i - j0 - p.mask.window : INT_MIN,
-                   P == INT_MIN ? INT_MIN : min(P, p.Skv) - j0, docb ? wdoc : nullptr, doc_i,
-                   0u, rb_win};
+                   float(j0 - i - dqk),
+                   min((p.variant & ATTN_MASK_CAUSAL) ? i + dqk - j0 : INT_MAX, p.Skv - 1 - j0),
+                   (p.variant & ATTN_MASK_WINDOW) ? i + dqk - j0 - p.mask.window : INT_MIN,
+                   P == INT_MIN ? INT_MIN : min(P - p.mask.kv_off, p.Skv) - j0,
+                   docb ? wdoc : nullptr, doc_i, 0u, rb_win};
         if (partial) tc.modes = chunk_modes(tc);  // before the wait: off the critical path
         ok = __all_sync(0xffffffffu, wait_bounded(s_full + x, s_it & 1, wd));
         if (!ok) break;

@@ -77,31 +77,37 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(MaskArgs m, 
   const int n_outer = transposed ? nkv : nq;
   const int n_inner = transposed ? nq : nkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Tile ranges are in the call's rows and columns; the mask terms and the
+  // document ids use absolute positions (row + q_off, column + kv_off).
   const int* doc = (m.variant & ATTN_MASK_DOCUMENT) ? m.doc_id + (size_t)b * m.doc_len : nullptr;
+  const int* docq = doc ? doc + m.q_off : nullptr;   // by query row
+  const int* dock = doc ? doc + m.kv_off : nullptr;  // by key column
 
   const int outer_len = transposed ? Skv : Sq;
   const Range ro{outer * kTile, min((outer + 1) * kTile, outer_len) - 1};
   int omin = 0, omax = 0;
-  if (doc) warp_doc_minmax(doc, ro, omin, omax);  // every warp computes it
+  if (doc) warp_doc_minmax(transposed ? dock : docq, ro, omin, omax);  // every warp computes it
 
   for (int inner = warp; inner < n_inner; inner += kClassifyThreads / 32) {
     const int inner_len = transposed ? Sq : Skv;
     const Range rn{inner * kTile, min((inner + 1) * kTile, inner_len) - 1};
     const Range ri = transposed ? rn : ro;
     const Range rj = transposed ? ro : rn;
+    const Range ria{ri.lo + m.q_off, ri.hi + m.q_off};    // absolute
+    const Range rja{rj.lo + m.kv_off, rj.hi + m.kv_off};
     // The document term can only remove pairs: a tile the other terms already
     // leave empty is empty, and its document ids need not be read.
     MaskArgs m_nodoc = m;
     m_nodoc.variant &= ~ATTN_MASK_DOCUMENT;
-    int st = bounds_state(m_nodoc, b, ri, rj, 0, 0, 0, 0);
+    int st = bounds_state(m_nodoc, b, ria, rja, 0, 0, 0, 0);
     bool doc_uniform = true;  // one document id over the tile's rows and columns
     if (st != kEmpty && doc) {
       int nmin = 0, nmax = 0;
-      warp_doc_minmax(doc, rn, nmin, nmax);
+      warp_doc_minmax(transposed ? docq : dock, rn, nmin, nmax);
       const int qmin = transposed ? nmin : omin, qmax = transposed ? nmax : omax;
       const int kmin = transposed ? omin : nmin, kmax = transposed ? omax : nmax;
       doc_uniform = qmin == qmax && kmin == kmax && qmin == kmin;
-      st = bounds_state(m, b, ri, rj, qmin, qmax, kmin, kmax);
+      st = bounds_state(m, b, ria, rja, qmin, qmax, kmin, kmax);
     }
     if (st >= 8) {  // undecided: look at the pairs
       // Lane l owns columns l, l+32, l+64, l+96 of the tile; their document
@@ -114,7 +120,7 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(MaskArgs m, 
       for (int k = 0; k < 4; ++k) {
         const int c = lane + 32 * k;
         valid[k] = c < ncols;
-        dj[k] = (doc && valid[k]) ? doc[rj.lo + c] : 0;
+        dj[k] = (doc && valid[k]) ? dock[rj.lo + c] : 0;
       }
       // The rows' document ids too: lane l holds rows l, l+32, l+64, l+96 and
       // each row's id is shuffled out, so the row loop never waits on memory.
@@ -122,7 +128,7 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(MaskArgs m, 
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int i = ri.lo + lane + 32 * k;
-        qd[k] = (doc && i <= ri.hi) ? doc[i] : 0;
+        qd[k] = (doc && i <= ri.hi) ? docq[i] : 0;
       }
       const bool causal = m.variant & ATTN_MASK_CAUSAL, window = m.variant & ATTN_MASK_WINDOW;
       const int P = (m.variant & ATTN_MASK_PREFIX) ? m.prefix_len[b] : INT_MIN;
@@ -130,18 +136,20 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(MaskArgs m, 
       // a tile whose rows and columns do not all share one document certainly
       // drops a pair: only a kept pair has to be found, and the scan stops at
       // the first one instead of looking for a dropped row far down the tile.
-      const bool range_all = (!causal || rj.hi <= ri.lo) && (!window || ri.hi - rj.lo < m.window);
-      const bool prefix_none = rj.lo >= P;
+      const bool range_all =
+          (!causal || rja.hi <= ria.lo) && (!window || ria.hi - rja.lo < m.window);
+      const bool prefix_none = rja.lo >= P;
       bool any_keep = false, any_drop = range_all && prefix_none && !doc_uniform;
       for (int i = ri.lo; i <= ri.hi; ++i) {
         const int r = i - ri.lo, k = r >> 5;
         const int mine = k == 0 ? qd[0] : k == 1 ? qd[1] : k == 2 ? qd[2] : qd[3];
         const int di = __shfl_sync(0xffffffffu, mine, r & 31);
+        const int ia = i + m.q_off;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const int j = rj.lo + lane + 32 * k;
-          const bool keep = ((!causal | (j <= i)) & (!window | (i - j < m.window)) & (dj[k] == di)) |
-                            (j < P);
+          const int j = rja.lo + lane + 32 * k;
+          const bool keep =
+              ((!causal | (j <= ia)) & (!window | (ia - j < m.window)) & (dj[k] == di)) | (j < P);
           any_keep |= valid[k] & keep;
           any_drop |= valid[k] & !keep;
         }

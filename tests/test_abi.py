@@ -121,6 +121,58 @@ def test_argument_errors_return_before_launch(M):
     assert call_fwd(M, scale=float("nan")) == M.ATTN_ERR_INVALID_ARG
 
 
+def test_offset_and_merge_argument_errors(M):
+    """Shards of a longer sequence: negative or overflowing offsets are
+    invalid; offsets with the relative-position table, and in the backward,
+    are not supported. The merge checks its arguments before any launch."""
+    L = M.lib()
+
+    def fwd(variant=0, **kw):
+        p = M._params(0, 0.0, 0, 0.0, None, None, None, None, None, 0, rel_bias=kw.get("rb"),
+                      q_offset=kw.get("qo", 0), kv_offset=kw.get("ko", 0))
+        return L.attn_fwd(*([0x10000] * 5), 1, 2, 2, 128, 128, 64, variant, ctypes.byref(p), None)
+
+    assert fwd(qo=-1) == M.ATTN_ERR_INVALID_ARG
+    assert fwd(ko=-5) == M.ATTN_ERR_INVALID_ARG
+    assert fwd(qo=2**31 - 100) == M.ATTN_ERR_INVALID_ARG
+    assert fwd(M.SCORE_RELBIAS, rb=0x20000, qo=128) == M.ATTN_ERR_UNSUPPORTED
+    # document ids: a row length shorter than the absolute positions used
+    p = M._params(0, 0.0, 0, 0.0, None, 0x50000, None, None, None, 0, q_offset=64)
+    p.doc_len = 150   # needs q_offset + Sq = 192
+    st = L.attn_fwd(*([0x10000] * 5), 1, 2, 2, 128, 128, 64, M.MASK_DOCUMENT, ctypes.byref(p),
+                    None)
+    assert st == M.ATTN_ERR_INVALID_ARG
+    p = M._params(0, 0.0, 0, 0.0, None, None, None, None, None, 0, kv_offset=128)
+    st = L.attn_bwd(*([0x10000] * 10), 1 << 20, 1, 2, 2, 128, 128, 64, M.MASK_CAUSAL,
+                    ctypes.byref(p), None)
+    assert st == M.ATTN_ERR_UNSUPPORTED
+    # a block mask built for other offsets does not describe the call
+    bm = M.attn_block_mask()
+    bm.B, bm.Sq, bm.Skv, bm.nq, bm.nkv, bm.variant = 1, 128, 128, 1, 1, M.MASK_CAUSAL
+    bm.full_cnt = bm.part_cnt = bm.full_idx = bm.part_idx = bm.order = 0x30000
+    bm.q_offset = 128
+    p = M._params(0, 0.0, 0, 0.0, None, None, None, None, None, 0)
+    p.block_mask = ctypes.pointer(bm)
+    st = L.attn_fwd(*([0x10000] * 5), 1, 2, 2, 128, 128, 64, M.MASK_CAUSAL, ctypes.byref(p), None)
+    assert st == M.ATTN_ERR_INVALID_ARG
+
+    def comb(o_parts=0x100000, lse_parts=0x200000, n=2, rows=64, D=128, dtype=0, o=0x300000,
+             lse=0x400000):
+        return L.attn_combine(o_parts, lse_parts, n, rows, D, dtype, o, lse, None)
+
+    assert comb(n=0) == M.ATTN_ERR_INVALID_ARG
+    assert comb(rows=-1) == M.ATTN_ERR_INVALID_ARG
+    assert comb(D=96) == M.ATTN_ERR_UNSUPPORTED
+    assert comb(dtype=7) == M.ATTN_ERR_UNSUPPORTED
+    assert comb(rows=0) == M.ATTN_OK            # nothing to do, nothing launched
+    assert comb(o_parts=0) == M.ATTN_ERR_INVALID_ARG
+    assert comb(o=0x300008) == M.ATTN_ERR_MISALIGNED
+    assert comb(lse=0x400002) == M.ATTN_ERR_MISALIGNED
+    # the output may not overlap the parts
+    assert comb(o=0x100000 + 256) == M.ATTN_ERR_INVALID_ARG
+    assert comb(lse=0x200000 + 64) == M.ATTN_ERR_INVALID_ARG
+
+
 def test_block_mask_buffer_checks(M):
     L = M.lib()
     p = M._params(0, 0.0, 0, 0.0, None, None, None, None, None, 0)
