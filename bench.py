@@ -539,6 +539,45 @@ def run_backward(args) -> None:
                       "tflops": flops / ms / 1e9, "source_digest": source_digest()}), flush=True)
 
 
+def run_combine(args) -> None:
+    """Diagnostic: attn_combine merging the partial results of n key/value
+    shards for the document + window workload's queries (B=1, H=16, S=16384,
+    D=128, bf16), one launch timed with CUDA events, against the measured
+    HBM copy bandwidth. Algorithmic bytes per launch: every part's O row and
+    LSE read once, the merged row and LSE written once."""
+    import torch
+
+    import masked_attention_gb300 as M
+
+    n, B, H, S, D = args.combine, 1, 16, 16384, 128
+    rows = B * H * S
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(11)
+    o_parts = torch.randn(n, rows, D, generator=g, device=dev).to(torch.bfloat16)
+    l_parts = torch.randn(n, rows, generator=g, device=dev) * 4.0
+    o = torch.empty(rows, D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(rows, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        M.attn_combine(o_parts, l_parts, o, lse)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for s_ in range(args.steps):
+        flush.fill_(s_ & 0xFF)
+        ev[s_][0].record()
+        M.attn_combine(o_parts, l_parts, o, lse)
+        ev[s_][1].record()
+    torch.cuda.synchronize()
+    ms = sorted(a.elapsed_time(b) for a, b in ev)[args.steps // 2]
+    nbytes = (n + 1) * rows * (2 * D + 4)
+    peaks, src = read_peaks()
+    gbs = nbytes / ms / 1e6
+    print(json.dumps({"diagnostic": "combine", "parts": n, "rows": rows, "D": D,
+                      "ms_per_launch": ms, "bytes_per_launch": nbytes, "gbs": gbs,
+                      "frac_of_hbm": gbs / peaks["hbm_gbs"], "peak_source": src}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -557,7 +596,12 @@ def main():
                     help="diagnostic: add a relative-position bias table to the workload")
     ap.add_argument("--backward", action="store_true",
                     help="diagnostic: time the backward of the training workload instead")
+    ap.add_argument("--combine", type=int, default=0,
+                    help="diagnostic: time attn_combine over this many key/value shards")
     args = ap.parse_args()
+    if args.combine:
+        run_combine(args)
+        return
     if args.backward:
         run_backward(args)
         return

@@ -138,14 +138,17 @@ def test_block_mask_with_offsets_is_exact(qa, qb, ka, kb):
         assert np.array_equal(got["t_part_cnt"], ref.t_part_cnt)
 
 
-@pytest.mark.parametrize("D,dtype", [(64, "bf16"), (128, "bf16"), (128, "f32"), (64, "f32")])
-def test_combine_matches_oracle_merge(D, dtype):
+@pytest.mark.parametrize("D,dtype,n,rows", [(64, "bf16", 5, 3000), (128, "bf16", 5, 3000),
+                                            (128, "f32", 3, 3001), (64, "f32", 2, 2998),
+                                            (128, "bf16", 32, 1027), (64, "bf16", 40, 517)])
+def test_combine_matches_oracle_merge(D, dtype, n, rows):
     """attn_combine on random parts (with empty parts and rows empty in every
-    part) against the oracle's merge of the same stored values."""
+    part) against the oracle's merge of the same stored values; row counts
+    that are not a multiple of the rows a warp merges at once, and more parts
+    than a warp has lanes."""
     import torch
     import masked_attention_gb300 as M
-    g = torch.Generator().manual_seed(970 + D)
-    n, rows = 5, 3000
+    g = torch.Generator().manual_seed(970 + D + n)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     o_parts = torch.randn(n, rows, D, generator=g).to(tdt)
     l_parts = (torch.randn(n, rows, generator=g) * 4.0).float()
