@@ -274,8 +274,13 @@ def attn_combine(o_parts, lse_parts, o, lse, stream=None) -> None:
     [...rows...] in place: LSE = ln sum_k exp(LSE_k), O = sum_k
     exp(LSE_k - LSE) O_k."""
     import torch
+    for name, x in (("o_parts", o_parts), ("lse_parts", lse_parts), ("o", o), ("lse", lse)):
+        if not x.is_contiguous():
+            raise ValueError(f"attn_combine: {name} must be contiguous")
     n, D = o_parts.shape[0], o_parts.shape[-1]
     rows = lse_parts[0].numel()
+    if o.numel() != rows * D or lse.numel() != rows or o_parts.numel() != n * rows * D:
+        raise ValueError("attn_combine: shapes of the parts and the outputs disagree")
     dtype = F32 if o_parts.dtype == torch.float32 else BF16
     st = lib().attn_combine(_ptr(o_parts), _ptr(lse_parts), n, rows, D, dtype, _ptr(o),
                             _ptr(lse), _stream(stream))
