@@ -190,3 +190,16 @@ def test_block_mask_buffer_checks(M):
                             ctypes.byref(out), None)
     assert st == M.ATTN_ERR_MISALIGNED
     assert M.attn_bwd_workspace_bytes(8, 16, 4096) == 4 * 8 * 16 * 4096
+
+
+def test_combine_binding_refuses_strided_views(M):
+    """The Python binding passes raw addresses, so a strided view would be
+    written as if contiguous: it is refused before the library is called."""
+    import torch
+    parts = torch.zeros(2, 4, 8, 64)
+    lparts = torch.zeros(2, 4, 8)
+    o, lse = torch.zeros(4, 16, 64), torch.zeros(4, 16)
+    with pytest.raises(ValueError):
+        M.attn_combine(parts, lparts, o[:, :8], lse[:, :8])
+    with pytest.raises(ValueError):
+        M.attn_combine(parts, lparts, torch.zeros(4, 9, 64), torch.zeros(4, 9))
