@@ -19,7 +19,7 @@ pass 2 the sum of exp(s' - max), pass 3 normalises and multiplies by V. The
 full score matrix of every (b, h) is materialised (in row slabs only to bound
 memory; every row is always computed over all keys).
 
-Readings taken where the pages are silent (each is restated in the design doc):
+Readings taken where the pages are silent:
 
 * scale defaults to 1/sqrt(D) and multiplies QK^T before score_mod;
 * ALiBi adds ``-slope_h * (i - j)`` with ``slope_h = 2**(-8 (h+1) / Hq)``
@@ -31,6 +31,10 @@ Readings taken where the pages are silent (each is restated in the design doc):
   causal ``j <= i``, window ``i - j < W``, document ``doc[b,i] == doc[b,j]``,
   prefix ``j < P_b``; indices are absolute positions (top-left aligned);
 * a row with no kept key has O = 0 and LSE = -inf;
+* a call may be one shard of a longer sequence: query row r and key column c
+  stand for absolute positions q_offset + r and kv_offset + c, and results
+  over disjoint key shards merge by the online-softmax merge
+  (``combine_partials``);
 * GQA groups consecutive query heads: query head h reads KV head h // (Hq/Hkv).
 """
 from __future__ import annotations

@@ -44,7 +44,7 @@ def variant_bits(w) -> int:
     return v
 
 
-class GpuRun:
+class DeviceRun:
     """Uploads a workload and runs the library's forward on it."""
 
     def __init__(self, w, use_block_mask=True, transposed=False):

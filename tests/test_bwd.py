@@ -13,7 +13,7 @@ import pytest
 
 from oracle import attention_backward
 from synth import make_workload
-from tests.helpers import GpuRun, oracle_spec
+from tests.helpers import DeviceRun, oracle_spec
 
 pytestmark = pytest.mark.gpu
 
@@ -27,7 +27,7 @@ def grad_tol(ref):
 def run_bwd(w, use_block_mask=True):
     import torch
     import masked_attention_gb300 as M
-    g = GpuRun(w, use_block_mask=use_block_mask, transposed=True)
+    g = DeviceRun(w, use_block_mask=use_block_mask, transposed=True)
     O, L = g.fwd()
     dq = torch.empty_like(g.q)
     dk = torch.empty_like(g.k)

@@ -13,7 +13,7 @@ import pytest
 
 from oracle import attention_forward
 from synth import make_workload
-from tests.helpers import GpuRun, oracle_spec
+from tests.helpers import DeviceRun, oracle_spec
 
 pytestmark = pytest.mark.gpu
 
@@ -27,7 +27,7 @@ def test_forward_timeout_reports_status_and_recovers():
     import torch
     import masked_attention_gb300 as M
     w = workload()
-    g = GpuRun(w)
+    g = DeviceRun(w)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     o = torch.empty_like(g.q)
     lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device="cuda")
@@ -48,7 +48,7 @@ def test_backward_timeout_reports_status_and_recovers():
     import torch
     import masked_attention_gb300 as M
     w = workload()
-    g = GpuRun(w, transposed=True)
+    g = DeviceRun(w, transposed=True)
     O, L = g.fwd()
     dq, dk, dv = torch.empty_like(g.q), torch.empty_like(g.k), torch.empty_like(g.v)
     ws = torch.empty(M.attn_bwd_workspace_bytes(w.B, w.Hq, w.Sq), dtype=torch.uint8,
@@ -65,7 +65,7 @@ def test_mismatched_block_mask_is_rejected():
     import torch
     import masked_attention_gb300 as M
     w = workload()
-    g = GpuRun(w)  # block mask built for the causal mask
+    g = DeviceRun(w)  # block mask built for the causal mask
     o = torch.empty_like(g.q)
     lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device="cuda")
     with pytest.raises(M.AttnError) as e:
@@ -85,7 +85,7 @@ def test_small_workspace_is_rejected():
     import torch
     import masked_attention_gb300 as M
     w = workload()
-    g = GpuRun(w, transposed=True)
+    g = DeviceRun(w, transposed=True)
     O, L = g.fwd()
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(M.AttnError) as e:

@@ -17,7 +17,7 @@ import pytest
 
 from oracle import attention_forward
 from synth import make_workload
-from tests.helpers import GpuRun, oracle_spec
+from tests.helpers import DeviceRun, oracle_spec
 
 pytestmark = pytest.mark.gpu
 
@@ -62,7 +62,7 @@ def check(w, O, L, O_ref, L_ref, rows=None):
 
 def run_and_check(w, use_block_mask=True, rows=None, heads=None):
     import torch
-    g = GpuRun(w, use_block_mask=use_block_mask)
+    g = DeviceRun(w, use_block_mask=use_block_mask)
     O, L = g.fwd()
     torch.cuda.synchronize()
     O_ref, L_ref = attention_forward(w.q, w.k, w.v, oracle_spec(w), rows=rows, heads=heads)
@@ -202,7 +202,7 @@ def test_full_size_workloads_sampled(number):
     rows = sample_rows(w.Sq)
     heads = [(0, 0), (w.B - 1, w.Hq - 1), (w.B // 2, w.Hq // 2 + 1)]
     import torch
-    g = GpuRun(w)
+    g = DeviceRun(w)
     O, L = g.fwd()
     torch.cuda.synchronize()
     O_ref, L_ref = attention_forward(w.q, w.k, w.v, oracle_spec(w), rows=rows, heads=heads)
@@ -231,7 +231,7 @@ def test_zero_query_gives_mean_of_kept_values():
 def test_deterministic():
     import torch
     w = make_workload(0, seed=9, **BF16_CASES["gqa_prefix_softcap_d128"])
-    g = GpuRun(w)
+    g = DeviceRun(w)
     O1, L1 = g.fwd()
     O2, L2 = g.fwd()
     torch.cuda.synchronize()

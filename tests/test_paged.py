@@ -9,7 +9,7 @@ import torch
 
 from oracle import attention_forward
 from synth import make_workload
-from tests.helpers import GpuRun, oracle_spec
+from tests.helpers import DeviceRun, oracle_spec
 
 pytestmark = pytest.mark.gpu
 
@@ -52,7 +52,7 @@ def test_paged_forward_matches_contiguous_and_oracle(name):
     import masked_attention_gb300 as M
     spec, page_size = CASES[name]
     w = make_workload(0, seed=700 + sorted(CASES).index(name), **spec)
-    g = GpuRun(w)
+    g = DeviceRun(w)
     O_ref_gpu, L_ref_gpu = g.fwd()
     kp, vp, table = paged_pools(w.k, w.v, page_size, seed=710 + sorted(CASES).index(name))
     kp, vp, table = kp.cuda(), vp.cuda(), table.cuda()
@@ -72,7 +72,7 @@ def test_paged_forward_matches_contiguous_and_oracle(name):
 def test_paged_arguments_are_checked():
     import masked_attention_gb300 as M
     w = make_workload(0, seed=720, B=1, Hq=2, Hkv=2, Sq=128, Skv=300, D=64)
-    g = GpuRun(w, use_block_mask=False)
+    g = DeviceRun(w, use_block_mask=False)
     kp, vp, table = (t.cuda() for t in paged_pools(w.k, w.v, 32, seed=721))
     o = torch.empty_like(g.q)
     lse = torch.empty(1, 2, 128, dtype=torch.float32, device="cuda")

@@ -9,7 +9,7 @@ import torch
 
 from oracle import Spec, attention_backward, attention_forward
 from synth import make_workload
-from tests.helpers import GpuRun
+from tests.helpers import DeviceRun
 
 LENGTHS = [100, 300, 57, 1, 400, 166]   # total 1024: several tiles, ragged seams
 
@@ -55,7 +55,7 @@ def test_packed_forward_equals_per_sequence(D):
     w = packed_workload(D)
     cu = torch.tensor(np.concatenate([[0], np.cumsum(LENGTHS)]), dtype=torch.int32,
                       device="cuda")
-    g = GpuRun(w, use_block_mask=False)
+    g = DeviceRun(w, use_block_mask=False)
     g.doc_id = M.doc_ids_from_seqlens(cu)
     g.bm = M.build_block_mask(g.variant & 0xF, 1, w.Sq, w.Skv, doc_id=g.doc_id)
     O, L = g.fwd()
@@ -76,7 +76,7 @@ def test_packed_backward_equals_per_sequence():
     w = packed_workload(128, backward=True, seed=610, lengths=lengths)
     cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32,
                       device="cuda")
-    g = GpuRun(w, use_block_mask=False)
+    g = DeviceRun(w, use_block_mask=False)
     g.doc_id = M.doc_ids_from_seqlens(cu)
     g.bm = M.build_block_mask(g.variant & 0xF, 1, w.Sq, w.Skv, doc_id=g.doc_id,
                               transposed=True)

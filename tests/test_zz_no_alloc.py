@@ -18,7 +18,7 @@ import numpy as np
 import pytest
 
 from synth import make_workload
-from tests.helpers import GpuRun
+from tests.helpers import DeviceRun
 
 pytestmark = pytest.mark.gpu
 
@@ -39,7 +39,7 @@ def test_noalloc_backward_matches_workspace_backward_twice():
     ]
     for n, case in enumerate(cases):  # two calls in a row, different shapes and variants
         w = make_workload(0, seed=900 + n, backward=True, **case)
-        g = GpuRun(w, transposed=True)
+        g = DeviceRun(w, transposed=True)
         O, L = g.fwd()
         ref = [torch.empty_like(t) for t in (g.q, g.k, g.v)]
         ws = torch.empty(M.attn_bwd_workspace_bytes(w.B, w.Hq, w.Sq), dtype=torch.uint8,
