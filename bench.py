@@ -57,6 +57,34 @@ def kept_pairs(w) -> int:
     return total
 
 
+def visited_pairs(w, tile: int = 128) -> int:
+    """(q, kv) pairs inside the 128 x 128 tiles that hold at least one kept
+    pair (the tiles the forward visits; their in-bounds area), one head,
+    summed over the batch: the executed work beside the algorithmic one."""
+    import numpy as np
+    total = 0
+    j = np.arange(w.Skv)[None, :]
+    nkv = (w.Skv + tile - 1) // tile
+    for b in range(w.B):
+        for s in range(0, w.Sq, tile):
+            i = np.arange(s, min(s + tile, w.Sq))[:, None]
+            keep = np.ones((i.shape[0], w.Skv), bool)
+            if w.causal:
+                keep &= j <= i
+            if w.window is not None:
+                keep &= (i - j) < w.window
+            if w.document:
+                keep &= w.doc_id[b][i] == w.doc_id[b][j]
+            if w.prefix:
+                keep |= j < int(w.prefix_len[b])
+            pad = np.zeros((keep.shape[0], nkv * tile), bool)
+            pad[:, :w.Skv] = keep
+            hit = pad.reshape(keep.shape[0], nkv, tile).any(axis=(0, 2))
+            widths = np.minimum(tile, w.Skv - np.arange(nkv) * tile)
+            total += int((widths * hit).sum()) * keep.shape[0]
+    return total
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -488,6 +516,9 @@ def run_ours(args, rank: int, world: int) -> None:
         "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
         "flops_per_step": flops,
+        # context: 4 D per pair of every visited tile, and of the dense S x S square
+        "flops_executed_per_step": 4.0 * w.D * visited_pairs(w) * w.Hq,
+        "flops_dense_per_step": 4.0 * w.D * w.B * w.Sq * w.Skv * w.Hq,
         "fwd_ms_per_launch": fwd_s / args.steps * 1e3,
         "mask_ms_per_step": (total_s - fwd_s) / args.steps * 1e3,
         "source_digest": digest,

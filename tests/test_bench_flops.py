@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 import bench
-from oracle import kept_per_row
+from oracle import block_mask, kept_per_row
 from synth import make_workload
 from tests.helpers import oracle_spec
 
@@ -43,3 +43,27 @@ def test_window_workload_density():
     kept = bench.kept_pairs(w)
     assert 0 < kept <= w.B * w.Sq * 1024
     assert kept / (w.B * w.Sq * w.Skv) < 1024 / w.Skv
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_visited_pairs_match_oracle_tiles(case):
+    """Executed work: the in-bounds area of every tile the oracle's brute-force
+    classification calls full or partial."""
+    w = make_workload(0, seed=30 + case, with_tensors=False, **SMALL[case])
+    bm = block_mask(oracle_spec(w), w.B, w.Sq, w.Skv)
+    area = 0
+    for b, qt, kt in zip(*np.nonzero(bm.state)):
+        rows = min(128, w.Sq - 128 * qt)
+        cols = min(128, w.Skv - 128 * kt)
+        area += rows * cols
+    assert bench.visited_pairs(w) == area
+    assert bench.kept_pairs(w) <= area
+
+
+def test_bench_workload_executed_over_algorithmic():
+    """Causal S = 2048: 136 of 256 tiles per head are visited (16 of them on
+    the diagonal, a little over half kept there): 1.062 times the kept pairs."""
+    w = make_workload(2, with_tensors=False)
+    ratio = bench.visited_pairs(w) / bench.kept_pairs(w)
+    assert bench.visited_pairs(w) == w.B * 136 * 128 * 128
+    assert abs(ratio - (136 * 128 * 128) / (2048 * 2049 / 2)) < 1e-12
