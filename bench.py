@@ -455,7 +455,8 @@ def run_ours(args, rank: int, world: int) -> None:
     if M.attn_check_status() != M.ATTN_OK:
         raise RuntimeError("device status error during the timed steps")
     total_s = sum(a.elapsed_time(c) for a, _, c in ev) / 1e3
-    fwd_s = sum(b.elapsed_time(c) for _, b, c in ev) / 1e3
+    fwd_each = sorted(b.elapsed_time(c) for _, b, c in ev)  # ms per forward launch
+    fwd_s = sum(fwd_each) / 1e3
     total_s, fwd_s = max_over_ranks(total_s, fwd_s)
 
     e2e = None
@@ -520,6 +521,8 @@ def run_ours(args, rank: int, world: int) -> None:
         "flops_executed_per_step": 4.0 * w.D * visited_pairs(w) * w.Hq,
         "flops_dense_per_step": 4.0 * w.D * w.B * w.Sq * w.Skv * w.Hq,
         "fwd_ms_per_launch": fwd_s / args.steps * 1e3,
+        "fwd_ms_median": fwd_each[len(fwd_each) // 2],
+        "fwd_ms_min": fwd_each[0],
         "mask_ms_per_step": (total_s - fwd_s) / args.steps * 1e3,
         "source_digest": digest,
     }
