@@ -259,9 +259,12 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
  * the Delta row terms live in a fixed array inside the library (8 MiB per
  * GPU that loads it, held until the process exits), so B*Hq*Sq may be at most
  * 2,097,152; larger problems return ATTN_ERR_WORKSPACE_TOO_SMALL before
- * anything runs. No cudaMalloc, cudaFree or other allocating call is made.
- * The first call on a device looks up the array's device address (make it
- * before any stream capture). Every call shares the array, which keeps the
+ * anything runs (every other argument is checked first, with no CUDA call).
+ * No cudaMalloc, cudaFree or other allocating call is made. The first call
+ * on a device looks up the array's device address and keeps it (make that
+ * call before any stream capture); the address belongs to the device's
+ * primary context, so after cudaDeviceReset the entry point must not be
+ * called again in the same process. Every call shares the array, which keeps the
  * last call's contents (none needs to start at zero); calls that overlap on
  * the GPU race on it. */
 attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
@@ -275,6 +278,12 @@ attn_status attn_check_status(int* status_dev, struct CUstream_st* stream);
 
 /* Static string naming a status code. */
 const char* attn_status_str(attn_status s);
+
+/* Name of the CUDA runtime error behind the calling thread's most recent
+ * ATTN_ERR_CUDA (e.g. "cudaErrorLaunchOutOfResources"), or "cudaSuccess"
+ * if none occurred on this thread. Static string; makes no CUDA call that
+ * can fail. */
+const char* attn_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

@@ -19,7 +19,8 @@ __all__ = [
     "MASK_CAUSAL", "MASK_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX", "SCORE_ALIBI",
     "SCORE_SOFTCAP", "BF16", "F32", "AttnError", "BlockMask", "attn_fwd", "attn_bwd",
     "build_block_mask", "attn_block_mask_bytes", "attn_bwd_workspace_bytes", "attn_bwd_noalloc",
-    "attn_check_status", "attn_status_str", "attn_combine", "lib", "LIB_PATH",
+    "attn_check_status", "attn_status_str", "attn_last_cuda_error", "attn_combine", "lib",
+    "LIB_PATH",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmattn.so")
@@ -95,6 +96,8 @@ def lib() -> ctypes.CDLL:
         L.attn_check_status.restype = i
         L.attn_status_str.argtypes = [i]
         L.attn_status_str.restype = ctypes.c_char_p
+        L.attn_last_cuda_error.argtypes = []
+        L.attn_last_cuda_error.restype = ctypes.c_char_p
         _lib = L
     return _lib
 
@@ -102,7 +105,15 @@ def lib() -> ctypes.CDLL:
 class AttnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {attn_status_str(status)} (status {status})")
+        msg = f"{where}: {attn_status_str(status)} (status {status})"
+        if status == ATTN_ERR_CUDA:
+            msg += f": {attn_last_cuda_error()}"
+        super().__init__(msg)
+
+
+def attn_last_cuda_error() -> str:
+    """Name of the CUDA error behind this thread's most recent ATTN_ERR_CUDA."""
+    return lib().attn_last_cuda_error().decode()
 
 
 def attn_status_str(status: int) -> str:

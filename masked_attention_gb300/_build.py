@@ -46,6 +46,43 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
+def _includes(path: str) -> list:
+    """Local headers a source file includes (quoted #include), resolved in
+    csrc/ or include/."""
+    out = []
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if line.startswith("#include \""):
+                name = line.split('"')[1]
+                for d in (CSRC, INCLUDE):
+                    cand = os.path.join(d, name)
+                    if os.path.exists(cand):
+                        out.append(cand)
+                        break
+    return out
+
+
+def _sources_of(src: str) -> set:
+    """The translation unit and every local header it reaches."""
+    seen, todo = set(), [os.path.join(CSRC, src)]
+    while todo:
+        f = todo.pop()
+        if f in seen:
+            continue
+        seen.add(f)
+        todo.extend(_includes(f))
+    return seen
+
+
+def _object_stale(src: str, obj: str) -> bool:
+    if not os.path.exists(obj):
+        return True
+    t = os.path.getmtime(obj)
+    deps = _sources_of(src) | {os.path.abspath(__file__)}
+    return any(os.path.getmtime(f) > t for f in deps)
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compile every CUDA translation unit and link libmattn.so; returns its path."""
     if not force and up_to_date():
@@ -55,6 +92,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     def compile_one(src: str) -> str:
         obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        if not force and not ptxas_info and not _object_stale(src, obj):
+            return obj
         cmd = [exe, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
         if ptxas_info:
             cmd += ["-Xptxas", "-v"]

@@ -12,6 +12,15 @@
 #define MATTN_API extern "C" __attribute__((visibility("default")))
 
 namespace mattn {
+
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+attn_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return ATTN_OK;
+  t_last_cuda_error = e;
+  return ATTN_ERR_CUDA;
+}
+
 namespace {
 
 __device__ int g_status;  // status word used when the caller passes none
@@ -21,11 +30,11 @@ int* default_status() {
   static int* addr[64] = {nullptr};
   static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (cuda_status(cudaGetDevice(&dev)) != ATTN_OK || dev < 0 || dev >= 64) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
   if (!addr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    if (cuda_status(cudaGetSymbolAddress(&p, g_status)) != ATTN_OK) return nullptr;
     addr[dev] = static_cast<int*>(p);
   }
   return addr[dev];
@@ -224,9 +233,9 @@ MATTN_API attn_status build_block_mask(unsigned variant, const attn_params* p, i
   char* base = static_cast<char*>(buf);
   auto at = [&](size_t off) { return reinterpret_cast<int*>(base + off); };
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (launch_block_mask(m, B, Sq, Skv, 0, at(L.full_cnt), at(L.part_cnt), at(L.full_idx),
-                        at(L.part_idx), at(L.order), s) != cudaSuccess)
-    return ATTN_ERR_CUDA;
+  st = cuda_status(launch_block_mask(m, B, Sq, Skv, 0, at(L.full_cnt), at(L.part_cnt),
+                                     at(L.full_idx), at(L.part_idx), at(L.order), s));
+  if (st != ATTN_OK) return st;
   attn_block_mask r{};
   r.B = B;
   r.Sq = Sq;
@@ -246,9 +255,9 @@ MATTN_API attn_status build_block_mask(unsigned variant, const attn_params* p, i
   r.part_idx = at(L.part_idx);
   r.order = at(L.order);
   if (transposed) {
-    if (launch_block_mask(m, B, Sq, Skv, 1, at(L.t_full_cnt), at(L.t_part_cnt),
-                          at(L.t_full_idx), at(L.t_part_idx), at(L.t_order), s) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+    st = cuda_status(launch_block_mask(m, B, Sq, Skv, 1, at(L.t_full_cnt), at(L.t_part_cnt),
+                                       at(L.t_full_idx), at(L.t_part_idx), at(L.t_order), s));
+    if (st != ATTN_OK) return st;
     r.t_full_cnt = at(L.t_full_cnt);
     r.t_part_cnt = at(L.t_part_cnt);
     r.t_full_idx = at(L.t_full_idx);
@@ -288,7 +297,7 @@ MATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void
   const int elem = p->dtype == ATTN_F32 ? 4 : 2;
   if (Skv == 0) {  // every row is empty: O = 0, LSE = -inf
     fill_empty_rows<<<256, 256, 0, s>>>(o, lse, (size_t)B * Hq * Sq, D, elem);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    return cuda_status(cudaGetLastError());
   }
   cudaError_t e;
   if (p->dtype == ATTN_F32) {
@@ -296,7 +305,7 @@ MATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void
   } else {
     e = launch_fwd_tc(f, s);
   }
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return cuda_status(e);
 }
 
 MATTN_API size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq) {
@@ -304,12 +313,14 @@ MATTN_API size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq) {
   return sizeof(float) * (size_t)B * Hq * Sq;
 }
 
-MATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
-                               const float* lse, const void* dO, void* dq, void* dk, void* dv,
-                               void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
-                               int Sq, int Skv, int D, unsigned variant, const attn_params* p,
-                               struct CUstream_st* stream) {
-  BwdProblem bp;
+namespace mattn {
+
+// Every check of attn_bwd's arguments except those on the workspace; makes no
+// CUDA call. Fills bp.f on success.
+attn_status bwd_check_args(BwdProblem& bp, const void* q, const void* k, const void* v,
+                           const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                           void* dv, int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                           unsigned variant, const attn_params* p) {
   attn_status st = fill_problem(bp.f, q, k, v, const_cast<void*>(o), const_cast<float*>(lse), B,
                                 Hq, Hkv, Sq, Skv, D, variant, p);
   if (st != ATTN_OK) return st;
@@ -319,15 +330,28 @@ MATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, cons
   if (p->page_table) return ATTN_ERR_UNSUPPORTED;                 // forward only
   if (Sq % kTile != 0 || Skv % kTile != 0) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || Sq == 0 || Skv == 0) return ATTN_ERR_UNSUPPORTED;
-  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
-    return ATTN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
-      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
-      !aligned16(lse) || ((variant & ATTN_MASK_DOCUMENT) && !aligned16(p->doc_id)))
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(lse) ||
+      ((variant & ATTN_MASK_DOCUMENT) && !aligned16(p->doc_id)))
     return ATTN_ERR_MISALIGNED;
-  if (workspace_bytes < attn_bwd_workspace_bytes(B, Hq, Sq)) return ATTN_ERR_WORKSPACE_TOO_SMALL;
-  st = check_block_mask(p->block_mask, variant, p, B, Sq, Skv, true);
+  return check_block_mask(p->block_mask, variant, p, B, Sq, Skv, true);
+}
+
+}  // namespace mattn
+
+MATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dO, void* dq, void* dk, void* dv,
+                               void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                               int Sq, int Skv, int D, unsigned variant, const attn_params* p,
+                               struct CUstream_st* stream) {
+  BwdProblem bp;
+  attn_status st = bwd_check_args(bp, q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv, Sq, Skv, D,
+                                  variant, p);
   if (st != ATTN_OK) return st;
+  if (!workspace) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+  if (workspace_bytes < attn_bwd_workspace_bytes(B, Hq, Sq)) return ATTN_ERR_WORKSPACE_TOO_SMALL;
   st = resolve_status(bp.f);
   if (st != ATTN_OK) return st;
   bp.dO = dO;
@@ -344,17 +368,25 @@ MATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, cons
   }
   const cudaError_t e = launch_bwd_tc(bp, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return cuda_status(e);
 }
 
 MATTN_API attn_status attn_check_status(int* status_dev, struct CUstream_st* stream) {
   int* addr = status_dev ? status_dev : default_status();
   if (!addr) return ATTN_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
+  attn_status st = cuda_status(cudaStreamSynchronize(s));
+  if (st != ATTN_OK) return st;
   int h = 0;
-  if (cudaMemcpy(&h, addr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  if (h != 0 && cudaMemset(addr, 0, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  st = cuda_status(cudaMemcpy(&h, addr, sizeof(int), cudaMemcpyDeviceToHost));
+  if (st != ATTN_OK) return st;
+  if (h != 0) {
+    st = cuda_status(cudaMemset(addr, 0, sizeof(int)));
+    if (st != ATTN_OK) return st;
+  }
   return static_cast<attn_status>(h);
+}
+
+MATTN_API const char* attn_last_cuda_error(void) {
+  return cudaGetErrorName(t_last_cuda_error);
 }

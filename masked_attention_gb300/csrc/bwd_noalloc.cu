@@ -12,7 +12,9 @@
 //
 // Set-up: the first call on a device looks up the device address of the array
 // (cudaGetSymbolAddress, with that device current) and caches it; make that
-// first call before any stream capture. All calls share the one array and it
+// first call before any stream capture. The cached address belongs to the
+// device's primary context: after cudaDeviceReset the entry point must not be
+// called again in that process. All calls share the one array and it
 // keeps the last call's contents; nothing in it has to start at zero (every
 // call writes each Delta entry before reading it). Calls that overlap on the
 // GPU (for example on two streams at once) race on the array.
@@ -34,11 +36,11 @@ float* workspace_address() {
   static float* addr[64] = {nullptr};
   static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (cuda_status(cudaGetDevice(&dev)) != ATTN_OK || dev < 0 || dev >= 64) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
   if (!addr[dev]) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_bwd_workspace) != cudaSuccess) return nullptr;
+    if (cuda_status(cudaGetSymbolAddress(&ptr, g_bwd_workspace)) != ATTN_OK) return nullptr;
     addr[dev] = static_cast<float*>(ptr);
   }
   return addr[dev];
@@ -52,7 +54,11 @@ MATTN_API attn_status attn_bwd_noalloc(const void* q, const void* k, const void*
                                        void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
                                        int Sq, int Skv, int D, unsigned variant,
                                        const attn_params* p, struct CUstream_st* stream) {
-  if (B < 0 || Hq < 0 || Sq < 0) return ATTN_ERR_INVALID_ARG;
+  // every argument check first: an invalid call fails without any CUDA call
+  mattn::BwdProblem bp;
+  const attn_status st = mattn::bwd_check_args(bp, q, k, v, o, lse, dO, dq, dk, dv, B, Hq, Hkv,
+                                               Sq, Skv, D, variant, p);
+  if (st != ATTN_OK) return st;
   if ((size_t)B * (size_t)Hq * (size_t)Sq > mattn::kMaxRows) return ATTN_ERR_WORKSPACE_TOO_SMALL;
   float* ws = mattn::workspace_address();
   if (!ws) return ATTN_ERR_CUDA;

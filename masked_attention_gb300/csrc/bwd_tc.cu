@@ -11,7 +11,7 @@
 //                  the exact Delta_i = sum_j P dP (it equals <dO_i, O_i> for
 //                  the exact O; the bf16 O is off by up to an ulp, which on
 //                  rows with few keys moves dQ by ~1e-2), accumulated on the fly:
-//                  A += bf16(P g (dP - Dhat)) K, B += bf16(P g) K,
+//                  A += (P g (dP - Dhat)) K, B += bf16(P g) K,
 //                  dQ = scale (A - (Delta - Dhat) B), g = score_mod'.
 //                  A carries the well-conditioned bulk (like dS itself), the
 //                  correction term is small. Delta goes to the workspace.
@@ -20,15 +20,37 @@
 //                  S^T = K Q^T, P^T, dV += P^T dO, dP^T = V dO^T,
 //                  dS^T = P^T (dP^T - Delta) score_mod', dK += dS^T Q (x scale)
 //
-// Both kernels share one structure (192 threads):
-//   warps 0-3  compute: thread t owns row t of the fixed tile (TMEM lane t)
-//   warp  4    TMA producer: the fixed tiles once per unit, then the streamed
+// Precision. The products P^T dO, dS^T Q and (P g (dP - Dhat)) K take their
+// first operand from TMEM in bf16. Rounding it once costs up to 2^-9 of each
+// term, which on rows and keys with few dominant terms moves a gradient of
+// magnitude 2..4 by several 1e-3: together with the final rounding of the
+// output to bf16 (up to 0.0078 there) that exceeds 1e-2. Each of these
+// operands is therefore split into a bf16 part and the bf16 rounding of its
+// remainder, x = hi + lo, and both parts are multiplied (two products into
+// the same accumulator): the error of hi + lo is about 2^-17 of x. The soft-
+// cap's tanh is evaluated to fp32 accuracy for the same reason (an odd
+// polynomial for small arguments, tanhf otherwise).
+//
+// Both kernels share one structure (384 threads):
+//   warps 0-7  compute, two warpgroups: thread t of warpgroup g owns row
+//              t % 128 of the fixed tile (TMEM lane) and columns
+//              [64 g, 64 g + 64) of each streamed tile
+//   warp  8    TMA producer: the fixed tiles once per unit, then the streamed
 //              tiles (plus LSE, Delta and document ids of the dKV stream) into
 //              a ring
-//   warp  5    MMA issuer and TMEM owner
+//   warp  9    MMA issuer and TMEM owner
+//   warps 10-11 idle (the rest of the third warpgroup)
 // Tensor memory: S [0,128), dP [128,256), accumulators from 256 (dQ: A, B;
-// dKV: dV, dK). The bf16 A operands of the TS products (dQ: P g and P g dP;
-// dKV: P and dS) overwrite the first 64 columns of S and dP.
+// dKV: dV, dK). The bf16 operands of the TS products are written over the
+// S and dP columns their warpgroup has read: warpgroup g's 64 columns hold
+// its 32 columns of hi parts, then its 32 columns of lo parts (dQ: P g over
+// S, the lo part of A beside it, the hi part of A over dP).
+//
+// Product order per streamed tile j (the tensor pipe runs them in order):
+//   dKV: dV += P_j^T dO (hi, lo) | S_{j+1} | dK += dS_j^T Q (hi, lo) | dP_{j+1}
+//   dQ:  B += (P g)_j K, A += lo_j K | S_{j+1} | A += hi_j K | dP_{j+1}
+// so the next tile's S is computed while the compute warps still work on the
+// current tile's dS.
 #include <cmath>
 #include <mutex>
 
@@ -38,9 +60,16 @@
 namespace mattn {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kWarpProducer = 4;
-constexpr int kWarpMma = 5;
+constexpr int kThreads = 384;
+constexpr int kComputeWarps = 8;
+// Registers: the CTA is launched with 168 per thread (384 x 168 = 64512 of the
+// SM's 65536); the third warpgroup (producer, MMA, two idle warps) gives up
+// most of its share to the compute warps, which hold 64 scores, their P g and
+// the packed operands of a tile half: 256 x 208 + 128 x 88 = 64512.
+constexpr int kRegsCompute = 208;
+constexpr int kRegsOther = 88;
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
 enum Mode { kDQ = 0, kDKV = 1 };
 
 template <int D, int MODE>
@@ -49,19 +78,23 @@ struct BwdCfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kBoxBytes = kTile * 128;
   static constexpr int kSlots = D == 128 ? 2 : 4;
-  // extra bytes per slot: doc ids (both modes) + LSE + Delta (dKV), 1024-aligned
-  static constexpr int kSlotExtra = MODE == kDKV ? 2048 : 1024;
+  // extra bytes per slot: doc ids, LSE and Delta of the streamed rows (the
+  // last two for dKV), 1024-aligned so the next slot's tiles stay aligned
+  static constexpr int kSlotExtra = 2048;
   static constexpr int kSlotBytes = 2 * kTileBytes + kSlotExtra;
   static constexpr int kOffFix = 0;
   static constexpr int kOffSlots = 2 * kTileBytes;
   static constexpr int kOffBars = kOffSlots + kSlots * kSlotBytes;
-  // fix_full, fix_empty, s_full, dp_full, p_full, ds_full, acc_done, acc_free, drain,
-  // slot_full[kSlots], slot_empty[kSlots]
-  static constexpr int kNumBars = 9 + 2 * kSlots;
-  static constexpr int kOffMisc = kOffBars + kNumBars * 8;
+  // fix_full, fix_empty, s_full, dp_full, p_full, ds_full, acc_done, acc_free,
+  // drain, dx_full, slot_full[kSlots], slot_empty[kSlots]
+  static constexpr int kNumBars = 10 + 2 * kSlots;
+  // per-row partial sums of Delta of the two warpgroups, double-buffered
+  static constexpr int kOffDx = (kOffBars + kNumBars * 8 + 15) & ~15;
+  static constexpr int kOffMisc = kOffDx + 2 * 2 * kTile * 4;
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
   static constexpr uint32_t kColAcc = 256;
+  static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
 };
 
 struct BwdArgs {
@@ -157,6 +190,73 @@ __global__ void delta_kernel(const __nv_bfloat16* __restrict__ o,
   if (lane == 0) delta[row] = acc;
 }
 
+// tanh of 16 values in place to fp32 accuracy: the odd Taylor series of
+// tanh at 0 through y^9 where every |y| of the warp's group is at most 1/4
+// (the first omitted term, 1382 y^11 / 155925, is below 9e-9 of tanh y
+// there), tanhf otherwise. The choice is uniform over the warp.
+__device__ __forceinline__ void tanh16(float (&y)[16]) {
+  float m = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 16; c += 2) m = fmax3(m, fabsf(y[c]), fabsf(y[c + 1]));
+  if (__all_sync(0xffffffffu, m <= 0.25f)) {
+    const float2 c3 = make_float2(-1.0f / 3.0f, -1.0f / 3.0f);
+    const float2 c5 = make_float2(2.0f / 15.0f, 2.0f / 15.0f);
+    const float2 c7 = make_float2(-17.0f / 315.0f, -17.0f / 315.0f);
+    const float2 c9 = make_float2(62.0f / 2835.0f, 62.0f / 2835.0f);
+#pragma unroll
+    for (int c = 0; c < 16; c += 2) {
+      const float2 v = make_float2(y[c], y[c + 1]);
+      const float2 v2 = fmul2(v, v);
+      float2 u = ffma2(v2, c9, c7);
+      u = ffma2(v2, u, c5);
+      u = ffma2(v2, u, c3);
+      u = fmul2(u, v2);
+      const float2 t = ffma2(v, u, v);
+      y[c] = t.x;
+      y[c + 1] = t.y;
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) y[c] = tanhf(y[c]);
+  }
+}
+
+// The bf16 pair of (a, b) and the bf16 pair of their rounding remainders:
+// hi + lo represents a and b to about 2^-17 of their magnitude.
+__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(a, b);
+  const float ha = __uint_as_float(hi << 16), hb = __uint_as_float(hi & 0xffff0000u);
+  lo = pack_bf16x2(a - ha, b - hb);
+}
+
+// TMEM column (within a 128-column S or dP block) of the 8 packed columns
+// that hold K-step kk (16 streamed rows) of a split operand: warpgroup kk / 4
+// wrote its hi parts at 64 (kk / 4) and its lo parts 32 columns further.
+__device__ __forceinline__ uint32_t hi_col(int kk) { return 64u * (kk >> 2) + 8u * (kk & 3); }
+
+// D(tmem) += A(tmem, 8 K-steps at hi_col + extra) * B(smem, MN-major), K = 128.
+// b_desc: descriptor of the B tile's first row; K-step kk advances 16 rows =
+// 2048 bytes (the start-address field counts 16-byte units).
+__device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_base, uint32_t extra,
+                                         uint64_t b_desc, uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk)
+    mma_bf16_ts(d_tmem, a_base + hi_col(kk) + extra, b_desc + (uint64_t)(kk * 128), idesc,
+                (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// D(tmem) = A(smem) * B(smem)^T over D (both K-major): K-step kk advances 32
+// bytes inside a 64-column box and moves to the next box every 4 steps.
+template <int D>
+__device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = (uint64_t)(((kk / 4) * kTile * 128 + (kk % 4) * 32) >> 4);
+    mma_bf16_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0);
+  }
+}
+
 template <int D, int SCORE, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -179,8 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_done = bars + 6;
   uint64_t* acc_free = bars + 7;
   uint64_t* drain = bars + 8;
-  uint64_t* slot_full = bars + 9;
-  uint64_t* slot_empty = bars + 9 + C::kSlots;
+  uint64_t* dx_full = bars + 9;
+  uint64_t* slot_full = bars + 10;
+  uint64_t* slot_empty = bars + 10 + C::kSlots;
+  float* sdx = reinterpret_cast<float*>(smem + C::kOffDx);  // [2 units][2 groups][128 rows]
   uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
@@ -193,11 +295,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(fix_empty, 1);
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_full, 128);
-    mbar_init(ds_full, 128);
+    mbar_init(p_full, kComputeWarps);  // one arrive per compute warp
+    mbar_init(ds_full, kComputeWarps);
     mbar_init(acc_done, 1);
-    mbar_init(acc_free, 128);
+    mbar_init(acc_free, kComputeWarps);
     mbar_init(drain, 1);
+    mbar_init(dx_full, kComputeWarps);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(slot_full + s, 1);
       mbar_init(slot_empty + s, 1);
@@ -224,192 +327,217 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_units = MODE == kDQ ? p.B * nq * p.Hq : p.B * nkv * p.Hkv;
   const int group = p.Hq / p.Hkv;
 
+  if (warp >= kComputeWarps) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+  }
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------- producer
-    {
-      // With ATTN_FAULT_NO_LOADS nothing is issued and the consumers' waits run out.
-      const bool leader = lane == 0 && !(p.fault_inject & ATTN_FAULT_NO_LOADS);
-      uint32_t slot_it = 0, fix_it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const BUnit U = decode_bwd<MODE>(a, u);
-        const int n = U.n();
-        if (n == 0) continue;
-        const int first = dense_first<MODE>(a, U);
-        ok = __all_sync(0xffffffffu, wait_bounded(fix_empty, (fix_it & 1) ^ 1, wd));
+    // With ATTN_FAULT_NO_LOADS nothing is issued and the consumers' waits run out.
+    const bool leader = lane == 0 && !(p.fault_inject & ATTN_FAULT_NO_LOADS);
+    uint32_t slot_it = 0, fix_it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const BUnit U = decode_bwd<MODE>(a, u);
+      const int n = U.n();
+      if (n == 0) continue;
+      const int first = dense_first<MODE>(a, U);
+      ok = __all_sync(0xffffffffu, wait_bounded(fix_empty, (fix_it & 1) ^ 1, wd));
+      if (!ok) break;
+      if (leader) {
+        mbar_arrive_expect_tx(fix_full, 2 * C::kTileBytes);
+        // dQ: Q and dO rows of (b, h, tile); dKV: K and V rows of (b, hk, tile)
+        const int row = MODE == kDQ ? (U.b * p.Hq + U.h) * p.Sq + U.tile * kTile
+                                    : (U.b * p.Hkv + U.h) * p.Skv + U.tile * kTile;
+        const CUtensorMap* m0 = MODE == kDQ ? &tm_q : &tm_k;
+        const CUtensorMap* m1 = MODE == kDQ ? &tm_do : &tm_v;
+        for (int bx = 0; bx < C::kBoxes; ++bx) {
+          tma_load_2d(sFix + bx * C::kBoxBytes, m0, fix_full, bx * 64, row);
+          tma_load_2d(sFix + C::kTileBytes + bx * C::kBoxBytes, m1, fix_full, bx * 64, row);
+        }
+      }
+      __syncwarp();
+      ++fix_it;
+      for (int it = 0; it < n && ok; ++it) {
+        int hoff, t;
+        bool partial;
+        U.at(it, hoff, t, partial);
+        t += first;
+        const int slot = slot_it % C::kSlots;
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(slot_empty + slot, ((slot_it / C::kSlots) & 1) ^ 1, wd));
         if (!ok) break;
-        if (leader) {
-          mbar_arrive_expect_tx(fix_full, 2 * C::kTileBytes);
-          // dQ: Q and dO rows of (b, h, tile); dKV: K and V rows of (b, hk, tile)
-          const int row = MODE == kDQ ? (U.b * p.Hq + U.h) * p.Sq + U.tile * kTile
-                                      : (U.b * p.Hkv + U.h) * p.Skv + U.tile * kTile;
-          const CUtensorMap* m0 = MODE == kDQ ? &tm_q : &tm_k;
-          const CUtensorMap* m1 = MODE == kDQ ? &tm_do : &tm_v;
+        uint8_t* base = sSlots + slot * C::kSlotBytes;
+        uint32_t bytes = 2 * C::kTileBytes;
+        if (has_doc) bytes += 512;
+        if (MODE == kDKV) bytes += 1024;
+        if (leader) mbar_arrive_expect_tx(slot_full + slot, bytes);
+        if (leader && MODE == kDQ) {
+          const int row = (U.b * p.Hkv + U.h / group) * p.Skv + t * kTile;
           for (int bx = 0; bx < C::kBoxes; ++bx) {
-            tma_load_2d(sFix + bx * C::kBoxBytes, m0, fix_full, bx * 64, row);
-            tma_load_2d(sFix + C::kTileBytes + bx * C::kBoxBytes, m1, fix_full, bx * 64, row);
+            tma_load_2d(base + bx * C::kBoxBytes, &tm_k, slot_full + slot, bx * 64, row);
+            tma_load_2d(base + C::kTileBytes + bx * C::kBoxBytes, &tm_v, slot_full + slot,
+                        bx * 64, row);
           }
+          if (has_doc)
+            bulk_load(base + 2 * C::kTileBytes,
+                      p.mask.doc_id + (size_t)U.b * p.mask.doc_len + t * kTile, 512,
+                      slot_full + slot);
+        } else if (leader) {
+          const int h = U.h * group + hoff;
+          const size_t qrow = (size_t)(U.b * p.Hq + h) * p.Sq + t * kTile;
+          for (int bx = 0; bx < C::kBoxes; ++bx) {
+            tma_load_2d(base + bx * C::kBoxBytes, &tm_q, slot_full + slot, bx * 64, (int)qrow);
+            tma_load_2d(base + C::kTileBytes + bx * C::kBoxBytes, &tm_do, slot_full + slot,
+                        bx * 64, (int)qrow);
+          }
+          if (has_doc)
+            bulk_load(base + 2 * C::kTileBytes,
+                      p.mask.doc_id + (size_t)U.b * p.mask.doc_len + t * kTile, 512,
+                      slot_full + slot);
+          bulk_load(base + 2 * C::kTileBytes + 512, p.lse + qrow, 512, slot_full + slot);
+          bulk_load(base + 2 * C::kTileBytes + 1024, a.delta + qrow, 512, slot_full + slot);
         }
         __syncwarp();
-        ++fix_it;
-        for (int it = 0; it < n && ok; ++it) {
-          int hoff, t;
-          bool partial;
-          U.at(it, hoff, t, partial);
-          t += first;
-          const int slot = slot_it % C::kSlots;
-          ok = __all_sync(0xffffffffu,
-                          wait_bounded(slot_empty + slot, ((slot_it / C::kSlots) & 1) ^ 1, wd));
-          if (!ok) break;
-          uint8_t* base = sSlots + slot * C::kSlotBytes;
-          uint32_t bytes = 2 * C::kTileBytes;
-          if (has_doc) bytes += 512;
-          if (MODE == kDKV) bytes += 1024;
-          if (leader) mbar_arrive_expect_tx(slot_full + slot, bytes);
-          if (leader && MODE == kDQ) {
-            const int row = (U.b * p.Hkv + U.h / group) * p.Skv + t * kTile;
-            for (int bx = 0; bx < C::kBoxes; ++bx) {
-              tma_load_2d(base + bx * C::kBoxBytes, &tm_k, slot_full + slot, bx * 64, row);
-              tma_load_2d(base + C::kTileBytes + bx * C::kBoxBytes, &tm_v, slot_full + slot,
-                          bx * 64, row);
-            }
-            if (has_doc)
-              bulk_load(base + 2 * C::kTileBytes,
-                        p.mask.doc_id + (size_t)U.b * p.mask.doc_len + t * kTile, 512,
-                        slot_full + slot);
-          } else if (leader) {
-            const int h = U.h * group + hoff;
-            const size_t qrow = (size_t)(U.b * p.Hq + h) * p.Sq + t * kTile;
-            for (int bx = 0; bx < C::kBoxes; ++bx) {
-              tma_load_2d(base + bx * C::kBoxBytes, &tm_q, slot_full + slot, bx * 64, (int)qrow);
-              tma_load_2d(base + C::kTileBytes + bx * C::kBoxBytes, &tm_do, slot_full + slot,
-                          bx * 64, (int)qrow);
-            }
-            if (has_doc)
-              bulk_load(base + 2 * C::kTileBytes,
-                        p.mask.doc_id + (size_t)U.b * p.mask.doc_len + t * kTile, 512,
-                        slot_full + slot);
-            bulk_load(base + 2 * C::kTileBytes + 512, p.lse + qrow, 512, slot_full + slot);
-            bulk_load(base + 2 * C::kTileBytes + 1024, a.delta + qrow, 512, slot_full + slot);
-          }
-          __syncwarp();
-          ++slot_it;
-        }
+        ++slot_it;
       }
-      if (!ok && !(p.fault_inject & ATTN_FAULT_NO_LOADS)) {  // let copies in flight land
-        for (uint32_t k = 0; k < C::kSlots && k < slot_it; ++k) {
-          const uint32_t it = slot_it - 1 - k;
-          wait_drain(slot_full + it % C::kSlots, (it / C::kSlots) & 1);
-        }
-        if (fix_it > 0) wait_drain(fix_full, (fix_it - 1) & 1);
+    }
+    if (!ok && !(p.fault_inject & ATTN_FAULT_NO_LOADS)) {  // let copies in flight land
+      for (uint32_t k = 0; k < C::kSlots && k < slot_it; ++k) {
+        const uint32_t it = slot_it - 1 - k;
+        wait_drain(slot_full + it % C::kSlots, (it / C::kSlots) & 1);
       }
+      if (fix_it > 0) wait_drain(fix_full, (fix_it - 1) & 1);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    {
-      const bool leader = lane == 0;
-      constexpr uint32_t kIdescSS = idesc_bf16(128, 128, false);
-      constexpr uint32_t kIdescTS = idesc_bf16(128, D, true);
-      const uint32_t fix_addr = smem_u32(sFix);
-      const uint32_t slots_addr = smem_u32(sSlots);
-      uint32_t slot_it = 0, fix_it = 0, p_it = 0, ds_it = 0, acc_it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-        const BUnit U = decode_bwd<MODE>(a, u);
-        const int n = U.n();
-        if (n == 0) continue;
-        ok = __all_sync(0xffffffffu, wait_bounded(fix_full, fix_it & 1, wd));
-        if (!ok) break;
-        ++fix_it;
-        tc_fence_after();
-        for (int it = 0; it < n && ok; ++it) {
-          const uint32_t seq = slot_it + it;
-          const uint32_t slot = seq % C::kSlots;
-          ok = __all_sync(0xffffffffu, wait_bounded(slot_full + slot, (seq / C::kSlots) & 1, wd));
+    // The whole warp runs the loop (waits stay converged); lane 0 issues.
+    const bool leader = lane == 0;
+    constexpr uint32_t kIdescSS = idesc_bf16(128, 128, false);
+    constexpr uint32_t kIdescTS = idesc_bf16(128, D, true);
+    // shared-memory descriptors: K-major (SS operands) and MN-major (B of the
+    // TS products) views of the fixed tiles and of ring slot 0; other slots
+    // and tiles add their byte offset >> 4
+    const uint64_t dFixK = sdesc_sw128(smem_u32(sFix), 16, 1024);
+    const uint64_t dSlotK = sdesc_sw128(smem_u32(sSlots), 16, 1024);
+    const uint64_t dSlotMN = sdesc_sw128(smem_u32(sSlots), C::kBoxBytes, 1024);
+    constexpr uint64_t kTileOff = C::kTileBytes >> 4;
+    const uint32_t colS = tmem, colP = tmem + 128, acc0 = tmem + C::kColAcc,
+                   acc1 = tmem + C::kColAcc + D;
+    uint32_t slot_it = 0, fix_it = 0, p_it = 0, ds_it = 0, acc_it = 0;
+    bool ok = true;
+    auto slot_off = [&](uint32_t seq) {
+      return (uint64_t)(((seq % C::kSlots) * C::kSlotBytes) >> 4);
+    };
+    // S = fix0 . slot0^T into S, dP = fix1 . slot1^T into dP
+    auto issue_s = [&](uint32_t seq) {
+      if (leader) {
+        issue_ss<D>(colS, dFixK, dSlotK + slot_off(seq), kIdescSS);
+        mma_commit(s_full);
+      }
+    };
+    auto issue_dp = [&](uint32_t seq) {
+      if (leader) {
+        issue_ss<D>(colP, dFixK + kTileOff, dSlotK + slot_off(seq) + kTileOff, kIdescSS);
+        mma_commit(dp_full);
+      }
+    };
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      const BUnit U = decode_bwd<MODE>(a, u);
+      const int n = U.n();
+      if (n == 0) continue;
+      ok = __all_sync(0xffffffffu, wait_bounded(fix_full, fix_it & 1, wd));
+      if (!ok) break;
+      ++fix_it;
+      ok = __all_sync(0xffffffffu, wait_bounded(slot_full + slot_it % C::kSlots,
+                                                (slot_it / C::kSlots) & 1, wd));
+      if (!ok) break;
+      tc_fence_after();
+      issue_s(slot_it);
+      issue_dp(slot_it);
+      if (n == 1 && leader) mma_commit(fix_empty);  // the fixed tiles are read by S and dP only
+      __syncwarp();
+      for (int it = 0; it < n && ok; ++it) {
+        const uint32_t seq = slot_it + it;
+        const uint64_t s0 = dSlotMN + slot_off(seq);  // K (dQ) or Q (dKV), as B
+        const uint64_t s1 = s0 + kTileOff;             // V (dQ) or dO (dKV), as B
+        if (it == 0) {  // the accumulators of the previous unit have been read
+          ok = __all_sync(0xffffffffu, wait_bounded(acc_free, (acc_it & 1) ^ 1, wd));
           if (!ok) break;
+        }
+        const bool acc = it > 0;
+        if constexpr (MODE == kDKV) {
+          // dV += P^T dO (hi, lo parts over S)
+          ok = __all_sync(0xffffffffu, wait_bounded(p_full, p_it & 1, wd));
+          if (!ok) break;
+          ++p_it;
           tc_fence_after();
-          const uint32_t s0 = slots_addr + slot * C::kSlotBytes;  // K (dQ) or Q (dKV)
-          const uint32_t s1 = s0 + C::kTileBytes;                 // V (dQ) or dO (dKV)
-          // S = fix0 . slot0^T and dP = fix1 . slot1^T (K-major operands)
           if (leader) {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
-              mma_bf16_ss(tmem, sdesc_sw128(fix_addr + off, 16, 1024),
-                          sdesc_sw128(s0 + off, 16, 1024), kIdescSS, kk > 0);
-            }
-            mma_commit(s_full);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk / 4) * C::kBoxBytes + (kk % 4) * 32;
-              mma_bf16_ss(tmem + 128, sdesc_sw128(fix_addr + C::kTileBytes + off, 16, 1024),
-                          sdesc_sw128(s1 + off, 16, 1024), kIdescSS, kk > 0);
-            }
-            mma_commit(dp_full);
+            issue_ts(acc0, colS, 0, s1, kIdescTS, acc);
+            issue_ts(acc0, colS, 32, s1, kIdescTS, true);
           }
-          __syncwarp();
-          if (it == 0) {
-            ok = __all_sync(0xffffffffu, wait_bounded(acc_free, (acc_it & 1) ^ 1, wd));
-            if (!ok) break;
-          }
-          if (MODE == kDKV) {  // dV += P^T dO (B = dO tile, MN-major)
-            ok = __all_sync(0xffffffffu, wait_bounded(p_full, p_it & 1, wd));
-            if (!ok) break;
-            ++p_it;
-            tc_fence_after();
-            if (leader) {
-#pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk)
-                mma_bf16_ts(tmem + C::kColAcc, tmem + kk * 8,
-                            sdesc_sw128(s1 + kk * 16 * 128, C::kBoxBytes, 1024), kIdescTS,
-                            (it > 0 || kk > 0) ? 1u : 0u);
-            }
-            __syncwarp();
-          }
+        } else {
+          // B += (P g) K and A += lo K (operands over S)
           ok = __all_sync(0xffffffffu, wait_bounded(ds_full, ds_it & 1, wd));
           if (!ok) break;
           ++ds_it;
           tc_fence_after();
-          // dQ: A += (P g dP) K, B += (P g) K;   dKV: dK += dS^T Q   (B = slot0, MN-major)
           if (leader) {
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_bf16_ts(tmem + C::kColAcc + D, tmem + 128 + kk * 8,
-                          sdesc_sw128(s0 + kk * 16 * 128, C::kBoxBytes, 1024), kIdescTS,
-                          (it > 0 || kk > 0) ? 1u : 0u);
-            if (MODE == kDQ) {
-#pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk)
-                mma_bf16_ts(tmem + C::kColAcc, tmem + kk * 8,
-                            sdesc_sw128(s0 + kk * 16 * 128, C::kBoxBytes, 1024), kIdescTS,
-                            (it > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(slot_empty + slot);
+            issue_ts(acc1, colS, 0, s0, kIdescTS, acc);
+            issue_ts(acc0, colS, 32, s0, kIdescTS, acc);
           }
-          __syncwarp();
-        }
-        if (!ok) break;
-        ++acc_it;
-        if (leader) {
-          mma_commit(acc_done);
-          mma_commit(fix_empty);
         }
         __syncwarp();
-        slot_it += n;
+        if (it + 1 < n) {  // S of the next tile (its P/lo operands over S are consumed)
+          ok = __all_sync(0xffffffffu, wait_bounded(slot_full + (seq + 1) % C::kSlots,
+                                                    ((seq + 1) / C::kSlots) & 1, wd));
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(seq + 1);
+          __syncwarp();
+        }
+        if constexpr (MODE == kDKV) {
+          // dK += dS^T Q (hi, lo parts over dP)
+          ok = __all_sync(0xffffffffu, wait_bounded(ds_full, ds_it & 1, wd));
+          if (!ok) break;
+          ++ds_it;
+          tc_fence_after();
+          if (leader) {
+            issue_ts(acc1, colP, 0, s0, kIdescTS, acc);
+            issue_ts(acc1, colP, 32, s0, kIdescTS, true);
+          }
+        } else {
+          // A += hi K (operand over dP)
+          if (leader) issue_ts(acc0, colP, 0, s0, kIdescTS, true);
+        }
+        if (leader) mma_commit(slot_empty + seq % C::kSlots);
+        __syncwarp();
+        if (it + 1 < n) {  // dP of the next tile (the operands over dP are consumed)
+          issue_dp(seq + 1);
+          if (it + 2 == n && leader) mma_commit(fix_empty);
+          __syncwarp();
+        }
       }
-      if (leader) mma_commit(drain);
+      if (!ok) break;
+      ++acc_it;
+      if (leader) mma_commit(acc_done);
       __syncwarp();
-      wait_drain(drain, 0);
+      slot_it += n;
     }
-  } else {
+    if (leader) mma_commit(drain);
+    __syncwarp();
+    wait_drain(drain, 0);
+  } else if (warp < kComputeWarps) {
     // ------------------------------------------------------------- compute
-    const int t = threadIdx.x;  // row of the fixed tile == TMEM lane
-    const uint32_t lane_base = uint32_t(warp * 32) << 16;
-    const uint32_t colS = tmem + lane_base;
-    const uint32_t colP = tmem + lane_base + 128;
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsCompute));
+    const int g = warp >> 2;           // column half of the streamed tile
+    const int t = threadIdx.x & 127;   // row of the fixed tile == TMEM lane
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+    const uint32_t colS = tmem + lane_base + 64 * g;
+    const uint32_t colP = tmem + lane_base + 128 + 64 * g;
     const uint32_t colAcc = tmem + lane_base + C::kColAcc;
     const float scale = p.score.scale;
-    uint32_t slot_it = 0, s_it = 0, acc_it = 0;
+    const float cap = p.score.softcap, inv_cap = 1.0f / p.score.softcap;
+    uint32_t slot_it = 0, s_it = 0, acc_it = 0, dx_it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
       const BUnit U = decode_bwd<MODE>(a, u);
@@ -417,18 +545,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int first = dense_first<MODE>(a, U);
       // the thread's own row: a query row (dQ) or a key row (dKV)
       const int r = U.tile * kTile + t;
+      constexpr int kHalfD = D / 2;  // accumulator columns stored by each warpgroup
       if (n == 0) {
         const uint4 z = make_uint4(0, 0, 0, 0);
         if (MODE == kDQ) {
           const size_t qrow = (size_t)(U.b * p.Hq + U.h) * p.Sq + r;
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) + qrow * D);
-          for (int c = 0; c < D / 8; ++c) dst[c] = z;
-          a.delta_out[qrow] = 0.0f;
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) + qrow * D +
+                                                g * kHalfD);
+          for (int c = 0; c < kHalfD / 8; ++c) dst[c] = z;
+          if (g == 0) a.delta_out[qrow] = 0.0f;
         } else {
-          const size_t off = ((size_t)(U.b * p.Hkv + U.h) * p.Skv + r) * D;
+          const size_t off = ((size_t)(U.b * p.Hkv + U.h) * p.Skv + r) * D + g * kHalfD;
           uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk) + off);
           uint4* dv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dv) + off);
-          for (int c = 0; c < D / 8; ++c) dk[c] = z, dv[c] = z;
+          for (int c = 0; c < kHalfD / 8; ++c) dk[c] = z, dv[c] = z;
         }
         continue;
       }
@@ -441,7 +571,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float l = p.lse[qrow];
         row_lse2 = l == -INFINITY ? INFINITY : l * kLog2e;  // empty row: every p is 0
         row_dhat = a.delta[qrow];  // estimate from the bf16 O (delta_kernel)
-        row_delta = 0.0f;          // exact: sum_j P dP, accumulated below
       }
       for (int it = 0; it < n; ++it) {
         int hoff, tt;
@@ -450,90 +579,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tt += first;
         const int h = MODE == kDQ ? U.h : U.h * group + hoff;
         const uint32_t seq = slot_it + it;
-        const uint32_t slot = seq % C::kSlots;
-        const uint8_t* base = sSlots + slot * C::kSlotBytes;
-        const int* sdoc = reinterpret_cast<const int*>(base + 2 * C::kTileBytes);
-        const float* slse = reinterpret_cast<const float*>(base + 2 * C::kTileBytes + 512);
-        const float* sdelta = reinterpret_cast<const float*>(base + 2 * C::kTileBytes + 1024);
+        const uint8_t* base = sSlots + (seq % C::kSlots) * C::kSlotBytes;
+        const int* sdoc = reinterpret_cast<const int*>(base + 2 * C::kTileBytes) + 64 * g;
+        const float* slse = reinterpret_cast<const float*>(base + 2 * C::kTileBytes + 512) + 64 * g;
+        const float* sdel = reinterpret_cast<const float*>(base + 2 * C::kTileBytes + 1024) + 64 * g;
         // the slot's shared-memory extras (doc ids, LSE, Delta) are read directly
-        ok = __all_sync(0xffffffffu, wait_bounded(slot_full + slot, (seq / C::kSlots) & 1, wd));
+        ok = __all_sync(0xffffffffu,
+                        wait_bounded(slot_full + seq % C::kSlots, (seq / C::kSlots) & 1, wd));
         if (!ok) break;
         ok = __all_sync(0xffffffffu, wait_bounded(s_full, s_it & 1, wd));
         if (!ok) break;
-        const int c0 = tt * kTile;  // first column position (key for dQ, query for dKV)
-        if constexpr (MODE == kDQ) {
-          // Wait for S and dP; 32 columns at a time: P g -> S columns, P g dP -> dP
-          // columns (bf16, packed below the columns still to be read), Delta += P dP.
-          ok = __all_sync(0xffffffffu, wait_bounded(dp_full, s_it & 1, wd));
-          if (!ok) break;
-          ++s_it;
-          tc_fence_after();
-          const float slope = (SCORE & 1) ? alibi_slope(p.score, h) : 0.0f;
-          int lo = INT_MIN, hi = INT_MAX, pre = INT_MIN;  // row i = r, column j = c0 + c
-          if (partial) {
-            if (p.variant & ATTN_MASK_CAUSAL) hi = r - c0 + 1;
-            if (p.variant & ATTN_MASK_WINDOW) lo = r - c0 - p.mask.window + 1;
-            if (P != INT_MIN) pre = P - c0;
-          }
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            uint32_t rs[32], rp[32];
-            tmem_ld32(colS + 32 * qq, rs);
-            tmem_ld32(colP + 32 * qq, rp);
-            tmem_ld_wait_regs(rs);
-            tmem_ld_wait_regs(rp);
-            uint32_t pg_pk[16], pd_pk[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float pg2[2], pd2[2];
-#pragma unroll
-              for (int z = 0; z < 2; ++z) {
-                const int c = 32 * qq + e + z;
-                float x = __uint_as_float(rs[e + z]) * scale, g = 1.0f;
-                if constexpr ((SCORE & 1) != 0) x = fmaf(slope, float(c0 - r + c), x);
-                if constexpr ((SCORE & 2) != 0) {
-                  const float th = tanh_approx(x * (1.0f / p.score.softcap));
-                  x = p.score.softcap * th;
-                  g = 1.0f - th * th;
-                }
-                float pr = ex2_approx(fmaf(x, kLog2e, -row_lse2));
-                if (partial) {
-                  // bitwise terms, document id read on a warp-uniform condition:
-                  // no divergent branch per element
-                  const bool same = docb ? (sdoc[c] == my_doc) : true;
-                  const bool keep = ((c >= lo) & (c < hi) & same) | (c < pre);
-                  pr = keep ? pr : 0.0f;
-                }
-                const float dp = __uint_as_float(rp[e + z]);
-                row_delta = fmaf(pr, dp, row_delta);
-                pg2[z] = pr * g;
-                pd2[z] = pg2[z] * (dp - row_dhat);
-              }
-              pg_pk[e >> 1] = pack_bf16x2(pg2[0], pg2[1]);
-              pd_pk[e >> 1] = pack_bf16x2(pd2[0], pd2[1]);
-            }
-            tmem_st16(colS + 16 * qq, pg_pk);
-            tmem_st16(colP + 16 * qq, pd_pk);
-          }
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(ds_full);
-          continue;
-        }
         tc_fence_after();
-        float v[kTile];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t rr[32];
-          tmem_ld32(colS + 32 * c, rr);
-          tmem_ld_wait_regs(rr);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[32 * c + e] = __uint_as_float(rr[e]);
-        }
+        const int c0 = tt * kTile + 64 * g;  // position of this warpgroup's first column
         const float slope = (SCORE & 1) ? alibi_slope(p.score, h) : 0.0f;
-        // (j - i) = base_ji + sgn * c
-        const int base_ji = MODE == kDQ ? c0 - r : r - c0;
-        const float sgn = MODE == kDQ ? 1.0f : -1.0f;
+        // mask bounds on the column c of this warpgroup's 64 (see below)
         int lo = INT_MIN, hi = INT_MAX, pre = INT_MIN;
         if (partial) {
           if (MODE == kDQ) {  // row i = r, column j = c0 + c
@@ -546,104 +605,179 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (P != INT_MIN && r < P) pre = INT_MAX;
           }
         }
-        // v <- P * score_mod'(s), the factor dS needs; for dKV, P itself (bf16)
-        // goes to TMEM as the A operand of dV += P^T dO, 64 columns at a time.
+        // (j - i) = base_ji + sgn * c
+        const int base_ji = MODE == kDQ ? c0 - r : r - c0;
+        const float sgn = MODE == kDQ ? 1.0f : -1.0f;
+        // P (and P g) from S, 16 columns at a time; v keeps P g for dS
+        constexpr bool kKeepP = MODE == kDQ && (SCORE & 2) != 0;  // Delta needs P itself
+        float v[64];
+        float pf[kKeepP ? 64 : 1];
+        {
+          uint32_t rr[64];
+          tmem_ld32(colS, *reinterpret_cast<uint32_t(*)[32]>(rr));
+          tmem_ld32(colS + 32, *reinterpret_cast<uint32_t(*)[32]>(rr + 32));
+          tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(rr));
+          tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(rr + 32));
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
-          float prev = 0.0f;
+          for (int e = 0; e < 64; ++e) v[e] = __uint_as_float(rr[e]);
+        }
 #pragma unroll
-          for (int e = 0; e < 64; ++e) {
-            const int c = 64 * half + e;
-            float x = v[c] * scale, g = 1.0f;
-            if constexpr ((SCORE & 1) != 0) x = fmaf(slope, float(base_ji) + sgn * float(c), x);
+        for (int h2 = 0; h2 < 2; ++h2) {  // 32 columns: 16 packed TMEM columns per part
+          uint32_t hi16[16], lo16[16];
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const int q = 2 * h2 + q2;
+            float x[16], gg[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int c = 16 * q + e;
+              x[e] = v[c] * scale;
+              if constexpr ((SCORE & 1) != 0)
+                x[e] = fmaf(slope, float(base_ji) + sgn * float(c), x[e]);
+              gg[e] = 1.0f;
+            }
             if constexpr ((SCORE & 2) != 0) {
-              const float th = tanh_approx(x * (1.0f / p.score.softcap));
-              x = p.score.softcap * th;
-              g = 1.0f - th * th;
+              float th[16];
+#pragma unroll
+              for (int e = 0; e < 16; ++e) th[e] = x[e] * inv_cap;
+              tanh16(th);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                x[e] = cap * th[e];
+                gg[e] = fmaf(-th[e], th[e], 1.0f);
+              }
             }
-            float lse2 = row_lse2;
-            if constexpr (MODE == kDKV) lse2 = slse[c] == -INFINITY ? INFINITY : slse[c] * kLog2e;
-            float pr = ex2_approx(fmaf(x, kLog2e, -lse2));
-            if (partial) {
-              // bitwise terms, document id read on a warp-uniform condition:
-              // no divergent branch per element
-              const bool same = docb ? (sdoc[c] == my_doc) : true;
-              const bool keep = ((c >= lo) & (c < hi) & same) | (c < pre);
-              pr = keep ? pr : 0.0f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int c = 16 * q + e;
+              float lse2 = row_lse2;
+              if constexpr (MODE == kDKV)
+                lse2 = slse[c] == -INFINITY ? INFINITY : slse[c] * kLog2e;
+              float pr = ex2_approx(fmaf(x[e], kLog2e, -lse2));
+              if (partial) {
+                // bitwise terms, document id read on a warp-uniform condition:
+                // no divergent branch per element
+                const bool same = docb ? (sdoc[c] == my_doc) : true;
+                const bool keep = ((c >= lo) & (c < hi) & same) | (c < pre);
+                pr = keep ? pr : 0.0f;
+              }
+              x[e] = pr;
+              v[c] = pr * gg[e];
+              if constexpr (kKeepP) pf[c] = pr;
             }
-            if constexpr (MODE == kDKV) {
-              if (e & 1) pk[e >> 1] = pack_bf16x2(prev, pr);
-              else prev = pr;
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              if constexpr (MODE == kDKV)  // P^T, split, for dV += P^T dO
+                split_bf16x2(x[e], x[e + 1], hi16[8 * q2 + e / 2], lo16[8 * q2 + e / 2]);
+              else  // P g in bf16, for B += (P g) K
+                hi16[8 * q2 + e / 2] = pack_bf16x2(v[16 * q + e], v[16 * q + e + 1]);
             }
-            v[c] = pr * g;
           }
-          if constexpr (MODE == kDKV) tmem_st32(colS + 32 * half, pk);
+          tmem_st16(colS + 16 * h2, hi16);
+          if constexpr (MODE == kDKV) tmem_st16(colS + 32 + 16 * h2, lo16);
         }
         if constexpr (MODE == kDKV) {
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(p_full);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_full);
         }
         ok = __all_sync(0xffffffffu, wait_bounded(dp_full, s_it & 1, wd));
         if (!ok) break;
         ++s_it;
         tc_fence_after();
-        // dS = p g (dP - Delta) -> bf16 into the first 64 columns of dP
+        // dKV: dS = P g (dP - Delta);  dQ: P g (dP - Dhat) and Delta += P dP.
+        // Split into hi and lo parts, 32 columns at a time; every part goes
+        // over columns this warpgroup has already read (the dKV lo parts of
+        // the first 32 columns wait for the second half's load).
+        uint32_t dl0[16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int hh = 0; hh < 2; ++hh) {
           uint32_t rr[32];
-          tmem_ld32(colP + 32 * c, rr);
+          tmem_ld32(colP + 32 * hh, rr);
           tmem_ld_wait_regs(rr);
+          uint32_t dh[16], dl[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int cc = 32 * c + e;
-            const float dl = MODE == kDQ ? row_delta : sdelta[cc];
-            v[cc] = v[cc] * (__uint_as_float(rr[e]) - dl);
+          for (int e = 0; e < 32; e += 2) {
+            const int c = 32 * hh + e;
+            const float dp0 = __uint_as_float(rr[e]), dp1 = __uint_as_float(rr[e + 1]);
+            float ds0, ds1;
+            if constexpr (MODE == kDKV) {
+              ds0 = v[c] * (dp0 - sdel[c]);
+              ds1 = v[c + 1] * (dp1 - sdel[c + 1]);
+            } else {
+              ds0 = v[c] * (dp0 - row_dhat);
+              ds1 = v[c + 1] * (dp1 - row_dhat);
+              if constexpr (kKeepP) {
+                row_delta = fmaf(pf[c], dp0, row_delta);
+                row_delta = fmaf(pf[c + 1], dp1, row_delta);
+              } else {  // identity or ALiBi score_mod: P g = P
+                row_delta = fmaf(v[c], dp0, row_delta);
+                row_delta = fmaf(v[c + 1], dp1, row_delta);
+              }
+            }
+            split_bf16x2(ds0, ds1, dh[e / 2], dl[e / 2]);
           }
-        }
+          tmem_st16(colP + 16 * hh, dh);
+          if constexpr (MODE == kDKV) {
+            if (hh == 0) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t rr[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) rr[e] = pack_bf16x2(v[64 * c + 2 * e], v[64 * c + 2 * e + 1]);
-          tmem_st32(colP + 32 * c, rr);
+              for (int e = 0; e < 16; ++e) dl0[e] = dl[e];
+            } else {
+              tmem_st16(colP + 32, dl0);
+              tmem_st16(colP + 48, dl);
+            }
+          } else {
+            tmem_st16(colS + 32 + 16 * hh, dl);  // beside P g over S
+          }
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(ds_full);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ds_full);
       }
       if (!ok) break;
       slot_it += n;
-      // epilogue
+      // epilogue: each warpgroup stores half of the accumulator columns
       ok = __all_sync(0xffffffffu, wait_bounded(acc_done, acc_it & 1, wd));
       if (!ok) break;
       ++acc_it;
       tc_fence_after();
-      auto store_row = [&](uint32_t col, __nv_bfloat16* dst, float mul) {
+      auto store_half = [&](uint32_t col, __nv_bfloat16* dst, float mul) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < kHalfD / 32; ++c) {
           uint32_t rr[32];
           tmem_ld32(col + 32 * c, rr);
           tmem_ld_wait_regs(rr);
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * mul, __uint_as_float(rr[2 * e + 1]) * mul);
+            pk[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * mul,
+                                __uint_as_float(rr[2 * e + 1]) * mul);
           uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          for (int e = 0; e < 4; ++e)
+            d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
       };
       if (MODE == kDQ) {  // dQ = scale (A - (Delta - Dhat) B); Delta to the workspace
+        // the two warpgroups' partial sums of Delta meet in shared memory
+        float* dx = sdx + (dx_it & 1) * 2 * kTile;
+        dx[g * kTile + t] = row_delta;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dx_full);
+        ok = __all_sync(0xffffffffu, wait_bounded(dx_full, dx_it & 1, wd));
+        if (!ok) break;
+        ++dx_it;
+        const float delta = dx[t] + dx[kTile + t];
         const size_t qrow = (size_t)(U.b * p.Hq + U.h) * p.Sq + r;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + qrow * D;
-        const float corr = row_delta - row_dhat;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + qrow * D + g * kHalfD;
+        const float corr = delta - row_dhat;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < kHalfD / 32; ++c) {
           uint32_t ra[32], rb[32];
-          tmem_ld32(colAcc + D + 32 * c, ra);
-          tmem_ld32(colAcc + 32 * c, rb);
+          tmem_ld32(colAcc + g * kHalfD + 32 * c, ra);
+          tmem_ld32(colAcc + D + g * kHalfD + 32 * c, rb);
           tmem_ld_wait_regs(ra);
           tmem_ld_wait_regs(rb);
           uint32_t pk[16];
@@ -657,14 +791,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
-        a.delta_out[qrow] = row_delta;
+        if (g == 0) a.delta_out[qrow] = delta;
       } else {
-        const size_t off = ((size_t)(U.b * p.Hkv + U.h) * p.Skv + r) * D;
-        store_row(colAcc, static_cast<__nv_bfloat16*>(a.dv) + off, 1.0f);
-        store_row(colAcc + D, static_cast<__nv_bfloat16*>(a.dk) + off, scale);
+        const size_t off = ((size_t)(U.b * p.Hkv + U.h) * p.Skv + r) * D + g * kHalfD;
+        store_half(colAcc + g * kHalfD, static_cast<__nv_bfloat16*>(a.dv) + off, 1.0f);
+        store_half(colAcc + D + g * kHalfD, static_cast<__nv_bfloat16*>(a.dk) + off, scale);
       }
       tc_fence_before();
-      mbar_arrive(acc_free);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_free);
     }
   }
 

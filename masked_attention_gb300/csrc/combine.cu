@@ -17,6 +17,7 @@
 #include <cstdint>
 
 #include "mattn.h"
+#include "status.h"
 
 #define MATTN_API extern "C" __attribute__((visibility("default")))
 
@@ -152,5 +153,5 @@ MATTN_API attn_status attn_combine(const void* o_parts, const float* lse_parts, 
   else
     e = D == 64 ? launch_combine<64, false>(o_parts, lse_parts, n_parts, rows, o, lse, s)
                 : launch_combine<128, false>(o_parts, lse_parts, n_parts, rows, o, lse, s);
-  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return mattn::cuda_status(e);
 }

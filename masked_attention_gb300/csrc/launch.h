@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "status.h"
 
 namespace mattn {
 
@@ -48,5 +49,12 @@ cudaError_t launch_fwd_tc(const FwdProblem& p, cudaStream_t stream);
 cudaError_t launch_fwd_tc_rb(const FwdProblem& p, cudaStream_t stream);     // relative bias
 cudaError_t launch_fwd_tc_paged(const FwdProblem& p, cudaStream_t stream);  // paged K/V
 cudaError_t launch_bwd_tc(const BwdProblem& p, cudaStream_t stream);
+
+// The checks attn_bwd makes on everything but its workspace (no CUDA call);
+// fills bp.f when they pass.
+attn_status bwd_check_args(BwdProblem& bp, const void* q, const void* k, const void* v,
+                           const void* o, const float* lse, const void* dO, void* dq, void* dk,
+                           void* dv, int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                           unsigned variant, const attn_params* p);
 
 }  // namespace mattn

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include "mattn.h"
+#include "status.h"
 
 #define MATTN_API extern "C" __attribute__((visibility("default")))
 
@@ -42,5 +43,5 @@ MATTN_API attn_status attn_doc_ids_from_seqlens(const int* cu_seqlens, int n, in
   if (blocks > 4096) blocks = 4096;
   mattn::seqlens_to_doc_kernel<<<blocks, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       cu_seqlens, n, total, doc_id);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return mattn::cuda_status(cudaGetLastError());
 }

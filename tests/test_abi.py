@@ -83,6 +83,11 @@ def test_struct_layout_matches_c(M, tmp_path):
             assert int(got[f"{s}.{f}"]) == getattr(cls, f).offset, f"{s}.{f}"
 
 
+def test_last_cuda_error_starts_clean(M):
+    """No CUDA call has failed on this thread: the name is cudaSuccess."""
+    assert M.attn_last_cuda_error() == "cudaSuccess"
+
+
 def test_status_strings(M):
     for code in range(7):
         assert M.attn_status_str(code)

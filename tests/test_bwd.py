@@ -2,26 +2,20 @@
 fp64 gradients (FlexAttention page, "Performance": a deterministic backward
 that recomputes intermediates).
 
-Tolerance: the 1e-2 bound on bf16 outputs applies to the computed value, on
-top of the unavoidable rounding of the output itself to bf16:
-|g - g_ref| <= 1e-2 + 0.5 ulp_bf16(g_ref). (Rounding alone costs half an ulp,
-0.0078 for |g| in [2, 4) and 0.0156 in [4, 8); the products round P and dS to
-bf16, relative 2^-9 per term, which is what the 1e-2 budget covers.)
+Tolerance: the flat bound max|g - g_ref| <= 1e-2 on the bf16 outputs dQ, dK
+and dV. Rounding an output to bf16 alone costs half an ulp, 0.0156 once
+|g_ref| >= 4; only such elements, and only within one bf16 ulp of g_ref, are
+exempt, and they are counted, printed and capped (tests/helpers.py,
+check_bf16).
 """
 import numpy as np
 import pytest
 
 from oracle import attention_backward
 from synth import make_workload
-from tests.helpers import DeviceRun, oracle_spec
+from tests.helpers import DeviceRun, check_bf16, oracle_spec
 
 pytestmark = pytest.mark.gpu
-
-
-def grad_tol(ref):
-    a = np.abs(ref)
-    ulp = np.where(a > 0, 2.0 ** (np.floor(np.log2(np.maximum(a, 1e-30))) - 7), 0.0)
-    return 1e-2 + 0.5 * ulp
 
 
 def run_bwd(w, use_block_mask=True):
@@ -49,10 +43,7 @@ def check_grads(w, dq, dk, dv, heads=None):
             sel = [(b, h if name == "dq" else h // (w.Hq // w.Hkv)) for b, h in heads]
             got = np.stack([got[b, h] for b, h in sel])
             ref = np.stack([ref[b, h] for b, h in sel])
-        err = np.abs(got - ref)
-        bad = err > grad_tol(ref)
-        out[name] = float(err.max())
-        assert not bad.any(), (name, float(err.max()), int(bad.sum()))
+        out[name] = check_bf16(got, ref, f"{name} {w.name}")["max_err"]
     return out
 
 

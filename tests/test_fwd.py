@@ -3,8 +3,10 @@ seeded inputs.
 
 Tolerances (1e-2 on bf16 O and 1e-4 on fp32 O are the stated bounds; the
 derivation of the others is beside each constant):
-* bf16 O: |O - O_ref| <= max(1e-2, 0.5 ulp_bf16(O_ref) + 2e-3). Rounding O to
-  bf16 alone costs half an ulp, which exceeds 1e-2 once |O_ref| >= 4.
+* bf16 O: max|O - O_ref| <= 1e-2 (flat). Rounding O to bf16 alone costs half
+  an ulp, which exceeds 1e-2 once |O_ref| >= 4: such elements are exempt when
+  they lie within one bf16 ulp of O_ref, and they are counted, printed and
+  capped (tests/helpers.py, check_bf16).
 * bf16 LSE: 2e-3 without soft-capping; with it, the hardware tanh (relative
   error below 2^-10.9) adds up to |s'| * 2^-10.9 <= 50 * tanh(|s|/50) * 5.3e-4,
   bounded here per row through the oracle's largest |s'|.
@@ -17,17 +19,11 @@ import pytest
 
 from oracle import attention_forward
 from synth import make_workload
-from tests.helpers import DeviceRun, oracle_spec
+from tests.helpers import DeviceRun, check_bf16, oracle_spec
 
 pytestmark = pytest.mark.gpu
 
 TANH_REL = 2.0 ** -10.9
-
-
-def bf16_o_tol(ref):
-    a = np.abs(ref)
-    ulp = np.where(a > 0, 2.0 ** (np.floor(np.log2(np.maximum(a, 1e-30))) - 7), 0.0)
-    return np.maximum(1e-2, 0.5 * ulp + 2e-3)
 
 
 def lse_tol(w, ref_lse):
@@ -50,10 +46,7 @@ def check(w, O, L, O_ref, L_ref, rows=None):
         err = np.abs(O - O_ref)[mask]
         assert err.max() <= 1e-4, err.max()
     else:
-        err = np.abs(O - O_ref)
-        tol = bf16_o_tol(O_ref)
-        bad = (err > tol) & mask[..., None]
-        assert not bad.any(), (err[mask].max(), int(bad.sum()))
+        check_bf16(O, O_ref, f"O {w.name}", valid=mask[..., None])
     both_inf = np.isneginf(L) & np.isneginf(L_ref)
     with np.errstate(invalid="ignore"):
         lerr = np.where(both_inf, 0.0, np.abs(L - L_ref))[mask]
@@ -211,8 +204,7 @@ def test_full_size_workloads_sampled(number):
     Oc = O.float().cpu().numpy()
     Lc = L.cpu().numpy()
     for b, h in heads:
-        err = np.abs(Oc[b, h, sel] - O_ref[b, h, sel])
-        assert (err <= bf16_o_tol(O_ref[b, h, sel])).all(), err.max()
+        check_bf16(Oc[b, h, sel], O_ref[b, h, sel], f"O workload {number} head {(b, h)}")
         lerr = np.abs(Lc[b, h, sel] - L_ref[b, h, sel])
         assert lerr.max() <= lse_tol(w, None), lerr.max()
     assert np.isfinite(Lc).all() and np.isfinite(Oc).all()

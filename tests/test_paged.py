@@ -9,7 +9,7 @@ import torch
 
 from oracle import attention_forward
 from synth import make_workload
-from tests.helpers import DeviceRun, oracle_spec
+from tests.helpers import DeviceRun, check_bf16, oracle_spec
 
 pytestmark = pytest.mark.gpu
 
@@ -63,10 +63,7 @@ def test_paged_forward_matches_contiguous_and_oracle(name):
     torch.cuda.synchronize()
     assert torch.equal(o, O_ref_gpu) and torch.equal(lse, L_ref_gpu)
     O_ref, L_ref = attention_forward(w.q, w.k, w.v, oracle_spec(w))
-    err = np.abs(o.float().cpu().numpy() - O_ref)
-    a = np.abs(O_ref)
-    ulp = np.where(a > 0, 2.0 ** (np.floor(np.log2(np.maximum(a, 1e-30))) - 7), 0.0)
-    assert (err <= np.maximum(1e-2, 0.5 * ulp + 2e-3)).all()
+    check_bf16(o.float().cpu().numpy(), O_ref, f"paged O {name}")
 
 
 def test_paged_arguments_are_checked():

@@ -9,7 +9,7 @@ import torch
 
 from oracle import Spec, attention_backward, attention_forward
 from synth import make_workload
-from tests.helpers import DeviceRun
+from tests.helpers import DeviceRun, check_bf16
 
 LENGTHS = [100, 300, 57, 1, 400, 166]   # total 1024: several tiles, ragged seams
 
@@ -63,9 +63,7 @@ def test_packed_forward_equals_per_sequence(D):
     O_ref, L_ref = per_sequence(w, LENGTHS)
     O = O.float().cpu().numpy()
     L = L.cpu().numpy()
-    a = np.abs(O_ref)
-    ulp = np.where(a > 0, 2.0 ** (np.floor(np.log2(np.maximum(a, 1e-30))) - 7), 0.0)
-    assert (np.abs(O - O_ref) <= np.maximum(1e-2, 0.5 * ulp + 2e-3)).all()
+    check_bf16(O, O_ref, f"packed O D={D}")
     assert np.abs(L - L_ref).max() <= 2e-3
 
 
@@ -87,11 +85,8 @@ def test_packed_backward_equals_per_sequence():
     M.attn_bwd(g.q, g.k, g.v, O, L, g.do, dq, dk, dv, ws, g.variant, **g.kwargs())
     torch.cuda.synchronize()
     ref = per_sequence(w, lengths, backward=True)
-    for got, want in zip((dq, dk, dv), ref[:3]):
-        got = got.float().cpu().numpy()
-        a = np.abs(want)
-        ulp = np.where(a > 0, 2.0 ** (np.floor(np.log2(np.maximum(a, 1e-30))) - 7), 0.0)
-        assert (np.abs(got - want) <= 1e-2 + 0.5 * ulp).all()
+    for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv), ref[:3]):
+        check_bf16(got.float().cpu().numpy(), want, f"packed {name}")
 
 
 def test_doc_ids_from_seqlens_rejects_bad_arguments():
