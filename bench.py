@@ -574,7 +574,7 @@ def run_backward(args) -> None:
     import masked_attention_gb300 as M
     from synth import make_workload
 
-    w = make_workload(5)
+    w = make_workload(5, **({"B": args.batch} if args.batch else {}))
     dev = torch.device("cuda", 0)
     variant = variant_of(w, M)
     flops = 2.5 * 4.0 * w.D * kept_pairs(w) * w.Hq

@@ -86,8 +86,9 @@ struct BwdCfg {
   static constexpr int kOffSlots = 2 * kTileBytes;
   static constexpr int kOffBars = kOffSlots + kSlots * kSlotBytes;
   // fix_full, fix_empty, s_full, dp_full, p_full, ds_full, acc_done, acc_free,
-  // drain, dx_full, slot_full[kSlots], slot_empty[kSlots]
-  static constexpr int kNumBars = 10 + 2 * kSlots;
+  // drain, dx_full, then per slot and half (0: Q or K with the extras, 1: dO
+  // or V) full[2][kSlots] and empty[2][kSlots]
+  static constexpr int kNumBars = 10 + 4 * kSlots;
   // per-row partial sums of Delta of the two warpgroups, double-buffered
   static constexpr int kOffDx = (kOffBars + kNumBars * 8 + 15) & ~15;
   static constexpr int kOffMisc = kOffDx + 2 * 2 * kTile * 4;
@@ -225,8 +226,9 @@ __device__ __forceinline__ void tanh16(float (&y)[16]) {
 // hi + lo represents a and b to about 2^-17 of their magnitude.
 __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
   hi = pack_bf16x2(a, b);
-  const float ha = __uint_as_float(hi << 16), hb = __uint_as_float(hi & 0xffff0000u);
-  lo = pack_bf16x2(a - ha, b - hb);
+  const float2 h = make_float2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u));
+  const float2 r = ffma2(h, make_float2(-1.0f, -1.0f), make_float2(a, b));
+  lo = pack_bf16x2(r.x, r.y);
 }
 
 // TMEM column (within a 128-column S or dP block) of the 8 packed columns
@@ -236,25 +238,35 @@ __device__ __forceinline__ uint32_t hi_col(int kk) { return 64u * (kk >> 2) + 8u
 
 // D(tmem) += A(tmem, 8 K-steps at hi_col + extra) * B(smem, MN-major), K = 128.
 // b_desc: descriptor of the B tile's first row; K-step kk advances 16 rows =
-// 2048 bytes (the start-address field counts 16-byte units).
+// 2048 bytes (the start-address field counts 16-byte units). Called by the
+// whole (converged) MMA warp; lane 0 issues (mma_ts_warp).
 __device__ __forceinline__ void issue_ts(uint32_t d_tmem, uint32_t a_base, uint32_t extra,
                                          uint64_t b_desc, uint32_t idesc, bool accumulate) {
+  uint32_t a[8];
+  uint64_t b[8];
 #pragma unroll
-  for (int kk = 0; kk < kTile / 16; ++kk)
-    mma_bf16_ts(d_tmem, a_base + hi_col(kk) + extra, b_desc + (uint64_t)(kk * 128), idesc,
-                (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < 8; ++kk) {
+    a[kk] = a_base + hi_col(kk) + extra;
+    b[kk] = b_desc + (uint64_t)(kk * 128);
+  }
+  mma_ts_warp<8>(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
 }
 
 // D(tmem) = A(smem) * B(smem)^T over D (both K-major): K-step kk advances 32
 // bytes inside a 64-column box and moves to the next box every 4 steps.
+// Called by the whole MMA warp.
 template <int D>
 __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc) {
+  constexpr int K = D / 16;
+  uint64_t a[K], b[K];
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
+  for (int kk = 0; kk < K; ++kk) {
     const uint64_t off = (uint64_t)(((kk / 4) * kTile * 128 + (kk % 4) * 32) >> 4);
-    mma_bf16_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0);
+    a[kk] = a_desc + off;
+    b[kk] = b_desc + off;
   }
+  mma_ss_warp<K>(d_tmem, a, b, idesc, 0u);
 }
 
 template <int D, int SCORE, int MODE>
@@ -280,8 +292,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_free = bars + 7;
   uint64_t* drain = bars + 8;
   uint64_t* dx_full = bars + 9;
-  uint64_t* slot_full = bars + 10;
-  uint64_t* slot_empty = bars + 10 + C::kSlots;
+  // A slot's two halves are filled and released separately: the second
+  // (dO for dKV, V for dQ) is free once dV, or dP, has read it, well before
+  // the first, so its next load starts early. full0/empty0: first half.
+  uint64_t* slot_full0 = bars + 10;
+  uint64_t* slot_full1 = bars + 10 + C::kSlots;
+  uint64_t* slot_empty0 = bars + 10 + 2 * C::kSlots;
+  uint64_t* slot_empty1 = bars + 10 + 3 * C::kSlots;
   float* sdx = reinterpret_cast<float*>(smem + C::kOffDx);  // [2 units][2 groups][128 rows]
   uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -302,8 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     mbar_init(dx_full, kComputeWarps);
     for (int s = 0; s < C::kSlots; ++s) {
-      mbar_init(slot_full + s, 1);
-      mbar_init(slot_empty + s, 1);
+      mbar_init(slot_full0 + s, 1);
+      mbar_init(slot_full1 + s, 1);
+      mbar_init(slot_empty0 + s, 1);
+      mbar_init(slot_empty1 + s, 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -335,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // With ATTN_FAULT_NO_LOADS nothing is issued and the consumers' waits run out.
     const bool leader = lane == 0 && !(p.fault_inject & ATTN_FAULT_NO_LOADS);
     uint32_t slot_it = 0, fix_it = 0;
-    bool ok = true;
+    bool ok = true, pending1 = false;  // pending1: tile slot_it's second half issued alone
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
       const BUnit U = decode_bwd<MODE>(a, u);
       const int n = U.n();
@@ -363,55 +382,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         U.at(it, hoff, t, partial);
         t += first;
         const int slot = slot_it % C::kSlots;
-        ok = __all_sync(0xffffffffu,
-                        wait_bounded(slot_empty + slot, ((slot_it / C::kSlots) & 1) ^ 1, wd));
-        if (!ok) break;
+        const uint32_t ph = ((slot_it / C::kSlots) & 1) ^ 1;
         uint8_t* base = sSlots + slot * C::kSlotBytes;
-        uint32_t bytes = 2 * C::kTileBytes;
+        // second half first: it is released earlier
+        ok = __all_sync(0xffffffffu, wait_bounded(slot_empty1 + slot, ph, wd));
+        if (!ok) break;
+        if (leader) {
+          mbar_arrive_expect_tx(slot_full1 + slot, C::kTileBytes);
+          if (MODE == kDQ) {  // V rows of (b, hk, t)
+            const int row = (U.b * p.Hkv + U.h / group) * p.Skv + t * kTile;
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+              tma_load_2d(base + C::kTileBytes + bx * C::kBoxBytes, &tm_v, slot_full1 + slot,
+                          bx * 64, row);
+          } else {            // dO rows of (b, h, t)
+            const int h = U.h * group + hoff;
+            const int qrow = (U.b * p.Hq + h) * p.Sq + t * kTile;
+            for (int bx = 0; bx < C::kBoxes; ++bx)
+              tma_load_2d(base + C::kTileBytes + bx * C::kBoxBytes, &tm_do, slot_full1 + slot,
+                          bx * 64, qrow);
+          }
+        }
+        __syncwarp();
+        pending1 = true;
+        ok = __all_sync(0xffffffffu, wait_bounded(slot_empty0 + slot, ph, wd));
+        if (!ok) break;
+        uint32_t bytes = C::kTileBytes;
         if (has_doc) bytes += 512;
         if (MODE == kDKV) bytes += 1024;
-        if (leader) mbar_arrive_expect_tx(slot_full + slot, bytes);
-        if (leader && MODE == kDQ) {
+        if (leader) mbar_arrive_expect_tx(slot_full0 + slot, bytes);
+        if (leader && MODE == kDQ) {  // K rows and the keys' document ids
           const int row = (U.b * p.Hkv + U.h / group) * p.Skv + t * kTile;
-          for (int bx = 0; bx < C::kBoxes; ++bx) {
-            tma_load_2d(base + bx * C::kBoxBytes, &tm_k, slot_full + slot, bx * 64, row);
-            tma_load_2d(base + C::kTileBytes + bx * C::kBoxBytes, &tm_v, slot_full + slot,
-                        bx * 64, row);
-          }
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_2d(base + bx * C::kBoxBytes, &tm_k, slot_full0 + slot, bx * 64, row);
           if (has_doc)
             bulk_load(base + 2 * C::kTileBytes,
                       p.mask.doc_id + (size_t)U.b * p.mask.doc_len + t * kTile, 512,
-                      slot_full + slot);
-        } else if (leader) {
+                      slot_full0 + slot);
+        } else if (leader) {  // Q rows and the queries' document ids, LSE and Delta
           const int h = U.h * group + hoff;
           const size_t qrow = (size_t)(U.b * p.Hq + h) * p.Sq + t * kTile;
-          for (int bx = 0; bx < C::kBoxes; ++bx) {
-            tma_load_2d(base + bx * C::kBoxBytes, &tm_q, slot_full + slot, bx * 64, (int)qrow);
-            tma_load_2d(base + C::kTileBytes + bx * C::kBoxBytes, &tm_do, slot_full + slot,
-                        bx * 64, (int)qrow);
-          }
+          for (int bx = 0; bx < C::kBoxes; ++bx)
+            tma_load_2d(base + bx * C::kBoxBytes, &tm_q, slot_full0 + slot, bx * 64, (int)qrow);
           if (has_doc)
             bulk_load(base + 2 * C::kTileBytes,
                       p.mask.doc_id + (size_t)U.b * p.mask.doc_len + t * kTile, 512,
-                      slot_full + slot);
-          bulk_load(base + 2 * C::kTileBytes + 512, p.lse + qrow, 512, slot_full + slot);
-          bulk_load(base + 2 * C::kTileBytes + 1024, a.delta + qrow, 512, slot_full + slot);
+                      slot_full0 + slot);
+          bulk_load(base + 2 * C::kTileBytes + 512, p.lse + qrow, 512, slot_full0 + slot);
+          bulk_load(base + 2 * C::kTileBytes + 1024, a.delta + qrow, 512, slot_full0 + slot);
         }
         __syncwarp();
         ++slot_it;
+        pending1 = false;
       }
     }
     if (!ok && !(p.fault_inject & ATTN_FAULT_NO_LOADS)) {  // let copies in flight land
-      for (uint32_t k = 0; k < C::kSlots && k < slot_it; ++k) {
-        const uint32_t it = slot_it - 1 - k;
-        wait_drain(slot_full + it % C::kSlots, (it / C::kSlots) & 1);
+      // (slot_it counts tiles whose loads were all issued; the tile after
+      // them may have its second half in flight)
+      if (pending1) wait_drain(slot_full1 + slot_it % C::kSlots, (slot_it / C::kSlots) & 1);
+      for (uint32_t k = 1; k <= C::kSlots && k <= slot_it; ++k) {
+        const uint32_t it = slot_it - k;
+        wait_drain(slot_full0 + it % C::kSlots, (it / C::kSlots) & 1);
+        wait_drain(slot_full1 + it % C::kSlots, (it / C::kSlots) & 1);
       }
       if (fix_it > 0) wait_drain(fix_full, (fix_it - 1) & 1);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the loop (waits stay converged); lane 0 issues.
-    const bool leader = lane == 0;
+    // The whole warp runs the loop (waits stay converged) and issues each
+    // product as one block (issue_ss, issue_ts); lane 0 issues.
     constexpr uint32_t kIdescSS = idesc_bf16(128, 128, false);
     constexpr uint32_t kIdescTS = idesc_bf16(128, D, true);
     // shared-memory descriptors: K-major (SS operands) and MN-major (B of the
@@ -430,16 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // S = fix0 . slot0^T into S, dP = fix1 . slot1^T into dP
     auto issue_s = [&](uint32_t seq) {
-      if (leader) {
-        issue_ss<D>(colS, dFixK, dSlotK + slot_off(seq), kIdescSS);
-        mma_commit(s_full);
-      }
+      issue_ss<D>(colS, dFixK, dSlotK + slot_off(seq), kIdescSS);
+      mma_commit_warp(s_full);
     };
     auto issue_dp = [&](uint32_t seq) {
-      if (leader) {
-        issue_ss<D>(colP, dFixK + kTileOff, dSlotK + slot_off(seq) + kTileOff, kIdescSS);
-        mma_commit(dp_full);
-      }
+      issue_ss<D>(colP, dFixK + kTileOff, dSlotK + slot_off(seq) + kTileOff, kIdescSS);
+      mma_commit_warp(dp_full);
     };
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
       const BUnit U = decode_bwd<MODE>(a, u);
@@ -448,13 +482,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, wait_bounded(fix_full, fix_it & 1, wd));
       if (!ok) break;
       ++fix_it;
-      ok = __all_sync(0xffffffffu, wait_bounded(slot_full + slot_it % C::kSlots,
+      ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + slot_it % C::kSlots,
                                                 (slot_it / C::kSlots) & 1, wd));
       if (!ok) break;
       tc_fence_after();
       issue_s(slot_it);
+      ok = __all_sync(0xffffffffu, wait_bounded(slot_full1 + slot_it % C::kSlots,
+                                                (slot_it / C::kSlots) & 1, wd));
+      if (!ok) break;
+      tc_fence_after();
       issue_dp(slot_it);
-      if (n == 1 && leader) mma_commit(fix_empty);  // the fixed tiles are read by S and dP only
+      if (MODE == kDQ) mma_commit_warp(slot_empty1 + slot_it % C::kSlots);  // V read
+      if (n == 1) mma_commit_warp(fix_empty);  // the fixed tiles are read by S and dP only
       __syncwarp();
       for (int it = 0; it < n && ok; ++it) {
         const uint32_t seq = slot_it + it;
@@ -471,24 +510,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           ++p_it;
           tc_fence_after();
-          if (leader) {
-            issue_ts(acc0, colS, 0, s1, kIdescTS, acc);
-            issue_ts(acc0, colS, 32, s1, kIdescTS, true);
-          }
+          issue_ts(acc0, colS, 0, s1, kIdescTS, acc);
+          issue_ts(acc0, colS, 32, s1, kIdescTS, true);
+          mma_commit_warp(slot_empty1 + seq % C::kSlots);  // dO read
         } else {
           // B += (P g) K and A += lo K (operands over S)
           ok = __all_sync(0xffffffffu, wait_bounded(ds_full, ds_it & 1, wd));
           if (!ok) break;
           ++ds_it;
           tc_fence_after();
-          if (leader) {
-            issue_ts(acc1, colS, 0, s0, kIdescTS, acc);
-            issue_ts(acc0, colS, 32, s0, kIdescTS, acc);
-          }
+          issue_ts(acc1, colS, 0, s0, kIdescTS, acc);
+          issue_ts(acc0, colS, 32, s0, kIdescTS, acc);
         }
         __syncwarp();
         if (it + 1 < n) {  // S of the next tile (its P/lo operands over S are consumed)
-          ok = __all_sync(0xffffffffu, wait_bounded(slot_full + (seq + 1) % C::kSlots,
+          ok = __all_sync(0xffffffffu, wait_bounded(slot_full0 + (seq + 1) % C::kSlots,
                                                     ((seq + 1) / C::kSlots) & 1, wd));
           if (!ok) break;
           tc_fence_after();
@@ -501,29 +537,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           ++ds_it;
           tc_fence_after();
-          if (leader) {
-            issue_ts(acc1, colP, 0, s0, kIdescTS, acc);
-            issue_ts(acc1, colP, 32, s0, kIdescTS, true);
-          }
+          issue_ts(acc1, colP, 0, s0, kIdescTS, acc);
+          issue_ts(acc1, colP, 32, s0, kIdescTS, true);
         } else {
           // A += hi K (operand over dP)
-          if (leader) issue_ts(acc0, colP, 0, s0, kIdescTS, true);
+          issue_ts(acc0, colP, 0, s0, kIdescTS, true);
         }
-        if (leader) mma_commit(slot_empty + seq % C::kSlots);
+        mma_commit_warp(slot_empty0 + seq % C::kSlots);  // Q or K read
         __syncwarp();
         if (it + 1 < n) {  // dP of the next tile (the operands over dP are consumed)
+          ok = __all_sync(0xffffffffu, wait_bounded(slot_full1 + (seq + 1) % C::kSlots,
+                                                    ((seq + 1) / C::kSlots) & 1, wd));
+          if (!ok) break;
+          tc_fence_after();
           issue_dp(seq + 1);
-          if (it + 2 == n && leader) mma_commit(fix_empty);
+          if (MODE == kDQ) mma_commit_warp(slot_empty1 + (seq + 1) % C::kSlots);  // V read
+          if (it + 2 == n) mma_commit_warp(fix_empty);
           __syncwarp();
         }
       }
       if (!ok) break;
       ++acc_it;
-      if (leader) mma_commit(acc_done);
+      mma_commit_warp(acc_done);
       __syncwarp();
       slot_it += n;
     }
-    if (leader) mma_commit(drain);
+    mma_commit_warp(drain);
     __syncwarp();
     wait_drain(drain, 0);
   } else if (warp < kComputeWarps) {
@@ -585,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* sdel = reinterpret_cast<const float*>(base + 2 * C::kTileBytes + 1024) + 64 * g;
         // the slot's shared-memory extras (doc ids, LSE, Delta) are read directly
         ok = __all_sync(0xffffffffu,
-                        wait_bounded(slot_full + seq % C::kSlots, (seq / C::kSlots) & 1, wd));
+                        wait_bounded(slot_full0 + seq % C::kSlots, (seq / C::kSlots) & 1, wd));
         if (!ok) break;
         ok = __all_sync(0xffffffffu, wait_bounded(s_full, s_it & 1, wd));
         if (!ok) break;
@@ -605,10 +644,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (P != INT_MIN && r < P) pre = INT_MAX;
           }
         }
-        // (j - i) = base_ji + sgn * c
+        // (j - i) = base_ji + sgn * c for the column c of this warpgroup's 64
         const int base_ji = MODE == kDQ ? c0 - r : r - c0;
         const float sgn = MODE == kDQ ? 1.0f : -1.0f;
-        // P (and P g) from S, 16 columns at a time; v keeps P g for dS
+        // P (and P g) from S, 16 columns at a time, two columns per packed
+        // instruction; v keeps P g for dS. An empty row (LSE = -inf) occurs
+        // only in partial tiles, where the mask zeroes all of it, so LSE needs
+        // no special case here.
         constexpr bool kKeepP = MODE == kDQ && (SCORE & 2) != 0;  // Delta needs P itself
         float v[64];
         float pf[kKeepP ? 64 : 1];
@@ -621,56 +663,91 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 64; ++e) v[e] = __uint_as_float(rr[e]);
         }
+        // ALiBi in log2 units: slope2 (base_ji + sgn c) = a0 + a1 c
+        const float slope2 = slope * kLog2e;
+        const float a0 = slope2 * float(base_ji), a1 = slope2 * sgn;
+        const float sl2 = scale * kLog2e;
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {  // 32 columns: 16 packed TMEM columns per part
           uint32_t hi16[16], lo16[16];
 #pragma unroll
           for (int q2 = 0; q2 < 2; ++q2) {
             const int q = 2 * h2 + q2;
-            float x[16], gg[16];
+            // minus the LSE of each column in log2 units (dKV: the column's
+            // own row of the stream; dQ: this thread's row)
+            float2 nl[8];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int c = 16 * q + e;
-              x[e] = v[c] * scale;
-              if constexpr ((SCORE & 1) != 0)
-                x[e] = fmaf(slope, float(base_ji) + sgn * float(c), x[e]);
-              gg[e] = 1.0f;
+            for (int e = 0; e < 8; e += 2) {
+              if constexpr (MODE == kDKV) {
+                const float4 l4 = *reinterpret_cast<const float4*>(slse + 16 * q + 2 * e);
+                const float2 m2 = make_float2(-kLog2e, -kLog2e);
+                nl[e] = fmul2(make_float2(l4.x, l4.y), m2);
+                nl[e + 1] = fmul2(make_float2(l4.z, l4.w), m2);
+              } else {
+                nl[e] = nl[e + 1] = make_float2(-row_lse2, -row_lse2);
+              }
+            }
+            float2 pr[8], gg[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int c = 16 * q + 2 * e;
+              const float2 sv = make_float2(v[c], v[c + 1]);
+              float2 arg;
+              if constexpr ((SCORE & 2) == 0) {
+                // log2-unit score: s sl2 (+ ALiBi) - LSE2, one packed FMA each
+                float2 bias = nl[e];
+                if constexpr ((SCORE & 1) != 0)
+                  bias = ffma2(make_float2(a1, a1), make_float2(float(c), float(c + 1)),
+                               fadd2(bias, make_float2(a0, a0)));
+                arg = ffma2(sv, make_float2(sl2, sl2), bias);
+                gg[e] = make_float2(1.0f, 1.0f);
+              } else {
+                float2 x = fmul2(sv, make_float2(scale, scale));
+                if constexpr ((SCORE & 1) != 0)
+                  x = ffma2(make_float2(slope * sgn, slope * sgn),
+                            make_float2(float(c), float(c + 1)),
+                            fadd2(x, make_float2(slope * float(base_ji), slope * float(base_ji))));
+                pr[e] = fmul2(x, make_float2(inv_cap, inv_cap));  // tanh argument
+              }
+              if constexpr ((SCORE & 2) == 0) pr[e] = arg;
             }
             if constexpr ((SCORE & 2) != 0) {
               float th[16];
 #pragma unroll
-              for (int e = 0; e < 16; ++e) th[e] = x[e] * inv_cap;
+              for (int e = 0; e < 8; ++e) th[2 * e] = pr[e].x, th[2 * e + 1] = pr[e].y;
               tanh16(th);
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                x[e] = cap * th[e];
-                gg[e] = fmaf(-th[e], th[e], 1.0f);
+              for (int e = 0; e < 8; ++e) {
+                const float2 t2 = make_float2(th[2 * e], th[2 * e + 1]);
+                gg[e] = ffma2(fmul2(t2, make_float2(-1.0f, -1.0f)), t2, make_float2(1.0f, 1.0f));
+                // cap tanh in log2 units minus LSE2
+                pr[e] = ffma2(t2, make_float2(cap * kLog2e, cap * kLog2e), nl[e]);
               }
             }
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int c = 16 * q + e;
-              float lse2 = row_lse2;
-              if constexpr (MODE == kDKV)
-                lse2 = slse[c] == -INFINITY ? INFINITY : slse[c] * kLog2e;
-              float pr = ex2_approx(fmaf(x[e], kLog2e, -lse2));
+            for (int e = 0; e < 8; ++e) {
+              const int c = 16 * q + 2 * e;
+              float p0 = ex2_approx(pr[e].x), p1 = ex2_approx(pr[e].y);
               if (partial) {
                 // bitwise terms, document id read on a warp-uniform condition:
                 // no divergent branch per element
-                const bool same = docb ? (sdoc[c] == my_doc) : true;
-                const bool keep = ((c >= lo) & (c < hi) & same) | (c < pre);
-                pr = keep ? pr : 0.0f;
+                const bool same0 = docb ? (sdoc[c] == my_doc) : true;
+                const bool same1 = docb ? (sdoc[c + 1] == my_doc) : true;
+                const bool keep0 = ((c >= lo) & (c < hi) & same0) | (c < pre);
+                const bool keep1 = ((c + 1 >= lo) & (c + 1 < hi) & same1) | (c + 1 < pre);
+                p0 = keep0 ? p0 : 0.0f;
+                p1 = keep1 ? p1 : 0.0f;
               }
-              x[e] = pr;
-              v[c] = pr * gg[e];
-              if constexpr (kKeepP) pf[c] = pr;
-            }
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
+              const float2 p2 = make_float2(p0, p1);
+              float2 vg = p2;
+              if constexpr ((SCORE & 2) != 0) vg = fmul2(p2, gg[e]);
+              v[c] = vg.x;
+              v[c + 1] = vg.y;
+              if constexpr (kKeepP) pf[c] = p0, pf[c + 1] = p1;
               if constexpr (MODE == kDKV)  // P^T, split, for dV += P^T dO
-                split_bf16x2(x[e], x[e + 1], hi16[8 * q2 + e / 2], lo16[8 * q2 + e / 2]);
+                split_bf16x2(p0, p1, hi16[8 * q2 + e], lo16[8 * q2 + e]);
               else  // P g in bf16, for B += (P g) K
-                hi16[8 * q2 + e / 2] = pack_bf16x2(v[16 * q + e], v[16 * q + e + 1]);
+                hi16[8 * q2 + e] = pack_bf16x2(vg.x, vg.y);
             }
           }
           tmem_st16(colS + 16 * h2, hi16);
@@ -697,27 +774,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(colP + 32 * hh, rr);
           tmem_ld_wait_regs(rr);
           uint32_t dh[16], dl[16];
+          float2 dacc = make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
+          for (int e = 0; e < 32; e += 4) {
             const int c = 32 * hh + e;
-            const float dp0 = __uint_as_float(rr[e]), dp1 = __uint_as_float(rr[e + 1]);
-            float ds0, ds1;
-            if constexpr (MODE == kDKV) {
-              ds0 = v[c] * (dp0 - sdel[c]);
-              ds1 = v[c + 1] * (dp1 - sdel[c + 1]);
-            } else {
-              ds0 = v[c] * (dp0 - row_dhat);
-              ds1 = v[c + 1] * (dp1 - row_dhat);
-              if constexpr (kKeepP) {
-                row_delta = fmaf(pf[c], dp0, row_delta);
-                row_delta = fmaf(pf[c + 1], dp1, row_delta);
-              } else {  // identity or ALiBi score_mod: P g = P
-                row_delta = fmaf(v[c], dp0, row_delta);
-                row_delta = fmaf(v[c + 1], dp1, row_delta);
+            float4 d4;
+            if constexpr (MODE == kDKV) d4 = *reinterpret_cast<const float4*>(sdel + c);
+            else d4 = make_float4(row_dhat, row_dhat, row_dhat, row_dhat);
+#pragma unroll
+            for (int z = 0; z < 2; ++z) {
+              const float2 dp = make_float2(__uint_as_float(rr[e + 2 * z]),
+                                            __uint_as_float(rr[e + 2 * z + 1]));
+              const float2 dl2 = z ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
+              const float2 vv = make_float2(v[c + 2 * z], v[c + 2 * z + 1]);
+              // dKV: dS = P g (dP - Delta);  dQ: P g (dP - Dhat)
+              const float2 ds = fmul2(vv, ffma2(dl2, make_float2(-1.0f, -1.0f), dp));
+              if constexpr (MODE == kDQ) {  // Delta += P dP
+                if constexpr (kKeepP)
+                  dacc = ffma2(make_float2(pf[c + 2 * z], pf[c + 2 * z + 1]), dp, dacc);
+                else  // identity or ALiBi score_mod: P g = P
+                  dacc = ffma2(vv, dp, dacc);
               }
+              split_bf16x2(ds.x, ds.y, dh[e / 2 + z], dl[e / 2 + z]);
             }
-            split_bf16x2(ds0, ds1, dh[e / 2], dl[e / 2]);
           }
+          if constexpr (MODE == kDQ) row_delta += dacc.x + dacc.y;
           tmem_st16(colP + 16 * hh, dh);
           if constexpr (MODE == kDKV) {
             if (hh == 0) {

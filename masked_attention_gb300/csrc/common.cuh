@@ -282,6 +282,82 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
+// Products issued by a whole, converged warp: lane 0 issues all K-steps of
+// one product in a single block, the other lanes skip them by predicate.
+// On this GPU the tensor pipe then accepts M128 N128 K16 products at its
+// full rate (64 cycles each); issued one at a time from a divergent single
+// thread, each product costs about 3.5 times that. `first` is the enable
+// input of the first K-step (0: overwrite D); the others accumulate.
+template <int K>
+__device__ __forceinline__ void mma_ss_warp(uint32_t d, const uint64_t (&a)[K],
+                                            const uint64_t (&b)[K], uint32_t idesc,
+                                            uint32_t first) {
+  static_assert(K == 4 || K == 8, "4 or 8 K-steps");
+  if constexpr (K == 8) {
+    asm volatile(
+      "{\n\t.reg .pred pl, pa, pt;\n\t.reg .b32 ln;\n\t"
+      "mov.u32 ln, %laneid;\n\t"
+      "setp.eq.u32 pl, ln, 0;\n\t"
+      "setp.ne.b32 pa, %2, 0;\n\t"
+      "setp.eq.b32 pt, 0, 0;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %1, pa;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %1, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %1, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %1, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], %11, %12, %1, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], %13, %14, %1, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], %15, %16, %1, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], %17, %18, %1, pt;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(first), "l"(a[0]), "l"(b[0]), "l"(a[1]), "l"(b[1]), "l"(a[2]), "l"(b[2]), "l"(a[3]), "l"(b[3]), "l"(a[4]), "l"(b[4]), "l"(a[5]), "l"(b[5]), "l"(a[6]), "l"(b[6]), "l"(a[7]), "l"(b[7]));
+  } else {
+    asm volatile(
+      "{\n\t.reg .pred pl, pa, pt;\n\t.reg .b32 ln;\n\t"
+      "mov.u32 ln, %laneid;\n\t"
+      "setp.eq.u32 pl, ln, 0;\n\t"
+      "setp.ne.b32 pa, %2, 0;\n\t"
+      "setp.eq.b32 pt, 0, 0;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %4, %1, pa;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %1, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %1, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %1, pt;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(first), "l"(a[0]), "l"(b[0]), "l"(a[1]), "l"(b[1]), "l"(a[2]), "l"(b[2]), "l"(a[3]), "l"(b[3]));
+  }
+}
+
+// The same with A read from tensor memory (a[k]: TMEM address of K-step k).
+template <int K>
+__device__ __forceinline__ void mma_ts_warp(uint32_t d, const uint32_t (&a)[K],
+                                            const uint64_t (&b)[K], uint32_t idesc,
+                                            uint32_t first) {
+  static_assert(K == 8, "8 K-steps");
+  asm volatile(
+      "{\n\t.reg .pred pl, pa, pt;\n\t.reg .b32 ln;\n\t"
+      "mov.u32 ln, %laneid;\n\t"
+      "setp.eq.u32 pl, ln, 0;\n\t"
+      "setp.ne.b32 pa, %2, 0;\n\t"
+      "setp.eq.b32 pt, 0, 0;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %4, %1, pa;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %1, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %1, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %1, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [%11], %12, %1, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [%13], %14, %1, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [%15], %16, %1, pt;\n\t"
+      "@pl tcgen05.mma.cta_group::1.kind::f16 [%0], [%17], %18, %1, pt;\n\t"
+      "}" ::"r"(d), "r"(idesc), "r"(first), "r"(a[0]), "l"(b[0]), "r"(a[1]), "l"(b[1]), "r"(a[2]), "l"(b[2]), "r"(a[3]), "l"(b[3]), "r"(a[4]), "l"(b[4]), "r"(a[5]), "l"(b[5]), "r"(a[6]), "l"(b[6]), "r"(a[7]), "l"(b[7]));
+}
+
+// tcgen05.commit from a converged warp (issued by lane 0, the lane that
+// issued the products it tracks).
+__device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred pl;\n\t.reg .b32 ln;\n\t"
+      "mov.u32 ln, %laneid;\n\t"
+      "setp.eq.u32 pl, ln, 0;\n\t"
+      "@pl tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_u32(bar)));
+}
+
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(

@@ -237,25 +237,34 @@ __device__ __forceinline__ bool wait_warp(uint64_t* bar, uint32_t parity, const 
 
 // S = Q K^T over D (K-major operands, 128-byte swizzle): K-step kk advances
 // 32 bytes inside a 64-column box and moves to the next box every 4 steps.
+// Called by the whole (converged) MMA warp; lane 0 issues (mma_ss_warp).
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc) {
+  constexpr int K = D / 16;
+  uint64_t a[K], b[K];
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
+  for (int kk = 0; kk < K; ++kk) {
     const uint64_t off = (uint64_t)(((kk / 4) * kTile * 128 + (kk % 4) * 32) >> 4);
-    mma_bf16_ss(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0);
+    a[kk] = a_desc + off;
+    b[kk] = b_desc + off;
   }
+  mma_ss_warp<K>(d_tmem, a, b, idesc, 0u);
 }
 
 // O += P V: P (bf16, 8 TMEM columns per 16 keys) times V (MN-major); K-step kk
-// advances 16 key rows = 2048 bytes.
+// advances 16 key rows = 2048 bytes. Called by the whole MMA warp.
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t b_desc,
                                          uint32_t idesc, bool accumulate) {
+  uint32_t a[8];
+  uint64_t b[8];
 #pragma unroll
-  for (int kk = 0; kk < kTile / 16; ++kk)
-    mma_bf16_ts(d_tmem, p_tmem + kk * 8, b_desc + (uint64_t)((kk * 16 * 128) >> 4), idesc,
-                (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < 8; ++kk) {
+    a[kk] = p_tmem + kk * 8;
+    b[kk] = b_desc + (uint64_t)((kk * 16 * 128) >> 4);
+  }
+  mma_ts_warp<8>(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
 }
 
 // Loads n32 x 32 columns of this thread's TMEM lane into s (one wait for all).
@@ -548,10 +557,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma || (C::kDualMma && warp == kWarpMma2)) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop (waits stay converged); lane 0 issues the
-    // products and the commits. Loop state stays in registers and the
+    // products and the commits, each product's K-steps as one block
+    // (mma_ss_warp, mma_ts_warp). Loop state stays in registers and the
     // shared-memory descriptors are precomputed: the start-address field is
     // in 16-byte units, so an offset is added as (bytes >> 4).
-    const bool leader = lane == 0;
     constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false);
     constexpr uint32_t kIdescPV = idesc_bf16(128, D, true);
     const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);
@@ -582,15 +591,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
           }
-          if (leader) {
-            issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
-                        dK0 + ((slot * C::kTileBytes) >> 4), kIdescQK);
-            mma_commit(s_full + x);
-            if (!shared || x == nx - 1) mma_commit(slot_empty + slot);
-          }
+          issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
+                      dK0 + ((slot * C::kTileBytes) >> 4), kIdescQK);
+          mma_commit_warp(s_full + x);
+          if (!shared || x == nx - 1) mma_commit_warp(slot_empty + slot);
           __syncwarp();
         }
-        if (ok && n == 1 && leader) mma_commit(q_empty);
+        if (ok && n == 1) mma_commit_warp(q_empty);
         for (int j = 0; j < n && ok; ++j) {
           for (int x = 0; x < nx && ok; ++x) {
             // O_x += P_x V_j
@@ -609,11 +616,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!ok) break;
             }
             tc_fence_after();
-            if (leader) {
-              issue_pv<D>(tmem + C::kColO0 + D * x, tmem + 128u * x,
-                          dV0 + ((vslot * C::kTileBytes) >> 4), kIdescPV, j > 0);
-              if (!shared || x == nx - 1) mma_commit(slot_empty + vslot);
-            }
+            issue_pv<D>(tmem + C::kColO0 + D * x, tmem + 128u * x,
+                        dV0 + ((vslot * C::kTileBytes) >> 4), kIdescPV, j > 0);
+            if (!shared || x == nx - 1) mma_commit_warp(slot_empty + vslot);
             __syncwarp();
             if (j + 1 < n) {  // S_x(j+1)
               const uint32_t kseq = slot_it + (j + 1) * T + (shared ? 0u : (uint32_t)x);
@@ -623,18 +628,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
               }
-              if (leader) {
-                issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
-                            dK0 + ((kslot * C::kTileBytes) >> 4), kIdescQK);
-                mma_commit(s_full + x);
-                if (!shared || x == nx - 1) mma_commit(slot_empty + kslot);
-              }
+              issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
+                          dK0 + ((kslot * C::kTileBytes) >> 4), kIdescQK);
+              mma_commit_warp(s_full + x);
+              if (!shared || x == nx - 1) mma_commit_warp(slot_empty + kslot);
               __syncwarp();
-            } else if (leader) {
-              mma_commit(o_done + x);
+            } else {
+              mma_commit_warp(o_done + x);
             }
           }
-          if (ok && j + 1 == n - 1 && leader) mma_commit(q_empty);
+          if (ok && j + 1 == n - 1) mma_commit_warp(q_empty);
         }
         __syncwarp();
         slot_it += n * T;
@@ -676,16 +679,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t kslot = kseq % C::kSlots;
           if (!wait_warp(slot_full + kslot, (kseq / C::kSlots) & 1, wd)) return false;
           tc_fence_after();
-          if (leader) {
-            issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
-                        dK0 + ((kslot * C::kTileBytes) >> 4), kIdescQK);
-            mma_commit(s_full + x);
-            mma_commit(slot_empty + kslot);
-            if (!both) mma_commit(slot_empty + kslot);
-            if (jj + 1 == n) {  // the unit's last Q.K^T for this head
-              mma_commit(q_empty);
-              if (nx == 1) mma_commit(q_empty);
-            }
+          issue_qk<D>(tmem + 128u * x, dQ0 + ((x * C::kTileBytes) >> 4),
+                      dK0 + ((kslot * C::kTileBytes) >> 4), kIdescQK);
+          mma_commit_warp(s_full + x);
+          mma_commit_warp(slot_empty + kslot);
+          if (!both) mma_commit_warp(slot_empty + kslot);
+          if (jj + 1 == n) {  // the unit's last Q.K^T for this head
+            mma_commit_warp(q_empty);
+            if (nx == 1) mma_commit_warp(q_empty);
           }
           __syncwarp();
           ++kq;
@@ -702,15 +703,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t vslot = vseq % C::kSlots;
           if (!wait_warp(slot_full + vslot, (vseq / C::kSlots) & 1, wd)) return false;
           tc_fence_after();
-          if (leader) {
-            const uint32_t pcol = C::kSepP ? C::kColP + 64u * x : 128u * x;
-            issue_pv<D>(tmem + C::kColO0 + D * x, tmem + pcol,
-                        dV0 + ((vslot * C::kTileBytes) >> 4), kIdescPV, jj > 0);
-            if (C::kSepP) mma_commit(pv_done + x);
-            mma_commit(slot_empty + vslot);
-            if (!both) mma_commit(slot_empty + vslot);
-            if (jj + 1 == n) mma_commit(o_done + x);
-          }
+          const uint32_t pcol = C::kSepP ? C::kColP + 64u * x : 128u * x;
+          issue_pv<D>(tmem + C::kColO0 + D * x, tmem + pcol,
+                      dV0 + ((vslot * C::kTileBytes) >> 4), kIdescPV, jj > 0);
+          if (C::kSepP) mma_commit_warp(pv_done + x);
+          mma_commit_warp(slot_empty + vslot);
+          if (!both) mma_commit_warp(slot_empty + vslot);
+          if (jj + 1 == n) mma_commit_warp(o_done + x);
           __syncwarp();
           ++kp;
           return true;
@@ -732,13 +731,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // all products issued by this warp are complete before TMEM is freed
       uint64_t* dr = x ? drain2 : drain;
-      if (leader) mma_commit(dr);
+      mma_commit_warp(dr);
       __syncwarp();
       wait_drain(dr, 0);
     }
     if constexpr (!C::kDualMma) {
       // all products issued by this warp are complete before TMEM is freed
-      if (leader) mma_commit(drain);
+      mma_commit_warp(drain);
       __syncwarp();
       wait_drain(drain, 0);
     }

@@ -21,6 +21,7 @@ workspace. These tests call it through the C ABI and check:
 This file is named so that pytest collects it last.
 """
 import ctypes
+import gc
 
 import pytest
 
@@ -63,11 +64,19 @@ def test_noalloc_backward_equals_workspace_backward_twice():
     for g, O, L, ref, got in prepared:  # two calls in a row
         for t in got:
             t.fill_(float("nan"))
+        kw = g.kwargs()
         torch.cuda.synchronize()
-        free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
-        M.attn_bwd_noalloc(g.q, g.k, g.v, O, L, g.do, *got, g.variant, **g.kwargs())
-        torch.cuda.synchronize()
-        free1, alloc1 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+        # the garbage collector would free earlier tests' tensors at random
+        # points and move torch's allocated bytes: off around the measured call
+        gc.collect()
+        gc.disable()
+        try:
+            free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+            M.attn_bwd_noalloc(g.q, g.k, g.v, O, L, g.do, *got, g.variant, **kw)
+            torch.cuda.synchronize()
+            free1, alloc1 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+        finally:
+            gc.enable()
         assert M.attn_check_status() == M.ATTN_OK
         assert free1 == free0 and alloc1 == alloc0, (free0, free1, alloc0, alloc1)
         for name, a, b in zip(("dq", "dk", "dv"), got, ref):
