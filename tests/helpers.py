@@ -78,10 +78,11 @@ class DeviceRun:
         import torch
         w = self.w
         if o is None:
-            o = torch.empty_like(self.q)
+            o = guarded_like(self.q)
         if lse is None:
-            lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device="cuda")
+            lse = guarded_empty((w.B, w.Hq, w.Sq), torch.float32)
         self.M.attn_fwd(self.q, self.k, self.v, o, lse, self.variant, **self.kwargs())
+        check_canaries()
         return o, lse
 
 
@@ -128,3 +129,46 @@ def check_bf16(got, ref, what="", valid=None, tol=BF16_ABS_TOL) -> dict:
     assert not bad.any(), (what, float(err[bad].max()), int(bad.sum()))
     assert n_exempt <= cap, (what, n_exempt, cap)
     return stats
+
+
+# Guard canaries: an output tensor lives inside a larger buffer whose bytes
+# before and after it hold a sentinel; after the kernel ran, both guard
+# regions must still hold it (a write past either end of the output would
+# change them). Guards are 4 KiB, which keeps the output 16-byte aligned.
+CANARY_BYTE = 0xA5
+CANARY_BYTES = 4096
+_guarded = []
+
+
+def guarded_empty(shape, dtype, device="cuda"):
+    """An uninitialised tensor of `shape` and `dtype` with guard regions on
+    both sides; check_canaries() verifies them."""
+    import torch
+    itemsize = torch.empty((), dtype=dtype).element_size()
+    n = 1
+    for s in shape:
+        n *= int(s)
+    nbytes = n * itemsize
+    buf = torch.full((CANARY_BYTES * 2 + nbytes,), CANARY_BYTE, dtype=torch.uint8, device=device)
+    t = buf[CANARY_BYTES:CANARY_BYTES + nbytes].view(dtype).view(*shape)
+    _guarded.append((buf, nbytes))
+    return t
+
+
+def check_canaries():
+    """Asserts that no guarded output was written past either end; forgets
+    the checked buffers."""
+    import torch
+    torch.cuda.synchronize()
+    bad = []
+    for buf, nbytes in _guarded:
+        head = buf[:CANARY_BYTES]
+        tail = buf[CANARY_BYTES + nbytes:]
+        if not (bool((head == CANARY_BYTE).all()) and bool((tail == CANARY_BYTE).all())):
+            bad.append(nbytes)
+    _guarded.clear()
+    assert not bad, f"guard bytes around {len(bad)} output(s) were overwritten: {bad}"
+
+
+def guarded_like(t):
+    return guarded_empty(tuple(t.shape), t.dtype, t.device)

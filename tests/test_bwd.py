@@ -13,7 +13,8 @@ import pytest
 
 from oracle import attention_backward
 from synth import make_workload
-from tests.helpers import DeviceRun, check_bf16, oracle_spec
+from tests.helpers import (DeviceRun, check_bf16, check_canaries, guarded_empty,
+                           guarded_like, oracle_spec)
 
 pytestmark = pytest.mark.gpu
 
@@ -23,14 +24,14 @@ def run_bwd(w, use_block_mask=True):
     import masked_attention_gb300 as M
     g = DeviceRun(w, use_block_mask=use_block_mask, transposed=True)
     O, L = g.fwd()
-    dq = torch.empty_like(g.q)
-    dk = torch.empty_like(g.k)
-    dv = torch.empty_like(g.v)
-    ws = torch.empty(M.attn_bwd_workspace_bytes(w.B, w.Hq, w.Sq), dtype=torch.uint8,
-                     device="cuda")
+    dq = guarded_like(g.q)
+    dk = guarded_like(g.k)
+    dv = guarded_like(g.v)
+    ws = guarded_empty((M.attn_bwd_workspace_bytes(w.B, w.Hq, w.Sq),), torch.uint8)
     M.attn_bwd(g.q, g.k, g.v, O, L, g.do, dq, dk, dv, ws, g.variant, **g.kwargs())
     torch.cuda.synchronize()
     assert M.attn_check_status() == M.ATTN_OK
+    check_canaries()
     return g, dq, dk, dv
 
 

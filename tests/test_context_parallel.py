@@ -15,7 +15,8 @@ import pytest
 
 from oracle import attention_forward, block_mask, combine_partials
 from synth import make_workload
-from tests.helpers import check_bf16, max_abs, oracle_spec, variant_bits
+from tests.helpers import (check_bf16, check_canaries, guarded_empty, max_abs, oracle_spec,
+                           variant_bits)
 from tests.test_fwd import lse_tol
 
 pytestmark = pytest.mark.gpu
@@ -156,10 +157,10 @@ def test_combine_matches_oracle_merge(D, dtype, n, rows):
     o_parts[empty] = 0
     l_parts[:, :17] = -float("inf")   # rows with no kept key anywhere
     o_parts[:, :17] = 0
-    o = torch.empty(rows, D, dtype=tdt, device="cuda")
-    lse = torch.empty(rows, device="cuda")
+    o = guarded_empty((rows, D), tdt)
+    lse = guarded_empty((rows,), torch.float32)
     M.attn_combine(o_parts.cuda(), l_parts.cuda(), o, lse)
-    torch.cuda.synchronize()
+    check_canaries()
     O_ref, L_ref = combine_partials([(o_parts[k], l_parts[k]) for k in range(n)])
     O = o.float().cpu().numpy()
     L = lse.cpu().numpy()

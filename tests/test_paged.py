@@ -9,7 +9,8 @@ import torch
 
 from oracle import attention_forward
 from synth import make_workload
-from tests.helpers import DeviceRun, check_bf16, oracle_spec
+from tests.helpers import (DeviceRun, check_bf16, check_canaries, guarded_empty, guarded_like,
+                           oracle_spec)
 
 pytestmark = pytest.mark.gpu
 
@@ -56,11 +57,11 @@ def test_paged_forward_matches_contiguous_and_oracle(name):
     O_ref_gpu, L_ref_gpu = g.fwd()
     kp, vp, table = paged_pools(w.k, w.v, page_size, seed=710 + sorted(CASES).index(name))
     kp, vp, table = kp.cuda(), vp.cuda(), table.cuda()
-    o = torch.empty_like(g.q)
-    lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device="cuda")
+    o = guarded_like(g.q)
+    lse = guarded_empty((w.B, w.Hq, w.Sq), torch.float32)
     M.attn_fwd(g.q, kp, vp, o, lse, g.variant, Skv=w.Skv, page_table=table,
                page_size=page_size, **g.kwargs())
-    torch.cuda.synchronize()
+    check_canaries()
     assert torch.equal(o, O_ref_gpu) and torch.equal(lse, L_ref_gpu)
     O_ref, L_ref = attention_forward(w.q, w.k, w.v, oracle_spec(w))
     check_bf16(o.float().cpu().numpy(), O_ref, f"paged O {name}")
