@@ -644,6 +644,84 @@ def run_combine(args) -> None:
                       "frac_of_hbm": gbs / peaks["hbm_gbs"], "peak_source": src}), flush=True)
 
 
+# Decode workload: the grouped-query model shape of the prefix-LM workload
+# (Hq=32, Hkv=8, D=128, bf16), one new token per sequence at the end of a
+# 32768-token cache, 16 sequences: K and V total 2.1 GB, far above L2.
+DECODE_SHAPE = dict(B=16, Hq=32, Hkv=8, Sq=1, Skv=32768, D=128)
+# (label, page size or 0 for contiguous, sliding window or 0)
+DECODE_CASES = [("contiguous causal", 0, 0), ("paged 16 causal", 16, 0),
+                ("paged 64 causal", 64, 0), ("paged 64 causal + window 4096", 64, 4096)]
+
+
+def run_decode(args) -> None:
+    """Diagnostic: attn_decode (PagedAttention, alone and with a sliding
+    window) on the decode workload, contiguous and paged caches, one launch
+    sequence (decode kernel, then the merge of the key splits) timed with
+    CUDA events, L2 flushed between launches, against the measured HBM copy
+    bandwidth. Algorithmic bytes per launch: the K and V rows of the kept
+    keys read once per key/value head, Q read, O and LSE written, the page
+    table entries of the kept pages read."""
+    import torch
+
+    import masked_attention_gb300 as M
+
+    sh = dict(DECODE_SHAPE)
+    if args.batch:
+        sh["B"] = args.batch
+    B, Hq, Hkv, Sq, Skv, D = (sh[x] for x in ("B", "Hq", "Hkv", "Sq", "Skv", "D"))
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev).manual_seed(21)
+    q = torch.randn(B, Hq, Sq, D, generator=g, device=dev).to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, Sq, device=dev)
+    ws = torch.empty(max(M.attn_decode_workspace_bytes(B, Hq, Hkv, Sq, Skv, D), 256),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peaks, src = read_peaks()
+    variant_base = M.MASK_CAUSAL
+    for label, ps, window in DECODE_CASES:
+        if ps:
+            pps = Skv // ps
+            num_pages = B * pps
+            kc = torch.randn(num_pages, Hkv, ps, D, generator=g, device=dev).to(torch.bfloat16)
+            vc = torch.randn(num_pages, Hkv, ps, D, generator=g, device=dev).to(torch.bfloat16)
+            perm = torch.randperm(num_pages, generator=g, device=dev).to(torch.int32)
+            kw = dict(page_table=perm.view(B, pps), page_size=ps, Skv=Skv)
+        else:
+            kc = torch.randn(B, Hkv, Skv, D, generator=g, device=dev).to(torch.bfloat16)
+            vc = torch.randn(B, Hkv, Skv, D, generator=g, device=dev).to(torch.bfloat16)
+            kw = {}
+        variant = variant_base | (M.MASK_WINDOW if window else 0)
+        call = lambda: M.attn_decode(q, kc, vc, o, lse, variant, workspace=ws, window=window,
+                                     q_offset=Skv - Sq, **kw)
+        for _ in range(max(args.warmup, 3)):
+            call()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for s_ in range(args.steps):
+            flush.fill_(s_ & 0xFF)
+            ev[s_][0].record()
+            call()
+            ev[s_][1].record()
+        torch.cuda.synchronize()
+        if M.attn_check_status() != M.ATTN_OK:
+            raise RuntimeError("device status error during decode")
+        times = sorted(a.elapsed_time(b) for a, b in ev)
+        ms = times[args.steps // 2]
+        kept = min(window, Skv) if window else Skv
+        nbytes = (2 * B * Hkv * kept * D * 2 + 2 * B * Hq * Sq * D * 2 + 4 * B * Hq * Sq
+                  + (4 * B * ((kept + ps - 1) // ps + 1) if ps else 0))
+        gbs = nbytes / ms / 1e6
+        print(json.dumps({"diagnostic": "decode", "case": label, "B": B, "Hq": Hq, "Hkv": Hkv,
+                          "Sq": Sq, "Skv": Skv, "D": D, "page_size": ps, "window": window,
+                          "splits_workspace_bytes": ws.numel(), "ms_per_launch": ms,
+                          "ms_min": times[0], "bytes_per_launch": nbytes, "gbs": gbs,
+                          "frac_of_hbm": gbs / peaks["hbm_gbs"], "peak_source": src}),
+              flush=True)
+        del kc, vc
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -664,7 +742,12 @@ def main():
                     help="diagnostic: time the backward of the training workload instead")
     ap.add_argument("--combine", type=int, default=0,
                     help="diagnostic: time attn_combine over this many key/value shards")
+    ap.add_argument("--decode", action="store_true",
+                    help="diagnostic: time attn_decode on the decode workload")
     args = ap.parse_args()
+    if args.decode:
+        run_decode(args)
+        return
     if args.combine:
         run_combine(args)
         return

@@ -185,6 +185,32 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
                      int B, int Hq, int Hkv, int Sq, int Skv, int D,
                      unsigned variant, const attn_params* p, struct CUstream_st* stream);
 
+/* Decode: a few new query rows per sequence against a long key/value cache
+ * (FlexAttention page, variant list: PagedAttention, alone and with a
+ * sliding window). Same arguments, layouts and results as attn_fwd for
+ * ATTN_BF16, D = 64 or 128, with (Hq / Hkv) * Sq <= 16: the query rows of all
+ * query heads that share a key/value head are computed together, so each
+ * key and value row is read from memory once. K and V are contiguous or a
+ * paged cache (attn_params page_table etc., page_size 16, 32, 64 or 128); a
+ * page index outside [0, num_pages) reads as zeros. Every mask and score term
+ * is supported; for a new token at absolute position P, pass q_offset = P
+ * so the causal and window terms see it. p->block_mask is not used.
+ * The keys are split across CTAs when that gives more parallelism: the
+ * splits' partial results (fp32) go to `workspace` (device, 256-byte aligned,
+ * attn_decode_workspace_bytes() bytes for the full split count) and are
+ * merged into o and lse by the online-softmax merge. A smaller workspace (or
+ * NULL) means fewer splits (none with NULL). Asynchronous on `stream`;
+ * argument errors before any launch; ATTN_ERR_UNSUPPORTED for other dtypes,
+ * D or row counts, or B * Hkv > 65535. */
+attn_status attn_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                        unsigned variant, const attn_params* p,
+                        void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+
+/* Bytes of workspace attn_decode() uses for its full split count on the
+ * current device (0 when it does not split the keys). */
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int D);
+
 /* Merge of partial results over disjoint key sets, e.g. the key/value shards
  * of context-parallel attention (FlexAttention page, variant list: ... +
  * context parallel). It is the merge step of the online softmax

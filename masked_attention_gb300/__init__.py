@@ -7,6 +7,12 @@ been built (``python -m masked_attention_gb300._build``), loading it raises.
 
 Tensors are passed as torch CUDA tensors (or raw device addresses as ints);
 PyTorch provides device memory and streams only.
+
+With the environment variable ``MATTN_DEBUG=1`` set before the first call,
+the debug build ``libmattn_debug.so`` is loaded instead (device-side bounds
+checks, ``include/mattn_debug.h``; build it with
+``python -m masked_attention_gb300._build --debug``); ``debug_record`` and
+``debug_selftest`` read and test its checks.
 """
 from __future__ import annotations
 
@@ -18,12 +24,14 @@ from typing import Optional
 __all__ = [
     "MASK_CAUSAL", "MASK_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX", "SCORE_ALIBI",
     "SCORE_SOFTCAP", "BF16", "F32", "AttnError", "BlockMask", "attn_fwd", "attn_bwd",
+    "attn_decode", "attn_decode_workspace_bytes",
     "build_block_mask", "attn_block_mask_bytes", "attn_bwd_workspace_bytes", "attn_bwd_noalloc",
     "attn_check_status", "attn_status_str", "attn_last_cuda_error", "attn_combine", "lib",
-    "LIB_PATH",
+    "LIB_PATH", "LIB_DEBUG_PATH", "debug_record", "debug_selftest",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmattn.so")
+LIB_DEBUG_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmattn_debug.so")
 
 # Mirrors of the constants in include/mattn.h (a test checks they agree).
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_MISALIGNED = 0, 1, 2, 3
@@ -60,6 +68,11 @@ class attn_params(ctypes.Structure):
                 ("kv_offset", ctypes.c_int), ("doc_len", ctypes.c_int)]
 
 
+class attn_debug_info(ctypes.Structure):
+    _fields_ = [("count", ctypes.c_ulonglong), ("site", ctypes.c_int), ("pad", ctypes.c_int),
+                ("index", ctypes.c_longlong), ("bound", ctypes.c_longlong)]
+
+
 _lib = None
 
 
@@ -67,10 +80,13 @@ def lib() -> ctypes.CDLL:
     """The loaded library (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
-                               "`python -m masked_attention_gb300._build` (no CPU fallback)")
-        L = ctypes.CDLL(LIB_PATH)
+        debug = os.environ.get("MATTN_DEBUG", "0") not in ("", "0")
+        path = LIB_DEBUG_PATH if debug else LIB_PATH
+        if not os.path.exists(path):
+            flag = " --debug" if debug else ""
+            raise RuntimeError(f"{path} is missing: build it with "
+                               f"`python -m masked_attention_gb300._build{flag}` (no CPU fallback)")
+        L = ctypes.CDLL(path)
         vp, i, u, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
         P = ctypes.POINTER(attn_params)
         BM = ctypes.POINTER(attn_block_mask)
@@ -90,6 +106,10 @@ def lib() -> ctypes.CDLL:
         L.attn_bwd_noalloc.restype = i
         L.attn_doc_ids_from_seqlens.argtypes = [vp, i, i, vp, vp]
         L.attn_doc_ids_from_seqlens.restype = i
+        L.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, u, P, vp, sz, vp]
+        L.attn_decode.restype = i
+        L.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        L.attn_decode_workspace_bytes.restype = sz
         L.attn_combine.argtypes = [vp, vp, i, ctypes.c_longlong, i, i, vp, vp, vp]
         L.attn_combine.restype = i
         L.attn_check_status.argtypes = [vp, vp]
@@ -98,6 +118,13 @@ def lib() -> ctypes.CDLL:
         L.attn_status_str.restype = ctypes.c_char_p
         L.attn_last_cuda_error.argtypes = []
         L.attn_last_cuda_error.restype = ctypes.c_char_p
+        if debug:
+            L.attn_debug_record.argtypes = [ctypes.POINTER(attn_debug_info), i]
+            L.attn_debug_record.restype = i
+            L.attn_debug_site_name.argtypes = [i]
+            L.attn_debug_site_name.restype = ctypes.c_char_p
+            L.attn_debug_selftest.argtypes = [vp]
+            L.attn_debug_selftest.restype = i
         _lib = L
     return _lib
 
@@ -109,6 +136,30 @@ class AttnError(RuntimeError):
         if status == ATTN_ERR_CUDA:
             msg += f": {attn_last_cuda_error()}"
         super().__init__(msg)
+
+
+def _debug_lib():
+    L = lib()
+    if not hasattr(L, "attn_debug_record"):
+        raise RuntimeError("the release library is loaded: set MATTN_DEBUG=1 before the first "
+                           "call to load libmattn_debug.so")
+    return L
+
+
+def debug_record(clear: bool = False) -> dict:
+    """Debug build: the failed bounds checks of every kernel so far (count,
+    and site name, index and bound of the first); ``clear`` resets them."""
+    L = _debug_lib()
+    info = attn_debug_info()
+    _check(L.attn_debug_record(ctypes.byref(info), 1 if clear else 0), "attn_debug_record")
+    return {"count": int(info.count), "site": L.attn_debug_site_name(info.site).decode(),
+            "index": int(info.index), "bound": int(info.bound)}
+
+
+def debug_selftest(stream=None) -> None:
+    """Debug build: checks that an index planted past a buffer's end is
+    refused and recorded (attn_debug_selftest); raises if not."""
+    _check(_debug_lib().attn_debug_selftest(_stream(stream)), "attn_debug_selftest")
 
 
 def attn_last_cuda_error() -> str:
@@ -276,6 +327,38 @@ def attn_fwd(q, k, v, o, lse, variant: int = 0, *, B=None, Hq=None, Hkv=None, Sq
     st = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv, D,
                         variant, ctypes.byref(p), _stream(stream))
     _check(st, "attn_fwd")
+
+
+def attn_decode_workspace_bytes(B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int) -> int:
+    return int(lib().attn_decode_workspace_bytes(B, Hq, Hkv, Sq, Skv, D))
+
+
+def attn_decode(q, k, v, o, lse, variant: int = 0, *, workspace=None, Skv=None,
+                scale: float = 0.0, window: int = 0, softcap: float = 0.0, alibi_slopes=None,
+                doc_id=None, prefix_len=None, status=None, timeout_ns: int = 0, rel_bias=None,
+                page_table=None, page_size: int = 0, q_offset: int = 0, kv_offset: int = 0,
+                stream=None) -> None:
+    """Decode: few query rows (q [B,Hq,Sq,D], (Hq/Hkv) * Sq <= 16) against a
+    long key/value cache, contiguous [B,Hkv,Skv,D] or paged (``page_table``
+    [B, pages_per_seq] into pools [num_pages, Hkv, page_size, D]; pass
+    ``Skv``). ``workspace``: optional CUDA tensor for the split partial
+    results (``attn_decode_workspace_bytes``). Writes ``o`` and ``lse``."""
+    B, Hq, Sq, D = q.shape
+    Hkv = k.shape[1]
+    if Skv is None:
+        Skv = k.shape[2]
+    p = _params(BF16, scale, window, softcap, alibi_slopes, doc_id, prefix_len, None, status,
+                timeout_ns, 0, rel_bias, q_offset, kv_offset)
+    if page_table is not None:
+        p.page_table = _ptr(page_table)
+        p.page_size = page_size
+        p.pages_per_seq = page_table.shape[1]
+        p.num_pages = k.shape[0]
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Skv,
+                           D, variant, ctypes.byref(p), _ptr(workspace), ws_bytes,
+                           _stream(stream))
+    _check(st, "attn_decode")
 
 
 def attn_combine(o_parts, lse_parts, o, lse, stream=None) -> None:

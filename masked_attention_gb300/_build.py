@@ -1,6 +1,10 @@
 """Builds libmattn.so in-tree with nvcc for sm_103a (no cmake, no torch
 extension machinery). Translation units compile in parallel; the shared
-library links the CUDA runtime statically."""
+library links the CUDA runtime statically.
+
+build(debug=True) builds libmattn_debug.so from the same sources with
+-DMATTN_DEBUG: device-side bounds checks that record and skip an access out
+of range (include/mattn_debug.h), for tests."""
 from __future__ import annotations
 
 import os
@@ -15,8 +19,9 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libmattn.so")
+LIB_DEBUG_PATH = os.path.join(HERE, "libmattn_debug.so")
 SOURCES = ["api.cu", "mask_build.cu", "fwd_f32.cu", "fwd_tc.cu", "fwd_tc_rb.cu",
-           "fwd_tc_paged.cu", "bwd_tc.cu", "bwd_noalloc.cu", "varlen.cu", "combine.cu"]
+           "fwd_tc_paged.cu", "bwd_tc.cu", "bwd_noalloc.cu", "varlen.cu", "combine.cu", "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE]
@@ -34,15 +39,20 @@ def nvcc() -> str:
 
 def _deps() -> list:
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "mattn.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     files.append(os.path.abspath(__file__))
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def lib_path(debug: bool = False) -> str:
+    return LIB_DEBUG_PATH if debug else LIB_PATH
+
+
+def up_to_date(debug: bool = False) -> bool:
+    path = lib_path(debug)
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
@@ -83,18 +93,23 @@ def _object_stale(src: str, obj: str) -> bool:
     return any(os.path.getmtime(f) > t for f in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile every CUDA translation unit and link libmattn.so; returns its path."""
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          debug: bool = False) -> str:
+    """Compile every CUDA translation unit and link libmattn.so (with debug:
+    libmattn_debug.so, objects apart); returns its path."""
+    path = lib_path(debug)
+    if not force and up_to_date(debug):
+        return path
+    obj_dir = os.path.join(BUILD_DIR, "debug") if debug else BUILD_DIR
+    os.makedirs(obj_dir, exist_ok=True)
     exe = nvcc()
+    flags = FLAGS + (["-DMATTN_DEBUG"] if debug else [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
         if not force and not ptxas_info and not _object_stale(src, obj):
             return obj
-        cmd = [exe, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [exe, *ARCH, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if ptxas_info:
             cmd += ["-Xptxas", "-v"]
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -106,14 +121,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + ".tmp"
+    tmp = path + ".tmp"
     cmd = [exe, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, path)
+    return path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                debug="--debug" in sys.argv))

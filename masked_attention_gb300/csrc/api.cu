@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "host_util.h"
 #include "launch.h"
 
 #define MATTN_API extern "C" __attribute__((visibility("default")))
@@ -308,6 +309,114 @@ MATTN_API attn_status attn_fwd(const void* q, const void* k, const void* v, void
   return cuda_status(e);
 }
 
+namespace mattn {
+namespace {
+
+constexpr int kDecodeMaxRows = 16;  // query heads per key/value head times Sq
+
+// Splits of the keys for decode: enough CTAs for about two per SM, at least
+// 128 keys per split, at most 64 splits; chunk = keys per split (multiple of
+// 16). Returns the split count.
+int decode_splits(int B, int Hkv, int Skv, int& chunk) {
+  const long long ctas = (long long)B * Hkv;
+  long long want = ctas > 0 ? (2LL * sm_count() + ctas - 1) / ctas : 1;
+  long long cap = (Skv + 127) / 128;
+  if (want > cap) want = cap;
+  if (want > 64) want = 64;
+  if (want < 1) want = 1;
+  chunk = (int)(((Skv + want - 1) / want + 15) / 16 * 16);
+  if (chunk < 16) chunk = 16;
+  return (int)((Skv + chunk - 1) / chunk);
+}
+
+size_t decode_ws_per_split(int B, int Hq, int Sq, int D) {
+  const size_t rows = (size_t)B * Hq * Sq;
+  return align256(rows * D * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+}  // namespace
+}  // namespace mattn
+
+MATTN_API size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Skv, int D) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sq < 1 || Skv < 1 || (D != 64 && D != 128)) return 0;
+  int chunk = 0;
+  const int splits = decode_splits(B, Hkv, Skv, chunk);
+  return splits > 1 ? (size_t)splits * decode_ws_per_split(B, Hq, Sq, D) : 0;
+}
+
+MATTN_API attn_status attn_decode(const void* q, const void* k, const void* v, void* o,
+                                  float* lse, int B, int Hq, int Hkv, int Sq, int Skv, int D,
+                                  unsigned variant, const attn_params* p, void* workspace,
+                                  size_t workspace_bytes, struct CUstream_st* stream) {
+  DecodeProblem dp;
+  attn_status st = fill_problem(dp.f, q, k, v, o, lse, B, Hq, Hkv, Sq, Skv, D, variant, p);
+  if (st != ATTN_OK) return st;
+  if (p->dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)(Hq / Hkv) * Sq > kDecodeMaxRows) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * Hkv > 65535) return ATTN_ERR_UNSUPPORTED;  // one grid row per (b, hkv)
+  if (B == 0 || Sq == 0) return ATTN_OK;
+  if (!q || !o || !lse || (Skv > 0 && (!k || !v))) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3))
+    return ATTN_ERR_MISALIGNED;
+  if (p->page_table) {
+    const int ps = p->page_size;
+    if (ps != 16 && ps != 32 && ps != 64 && ps != 128) return ATTN_ERR_UNSUPPORTED;
+    if (p->num_pages < 1 || p->pages_per_seq < 1 ||
+        (long long)p->pages_per_seq * ps < (long long)Skv)
+      return ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(p->page_table) & 3) return ATTN_ERR_MISALIGNED;
+  }
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_MISALIGNED;
+  st = resolve_status(dp.f);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (Skv == 0) {  // every row is empty: O = 0, LSE = -inf
+    fill_empty_rows<<<256, 256, 0, s>>>(o, lse, (size_t)B * Hq * Sq, D, 2);
+    return cuda_status(cudaGetLastError());
+  }
+  // keys that some row can keep: without a prefix term, the causal bound of
+  // the last row and the window bound of the first one limit them
+  long long k_begin = 0, k_end = Skv;
+  if (!(variant & ATTN_MASK_PREFIX)) {
+    const long long qo = p->q_offset, ko = p->kv_offset;
+    if (variant & ATTN_MASK_CAUSAL) k_end = std::min<long long>(k_end, qo + Sq - ko);
+    if (variant & ATTN_MASK_WINDOW) k_begin = std::max<long long>(0, qo - p->window + 1 - ko);
+  }
+  k_begin &= ~15LL;
+  if (k_end <= k_begin) {  // no row keeps a key: O = 0, LSE = -inf
+    fill_empty_rows<<<256, 256, 0, s>>>(o, lse, (size_t)B * Hq * Sq, D, 2);
+    return cuda_status(cudaGetLastError());
+  }
+  const int span = (int)(k_end - k_begin);
+  int chunk = 0;
+  int splits = decode_splits(B, Hkv, span, chunk);
+  const size_t per = decode_ws_per_split(B, Hq, Sq, D);
+  const size_t fit = workspace ? workspace_bytes / per : 0;
+  if ((size_t)splits > fit) {  // as many splits as the workspace holds
+    splits = fit >= 2 ? (int)fit : 1;
+    chunk = (int)(((span + splits - 1) / splits + 15) / 16 * 16);
+    splits = (span + chunk - 1) / chunk;
+  }
+  if (splits <= 1) {
+    chunk = (span + 15) / 16 * 16;
+    splits = 1;
+  }
+  dp.splits = splits;
+  dp.chunk = chunk;
+  dp.k_begin = (int)k_begin;
+  dp.k_end = (int)k_end;
+  const size_t rows = (size_t)B * Hq * Sq;
+  dp.ws_o = splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  dp.ws_lse = splits > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                    align256(rows * D * sizeof(float)) * splits)
+                         : nullptr;
+  st = cuda_status(launch_decode(dp, s));
+  if (st != ATTN_OK || splits == 1) return st;
+  return cuda_status(launch_combine_f32_bf16(dp.ws_o, dp.ws_lse, splits, (long long)rows, D, o,
+                                             lse, s));
+}
+
 MATTN_API size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq) {
   if (B < 0 || Hq < 0 || Sq < 0) return 0;
   return sizeof(float) * (size_t)B * Hq * Sq;
@@ -390,3 +499,122 @@ MATTN_API attn_status attn_check_status(int* status_dev, struct CUstream_st* str
 MATTN_API const char* attn_last_cuda_error(void) {
   return cudaGetErrorName(t_last_cuda_error);
 }
+
+namespace mattn {
+MATTN_DEBUG_RECORD_ACCESSORS(api)
+}  // namespace mattn
+
+#ifdef MATTN_DEBUG
+// ---------------------------------------------------------------------------
+// Debug build only: the bounds-check records (debug.cuh) of every kernel
+// translation unit, and a self-test of the check.
+// ---------------------------------------------------------------------------
+#include "mattn_debug.h"
+
+namespace mattn {
+namespace {
+
+__global__ void debug_selftest_kernel(int* buf, int n) {
+  const int t = threadIdx.x;
+  const long long idx = t == 0 ? (long long)n + 3 : t;  // thread 0: planted past the end
+  if (MATTN_IN_BOUNDS(kSiteSelfTest, idx, n)) buf[idx] += 1;
+}
+
+struct DebugTu {
+  cudaError_t (*fetch)(DebugRecord*);
+  cudaError_t (*clear)();
+};
+
+const DebugTu kDebugTus[] = {
+    {debug_fetch_api, debug_clear_api},
+    {debug_fetch_fwd_f32, debug_clear_fwd_f32},
+    {debug_fetch_fwd_tc, debug_clear_fwd_tc},
+    {debug_fetch_fwd_tc_rb, debug_clear_fwd_tc_rb},
+    {debug_fetch_fwd_tc_paged, debug_clear_fwd_tc_paged},
+    {debug_fetch_bwd_tc, debug_clear_bwd_tc},
+    {debug_fetch_decode, debug_clear_decode},
+    {debug_fetch_combine, debug_clear_combine},
+    {debug_fetch_mask_build, debug_clear_mask_build},
+};
+
+}  // namespace
+}  // namespace mattn
+
+MATTN_API attn_status attn_debug_record(attn_debug_info* out, int clear) {
+  using namespace mattn;
+  if (!out) return ATTN_ERR_INVALID_ARG;
+  *out = attn_debug_info{};
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_status(e);
+  for (const DebugTu& tu : kDebugTus) {
+    DebugRecord r{};
+    e = tu.fetch(&r);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (r.count && !out->count) {
+      out->site = r.site;
+      out->index = r.index;
+      out->bound = r.bound;
+    }
+    out->count += r.count;
+    if (clear && r.count) {
+      e = tu.clear();
+      if (e != cudaSuccess) return cuda_status(e);
+    }
+  }
+  return ATTN_OK;
+}
+
+MATTN_API const char* attn_debug_site_name(int site) {
+  using namespace mattn;
+  switch (site) {
+    case kSiteNone: return "none";
+    case kSiteFwdList: return "forward: block-mask list entry";
+    case kSiteFwdPage: return "forward: page-table entry";
+    case kSiteFwdDoc: return "forward: document id";
+    case kSiteFwdO: return "forward: O row store";
+    case kSiteFwdLse: return "forward: LSE store";
+    case kSiteBwdList: return "backward: block-mask list entry";
+    case kSiteBwdRow: return "backward: LSE / Delta row term";
+    case kSiteBwdDoc: return "backward: document id";
+    case kSiteBwdGrad: return "backward: dQ / dK / dV row store";
+    case kSiteDecQ: return "decode: query row";
+    case kSiteDecKV: return "decode: key / value row";
+    case kSiteDecTable: return "decode: page-table entry";
+    case kSiteDecSide: return "decode: document id or relative-bias entry";
+    case kSiteDecOut: return "decode: output or split partial store";
+    case kSiteCombineIn: return "merge: part row or LSE";
+    case kSiteCombineOut: return "merge: merged row store";
+    case kSiteF32: return "fp32 forward: list entry, document id or bias entry";
+    case kSiteMaskBuild: return "block-mask builder: document id or order entry";
+    case kSiteSelfTest: return "self-test: planted index";
+  }
+  return "unknown";
+}
+
+MATTN_API attn_status attn_debug_selftest(struct CUstream_st* stream) {
+  using namespace mattn;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  constexpr int n = 16;
+  DebugRecord r{};
+  cudaError_t e = debug_clear_api();
+  int* buf = nullptr;
+  if (e == cudaSuccess) e = cudaMalloc(&buf, n * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemsetAsync(buf, 0, n * sizeof(int), s);
+  if (e == cudaSuccess) {
+    debug_selftest_kernel<<<1, n, 0, s>>>(buf, n);
+    e = cudaGetLastError();
+  }
+  int host[n] = {};
+  if (e == cudaSuccess) e = cudaMemcpyAsync(host, buf, sizeof(host), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = debug_fetch_api(&r);
+  if (buf) cudaFree(buf);
+  if (e != cudaSuccess) return cuda_status(e);
+  bool good = r.count == 1 && r.site == kSiteSelfTest && r.index == n + 3 && r.bound == n &&
+              host[0] == 0;
+  for (int t = 1; t < n; ++t) good = good && host[t] == 1;
+  e = debug_clear_api();
+  if (e != cudaSuccess) return cuda_status(e);
+  return good ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
+}
+#endif  // MATTN_DEBUG

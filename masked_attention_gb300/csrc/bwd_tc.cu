@@ -116,6 +116,7 @@ struct BUnit {
   int n_full, n_part, group;  // per head of the group (dKV) or total (dQ)
   const int* lf;
   const int* lp;
+  int n_inner;  // tiles of the streamed dimension (the debug build checks list entries)
   __device__ __forceinline__ int n() const { return (n_full + n_part) * group; }
   // iteration -> (head offset within group, streamed tile index, partial?)
   __device__ __forceinline__ void at(int it, int& hoff, int& t, bool& partial) const {
@@ -124,6 +125,7 @@ struct BUnit {
     const int j = it % m;
     partial = j >= n_full;
     t = j < n_full ? (lf ? lf[j] : j) : (lp ? lp[j - n_full] : j - n_full);
+    if (!MATTN_IN_BOUNDS(kSiteBwdList, t, n_inner)) t = 0;
   }
 };
 
@@ -137,8 +139,10 @@ __device__ __forceinline__ BUnit decode_bwd(const BwdArgs& a, int u) {
   const int n_inner = MODE == kDQ ? nkv : nq;
   const bool causal_bound = (p.variant & ATTN_MASK_CAUSAL) && !(p.variant & ATTN_MASK_PREFIX);
   int row;
-  if (a.lists.full_cnt) row = a.lists.order[rank];
-  else if (causal_bound)  // longest first: dQ large query tiles first, dKV small key tiles first
+  if (a.lists.full_cnt) {
+    row = a.lists.order[rank];
+    if (!MATTN_IN_BOUNDS(kSiteBwdList, row, p.B * n_outer)) row = 0;
+  } else if (causal_bound)  // longest first: dQ large query tiles first, dKV small key tiles first
     row = MODE == kDQ ? (rank % p.B) * nq + (nq - 1 - rank / p.B) : (rank % p.B) * nkv + rank / p.B;
   else row = rank;
   BUnit U;
@@ -151,6 +155,8 @@ __device__ __forceinline__ BUnit decode_bwd(const BwdArgs& a, int u) {
     U.n_part = a.lists.part_cnt[row];
     U.lf = a.lists.full_idx + (size_t)row * n_inner;
     U.lp = a.lists.part_idx + (size_t)row * n_inner;
+    if (!MATTN_IN_BOUNDS(kSiteBwdList, U.n_full, n_inner + 1)) U.n_full = 0;
+    if (!MATTN_IN_BOUNDS(kSiteBwdList, U.n_part, n_inner + 1 - U.n_full)) U.n_part = 0;
   } else {
     int first = 0, last = n_inner;
     if (causal_bound) {
@@ -162,6 +168,7 @@ __device__ __forceinline__ BUnit decode_bwd(const BwdArgs& a, int u) {
     U.n_part = masked ? last - first : 0;
     U.lf = U.lp = nullptr;  // dense: tiles first .. last-1 (first > 0 only for the causal dKV bound)
   }
+  U.n_inner = n_inner;
   return U;
 }
 
@@ -589,12 +596,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint4 z = make_uint4(0, 0, 0, 0);
         if (MODE == kDQ) {
           const size_t qrow = (size_t)(U.b * p.Hq + U.h) * p.Sq + r;
+          if (!MATTN_IN_BOUNDS(kSiteBwdGrad, qrow, (size_t)p.B * p.Hq * p.Sq)) continue;
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) + qrow * D +
                                                 g * kHalfD);
           for (int c = 0; c < kHalfD / 8; ++c) dst[c] = z;
           if (g == 0) a.delta_out[qrow] = 0.0f;
         } else {
           const size_t off = ((size_t)(U.b * p.Hkv + U.h) * p.Skv + r) * D + g * kHalfD;
+          if (!MATTN_IN_BOUNDS(kSiteBwdGrad, off / D, (size_t)p.B * p.Hkv * p.Skv)) continue;
           uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk) + off);
           uint4* dv = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dv) + off);
           for (int c = 0; c < kHalfD / 8; ++c) dk[c] = z, dv[c] = z;
@@ -602,14 +611,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const int* docb = has_doc ? p.mask.doc_id + (size_t)U.b * p.mask.doc_len : nullptr;
-      const int my_doc = docb ? docb[r] : 0;
+      const int my_doc = (docb && MATTN_IN_BOUNDS(kSiteBwdDoc, r, p.mask.doc_len)) ? docb[r] : 0;
       const int P = (p.variant & ATTN_MASK_PREFIX) ? p.mask.prefix_len[U.b] : INT_MIN;
       float row_lse2 = 0.0f, row_delta = 0.0f, row_dhat = 0.0f;
       if (MODE == kDQ) {
         const size_t qrow = (size_t)(U.b * p.Hq + U.h) * p.Sq + r;
-        const float l = p.lse[qrow];
+        const bool in = MATTN_IN_BOUNDS(kSiteBwdRow, qrow, (size_t)p.B * p.Hq * p.Sq);
+        const float l = in ? p.lse[qrow] : 0.0f;
         row_lse2 = l == -INFINITY ? INFINITY : l * kLog2e;  // empty row: every p is 0
-        row_dhat = a.delta[qrow];  // estimate from the bf16 O (delta_kernel)
+        row_dhat = in ? a.delta[qrow] : 0.0f;  // estimate from the bf16 O (delta_kernel)
       }
       for (int it = 0; it < n; ++it) {
         int hoff, tt;
@@ -824,7 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ++acc_it;
       tc_fence_after();
-      auto store_half = [&](uint32_t col, __nv_bfloat16* dst, float mul) {
+      auto store_half = [&](uint32_t col, __nv_bfloat16* dst, float mul, bool in) {
 #pragma unroll
         for (int c = 0; c < kHalfD / 32; ++c) {
           uint32_t rr[32];
@@ -838,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            if (in) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
       };
       if (MODE == kDQ) {  // dQ = scale (A - (Delta - Dhat) B); Delta to the workspace
@@ -852,7 +862,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++dx_it;
         const float delta = dx[t] + dx[kTile + t];
         const size_t qrow = (size_t)(U.b * p.Hq + U.h) * p.Sq + r;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + qrow * D + g * kHalfD;
+        const bool in = MATTN_IN_BOUNDS(kSiteBwdGrad, qrow, (size_t)p.B * p.Hq * p.Sq);
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + (in ? qrow : 0) * D + g * kHalfD;
         const float corr = delta - row_dhat;
 #pragma unroll
         for (int c = 0; c < kHalfD / 32; ++c) {
@@ -870,13 +881,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          for (int e = 0; e < 4; ++e)
+            if (in) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
         }
-        if (g == 0) a.delta_out[qrow] = delta;
+        if (g == 0 && in) a.delta_out[qrow] = delta;
       } else {
         const size_t off = ((size_t)(U.b * p.Hkv + U.h) * p.Skv + r) * D + g * kHalfD;
-        store_half(colAcc + g * kHalfD, static_cast<__nv_bfloat16*>(a.dv) + off, 1.0f);
-        store_half(colAcc + D + g * kHalfD, static_cast<__nv_bfloat16*>(a.dk) + off, scale);
+        // every thread loads its accumulator (a warp-wide TMEM load); the
+        // debug build skips the stores of a row outside dK / dV
+        const bool in = MATTN_IN_BOUNDS(kSiteBwdGrad, off / D, (size_t)p.B * p.Hkv * p.Skv);
+        store_half(colAcc + g * kHalfD, static_cast<__nv_bfloat16*>(a.dv) + off, 1.0f, in);
+        store_half(colAcc + D + g * kHalfD, static_cast<__nv_bfloat16*>(a.dk) + off, scale, in);
       }
       tc_fence_before();
       __syncwarp();
@@ -954,4 +969,8 @@ cudaError_t launch_bwd_tc(const BwdProblem& bp, cudaStream_t stream) {
   }
 }
 
+}  // namespace mattn
+
+namespace mattn {
+MATTN_DEBUG_RECORD_ACCESSORS(bwd_tc)
 }  // namespace mattn

@@ -8,6 +8,7 @@
 #include <cuda_bf16.h>
 #include <cuda.h>
 
+#include "debug.cuh"
 #include "mattn.h"  // include/ is on the include path
 
 namespace mattn {
@@ -70,7 +71,8 @@ __device__ __forceinline__ bool mask_keep(const MaskArgs& m, int b, int i, int j
   if (m.variant & ATTN_MASK_WINDOW) keep = keep && (i - j < m.window);
   if (m.variant & ATTN_MASK_DOCUMENT) {
     const int* d = m.doc_id + (size_t)b * m.doc_len;
-    keep = keep && (d[i] == d[j]);
+    const bool in = MATTN_IN_BOUNDS(kSiteF32, i, m.doc_len) && MATTN_IN_BOUNDS(kSiteF32, j, m.doc_len);
+    keep = keep && in && (d[i] == d[j]);
   }
   if (m.variant & ATTN_MASK_PREFIX) keep = keep || (j < m.prefix_len[b]);
   return keep;

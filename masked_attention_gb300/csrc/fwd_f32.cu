@@ -56,6 +56,8 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(FwdProblem p) {
     const int row = b * p.lists.nq + qt;
     n_full = p.lists.full_cnt[row];
     n_part = p.lists.part_cnt[row];
+    if (!MATTN_IN_BOUNDS(kSiteF32, n_full, min(nkv, p.lists.nkv) + 1)) n_full = 0;
+    if (!MATTN_IN_BOUNDS(kSiteF32, n_part, min(nkv, p.lists.nkv) + 1 - n_full)) n_part = 0;
     lf = p.lists.full_idx + (size_t)row * p.lists.nkv;
     lp = p.lists.part_idx + (size_t)row * p.lists.nkv;
   } else {
@@ -68,7 +70,8 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(FwdProblem p) {
 
   for (int t = 0; t < n_full + n_part; ++t) {
     const bool partial = t >= n_full;
-    const int kt = partial ? (lp ? lp[t - n_full] : t - n_full) : (lf ? lf[t] : t);
+    int kt = partial ? (lp ? lp[t - n_full] : t - n_full) : (lf ? lf[t] : t);
+    if (!MATTN_IN_BOUNDS(kSiteF32, kt, nkv)) kt = 0;
     for (int j0 = kt * kTile; j0 < min((kt + 1) * kTile, p.Skv); j0 += kChunk) {
       __syncthreads();
       for (int e = threadIdx.x; e < kChunk * D; e += 128) {
@@ -89,7 +92,8 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(FwdProblem p) {
         const int j = j0 + jj;
         if (p.variant & ATTN_SCORE_ALIBI) x -= slope * float(i - j + p.mask.q_off - p.mask.kv_off);
         bool keep = row_ok && j < p.Skv;
-        if (rb && keep) x += rb[i - j + p.score.rb_zero];
+        if (rb && keep && MATTN_IN_BOUNDS(kSiteF32, i - j + p.score.rb_zero, p.score.rb_len))
+          x += rb[i - j + p.score.rb_zero];
         if (p.variant & ATTN_SCORE_SOFTCAP) x = p.score.softcap * tanhf(x / p.score.softcap);
         if (partial && keep) keep = mask_keep(p.mask, b, i, j);
         s[jj] = keep ? x : -INFINITY;
@@ -129,4 +133,8 @@ cudaError_t launch_fwd_f32(const FwdProblem& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+}  // namespace mattn
+
+namespace mattn {
+MATTN_DEBUG_RECORD_ACCESSORS(fwd_f32)
 }  // namespace mattn

@@ -29,3 +29,7 @@ cudaError_t launch_fwd_tc(const FwdProblem& p, cudaStream_t stream) {
 }
 
 }  // namespace mattn
+
+namespace mattn {
+MATTN_DEBUG_RECORD_ACCESSORS(fwd_tc)
+}  // namespace mattn

@@ -97,6 +97,7 @@ struct Unit {
   int n_full, n_part;
   const int* lf;
   const int* lp;
+  int nkv;  // key tiles of the problem (the debug build checks list entries against it)
   __device__ __forceinline__ int n() const { return n_full + n_part; }
   // Visiting order: partial tiles, then full tiles, each from the largest key
   // index down. Keys near the query usually carry the largest scores (causal
@@ -104,12 +105,15 @@ struct Unit {
   // accumulator is rarely rescaled. The softmax result does not depend on it.
   __device__ __forceinline__ bool partial(int j) const { return j < n_part; }
   __device__ __forceinline__ int kt(int j) const {
+    int t;
     if (j < n_part) {
       const int a = n_part - 1 - j;
-      return lp ? lp[a] : a;
+      t = lp ? lp[a] : a;
+    } else {
+      const int a = n_full - 1 - (j - n_part);
+      t = lf ? lf[a] : a;
     }
-    const int a = n_full - 1 - (j - n_part);
-    return lf ? lf[a] : a;
+    return MATTN_IN_BOUNDS(kSiteFwdList, t, nkv) ? t : 0;
   }
 };
 
@@ -128,6 +132,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp)
   int row;
   if (p.lists.full_cnt) {
     row = p.lists.order[rank];
+    if (!MATTN_IN_BOUNDS(kSiteFwdList, row, p.B * nq)) row = 0;
   } else if (causal_bound) {
     row = (rank % p.B) * nq + (nq - 1 - rank / p.B);  // longest first
   } else {
@@ -143,6 +148,9 @@ __device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp)
     U.n_part = p.lists.part_cnt[row];
     U.lf = p.lists.full_idx + (size_t)row * p.lists.nkv;
     U.lp = p.lists.part_idx + (size_t)row * p.lists.nkv;
+    if (!MATTN_IN_BOUNDS(kSiteFwdList, U.n_full, min(nkv, p.lists.nkv) + 1)) U.n_full = 0;
+    if (!MATTN_IN_BOUNDS(kSiteFwdList, U.n_part, min(nkv, p.lists.nkv) + 1 - U.n_full))
+      U.n_part = 0;
   } else {
     const int last = causal_bound ? causal_tiles(p.mask, min((U.qt + 1) * kTile, p.Sq) - 1, nkv)
                                   : nkv;
@@ -151,13 +159,14 @@ __device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp)
     U.n_part = masked ? last : 0;
     U.lf = U.lp = nullptr;
   }
+  U.nkv = nkv;
   return U;
 }
 
 // Document id of key j, or -1 past the end of the keys (those columns are
-// masked by the key-length bound anyway).
-__device__ __forceinline__ int doc_at(const int* docb, int j, int Skv) {
-  return j < Skv ? docb[j] : -1;
+// masked by the key-length bound anyway). lim: entries of docb from key 0 on.
+__device__ __forceinline__ int doc_at(const int* docb, int j, int Skv, int lim) {
+  return (j < Skv && MATTN_IN_BOUNDS(kSiteFwdDoc, j, lim)) ? docb[j] : -1;
 }
 
 // A key tile is masked element by element when the lists call it partial or
@@ -186,7 +195,9 @@ __device__ __forceinline__ void load_kv_tile(uint8_t* dst, const CUtensorMap* ma
   const int last = (Skv + ps - 1) / ps - 1;
   for (int q = 0; q < per; ++q) {
     const int lp = min(kt * per + q, last);
-    const int phys = page_table[(size_t)b * pages_per_seq + lp];
+    const int phys = MATTN_IN_BOUNDS(kSiteFwdPage, lp, pages_per_seq)
+                         ? page_table[(size_t)b * pages_per_seq + lp]
+                         : 0;
 #pragma unroll
     for (int bx = 0; bx < kBoxes; ++bx)
       tma_load_3d(dst + bx * kBoxBytes + q * ps * 128, map, bar, bx * 64, 0, phys * Hkv + hk);
@@ -767,8 +778,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_in = i < p.Sq;  // a last query tile may run past Sq
       const size_t orow = ((size_t)(U.b * p.Hq + h) * p.Sq + i);
       __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + orow * D;
+      const size_t total_rows = (size_t)p.B * p.Hq * p.Sq;
+      (void)total_rows;
       if (n == 0) {
-        if (row_in) {
+        if (row_in && MATTN_IN_BOUNDS(kSiteFwdO, orow, total_rows)) {
           const uint4 z = make_uint4(0, 0, 0, 0);
           for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(O)[c] = z;
           p.lse[orow] = -INFINITY;
@@ -782,8 +795,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int* docb = (p.variant & ATTN_MASK_DOCUMENT)
                             ? p.mask.doc_id + (size_t)U.b * p.mask.doc_len + p.mask.kv_off
                             : nullptr;
+      const int doc_lim = p.mask.doc_len - p.mask.kv_off;
+      (void)doc_lim;
       const int doc_i =
-          (docb && row_in) ? p.mask.doc_id[(size_t)U.b * p.mask.doc_len + p.mask.q_off + i] : 0;
+          (docb && row_in && MATTN_IN_BOUNDS(kSiteFwdDoc, p.mask.q_off + i, p.mask.doc_len))
+              ? p.mask.doc_id[(size_t)U.b * p.mask.doc_len + p.mask.q_off + i]
+              : 0;
       const int dqk = p.mask.q_off - p.mask.kv_off;  // absolute i - j = (i - j) + dqk
       const int P = (p.variant & ATTN_MASK_PREFIX) ? p.mask.prefix_len[U.b] : INT_MIN;
       float m_ref = -INFINITY, l = 0.0f;
@@ -799,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int dcur[4] = {0, 0, 0, 0};
       if (docb && elementwise_tile(U, 0, kt_cur, p.Skv)) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) dcur[c] = doc_at(docb, kt_cur * kTile + lane + 32 * c, p.Skv);
+        for (int c = 0; c < 4; ++c) dcur[c] = doc_at(docb, kt_cur * kTile + lane + 32 * c, p.Skv, doc_lim);
       }
 
       for (int j = 0; j < n; ++j) {
@@ -808,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int dnext[4] = {0, 0, 0, 0};
         if (docb && j + 1 < n && elementwise_tile(U, j + 1, kt_n1, p.Skv)) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) dnext[c] = doc_at(docb, kt_n1 * kTile + lane + 32 * c, p.Skv);
+          for (int c = 0; c < 4; ++c) dnext[c] = doc_at(docb, kt_n1 * kTile + lane + 32 * c, p.Skv, doc_lim);
         }
         const int j0 = kt * kTile;
         const bool partial = elementwise_tile(U, j, kt, p.Skv);
@@ -963,7 +980,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // epilogue: O / l -> bf16, LSE = ln(sum exp); the LSE store goes first
       // so that it does not queue behind the output's
-      if (row_in) p.lse[orow] = l > 0.0f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
+      if (row_in && MATTN_IN_BOUNDS(kSiteFwdLse, orow, total_rows))
+        p.lse[orow] = l > 0.0f ? (m_ref + __log2f(l)) * kLn2 : -INFINITY;
       ok = __all_sync(0xffffffffu, wait_bounded(o_done + x, o_it & 1, wd));
       if (!ok) break;
       ++o_it;
@@ -1002,7 +1020,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 4; ++k) {
             const int rr = 8 * k + (lane >> 2), e = lane & 3;
             const uint4 v = stg[rr * 4 + (e ^ ((rr >> 1) & 3))];
-            if (row0 + rr < p.Sq)
+            if (row0 + rr < p.Sq &&
+                MATTN_IN_BOUNDS(kSiteFwdO, (size_t)(U.b * p.Hq + h) * p.Sq + row0 + rr, total_rows))
               *reinterpret_cast<uint4*>(Oh + (size_t)(row0 + rr) * D + 32 * c + 8 * e) = v;
           }
         }

@@ -25,3 +25,7 @@ cudaError_t launch_fwd_tc_paged(const FwdProblem& p, cudaStream_t stream) {
 }
 
 }  // namespace mattn
+
+namespace mattn {
+MATTN_DEBUG_RECORD_ACCESSORS(fwd_tc_paged)
+}  // namespace mattn

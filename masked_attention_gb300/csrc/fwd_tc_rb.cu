@@ -24,3 +24,7 @@ cudaError_t launch_fwd_tc_rb(const FwdProblem& p, cudaStream_t stream) {
 }
 
 }  // namespace mattn
+
+namespace mattn {
+MATTN_DEBUG_RECORD_ACCESSORS(fwd_tc_rb)
+}  // namespace mattn

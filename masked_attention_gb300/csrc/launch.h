@@ -37,6 +37,45 @@ struct BwdProblem {
   BlockLists t_lists;  // transposed lists (per key tile), or full_cnt == nullptr
 };
 
+// Decode (few query rows against a long cache): one CTA per (batch element,
+// key/value head, split of the keys); a split's partial result goes to the
+// fp32 workspace when splits > 1, else straight to o and lse.
+struct DecodeProblem {
+  FwdProblem f;
+  int splits;
+  int chunk;     // keys per split, a multiple of 16
+  int k_begin;   // keys [k_begin, k_end) can be kept (k_begin a multiple of 16);
+  int k_end;     // split s covers [k_begin + s * chunk, ...) within them
+  float* ws_o;   // [splits][B*Hq*Sq][D] fp32, or nullptr (splits == 1)
+  float* ws_lse; // [splits][B*Hq*Sq]
+};
+
+cudaError_t launch_decode(const DecodeProblem& dp, cudaStream_t stream);
+
+#ifdef MATTN_DEBUG
+// Debug build: each kernel translation unit's bounds-check record (copy out
+// and clear; see debug.cuh).
+#define MATTN_DECLARE_DEBUG_RECORD(name)             \
+  cudaError_t debug_fetch_##name(DebugRecord* out); \
+  cudaError_t debug_clear_##name();
+MATTN_DECLARE_DEBUG_RECORD(api)
+MATTN_DECLARE_DEBUG_RECORD(fwd_f32)
+MATTN_DECLARE_DEBUG_RECORD(fwd_tc)
+MATTN_DECLARE_DEBUG_RECORD(fwd_tc_rb)
+MATTN_DECLARE_DEBUG_RECORD(fwd_tc_paged)
+MATTN_DECLARE_DEBUG_RECORD(bwd_tc)
+MATTN_DECLARE_DEBUG_RECORD(decode)
+MATTN_DECLARE_DEBUG_RECORD(combine)
+MATTN_DECLARE_DEBUG_RECORD(mask_build)
+#undef MATTN_DECLARE_DEBUG_RECORD
+#endif
+
+// Merge of fp32 partial results into bf16 O (and fp32 LSE): the
+// online-softmax merge of attn_combine with fp32 parts and a bf16 output.
+cudaError_t launch_combine_f32_bf16(const float* o_parts, const float* lse_parts, int n_parts,
+                                    long long rows, int D, void* o, float* lse,
+                                    cudaStream_t stream);
+
 // Block-mask builder: writes counts, ascending index lists and the
 // longest-first order for the per-query-tile (transposed = 0) or per-key-tile
 // (transposed = 1) view.

@@ -18,12 +18,14 @@ struct Range {
   int lo, hi;  // inclusive
 };
 
-__device__ __forceinline__ void warp_doc_minmax(const int* doc, Range r, int& mn, int& mx) {
+// lim: entries of doc from position 0 on (the debug build checks against it).
+__device__ __forceinline__ void warp_doc_minmax(const int* doc, Range r, int lim, int& mn,
+                                                int& mx) {
   const int lane = threadIdx.x & 31;
   mn = INT_MAX;
   mx = INT_MIN;
   for (int p = r.lo + lane; p <= r.hi; p += 32) {
-    const int d = doc[p];
+    const int d = MATTN_IN_BOUNDS(kSiteMaskBuild, p, lim) ? doc[p] : 0;
     mn = min(mn, d);
     mx = max(mx, d);
   }
@@ -82,11 +84,14 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(MaskArgs m, 
   const int* doc = (m.variant & ATTN_MASK_DOCUMENT) ? m.doc_id + (size_t)b * m.doc_len : nullptr;
   const int* docq = doc ? doc + m.q_off : nullptr;   // by query row
   const int* dock = doc ? doc + m.kv_off : nullptr;  // by key column
+  const int limq = m.doc_len - m.q_off, limk = m.doc_len - m.kv_off;
+  (void)limq;
+  (void)limk;
 
   const int outer_len = transposed ? Skv : Sq;
   const Range ro{outer * kTile, min((outer + 1) * kTile, outer_len) - 1};
   int omin = 0, omax = 0;
-  if (doc) warp_doc_minmax(transposed ? dock : docq, ro, omin, omax);  // every warp computes it
+  if (doc) warp_doc_minmax(transposed ? dock : docq, ro, transposed ? limk : limq, omin, omax);  // every warp computes it
 
   for (int inner = warp; inner < n_inner; inner += kClassifyThreads / 32) {
     const int inner_len = transposed ? Sq : Skv;
@@ -103,7 +108,7 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(MaskArgs m, 
     bool doc_uniform = true;  // one document id over the tile's rows and columns
     if (st != kEmpty && doc) {
       int nmin = 0, nmax = 0;
-      warp_doc_minmax(transposed ? docq : dock, rn, nmin, nmax);
+      warp_doc_minmax(transposed ? docq : dock, rn, transposed ? limq : limk, nmin, nmax);
       const int qmin = transposed ? nmin : omin, qmax = transposed ? nmax : omax;
       const int kmin = transposed ? omin : nmin, kmax = transposed ? omax : nmax;
       doc_uniform = qmin == qmax && kmin == kmax && qmin == kmin;
@@ -120,7 +125,9 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(MaskArgs m, 
       for (int k = 0; k < 4; ++k) {
         const int c = lane + 32 * k;
         valid[k] = c < ncols;
-        dj[k] = (doc && valid[k]) ? dock[rj.lo + c] : 0;
+        dj[k] = (doc && valid[k] && MATTN_IN_BOUNDS(kSiteMaskBuild, rj.lo + c, limk))
+                    ? dock[rj.lo + c]
+                    : 0;
       }
       // The rows' document ids too: lane l holds rows l, l+32, l+64, l+96 and
       // each row's id is shuffled out, so the row loop never waits on memory.
@@ -128,7 +135,7 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(MaskArgs m, 
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int i = ri.lo + lane + 32 * k;
-        qd[k] = (doc && i <= ri.hi) ? docq[i] : 0;
+        qd[k] = (doc && i <= ri.hi && MATTN_IN_BOUNDS(kSiteMaskBuild, i, limq)) ? docq[i] : 0;
       }
       const bool causal = m.variant & ATTN_MASK_CAUSAL, window = m.variant & ATTN_MASK_WINDOW;
       const int P = (m.variant & ATTN_MASK_PREFIX) ? m.prefix_len[b] : INT_MIN;
@@ -194,21 +201,29 @@ __global__ void order_kernel(const int* cnt_full, const int* cnt_part, int n_row
         const int ck = cost[k];
         rank += (ck > c) || (ck == c && k < r);
       }
-      order[rank] = r;
+      if (MATTN_IN_BOUNDS(kSiteMaskBuild, rank, n_rows)) order[rank] = r;
     }
     return;
   }
   if (threadIdx.x != 0) return;
   int* hist = cost;  // n_inner + 2 buckets
   for (int c = 0; c < n_inner + 2; ++c) hist[c] = 0;
-  for (int r = 0; r < n_rows; ++r) ++hist[cnt_full[r] + cnt_part[r]];
+  for (int r = 0; r < n_rows; ++r) {
+    const int c = cnt_full[r] + cnt_part[r];
+    if (MATTN_IN_BOUNDS(kSiteMaskBuild, c, n_inner + 1)) ++hist[c];
+  }
   int pos = 0;
   for (int c = n_inner; c >= 0; --c) {
     const int n = hist[c];
     hist[c] = pos;
     pos += n;
   }
-  for (int r = 0; r < n_rows; ++r) order[hist[cnt_full[r] + cnt_part[r]]++] = r;
+  for (int r = 0; r < n_rows; ++r) {
+    const int c = cnt_full[r] + cnt_part[r];
+    if (!MATTN_IN_BOUNDS(kSiteMaskBuild, c, n_inner + 1)) continue;
+    const int at = hist[c]++;
+    if (MATTN_IN_BOUNDS(kSiteMaskBuild, at, n_rows)) order[at] = r;
+  }
 }
 
 }  // namespace
@@ -236,4 +251,8 @@ cudaError_t launch_block_mask(const MaskArgs& m, int B, int Sq, int Skv, int tra
   return cudaGetLastError();
 }
 
+}  // namespace mattn
+
+namespace mattn {
+MATTN_DEBUG_RECORD_ACCESSORS(mask_build)
 }  // namespace mattn
