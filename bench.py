@@ -115,8 +115,7 @@ def source_digest() -> str:
 
 
 # committed ncu summaries of the forward, by workload number
-PROFILES = {2: "fwd_tc_causal_alibi_b4h16s2048d64.md",
-            3: "fwd_tc_doc_window_causal_b1h16s16384d128.md",
+PROFILES = {3: "fwd_tc_doc_window_causal_b1h16s16384d128.md",
             4: "fwd_tc_gqa_prefix_softcap_b2h32s8192d128.md",
             5: "fwd_tc_causal_b8h16s4096d128.md"}
 
