@@ -920,6 +920,17 @@ cudaError_t launch_one(const BwdArgs& a, const CUtensorMap& mq, const CUtensorMa
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   });
   if (attr_err != cudaSuccess) return attr_err;
+  // setmaxnreg.inc draws on the registers the launch holds: refuse to launch
+  // if the compiled register count cannot cover the split (the increase
+  // would wait forever)
+  static int regs = -1;
+  static std::once_flag regs_once;
+  std::call_once(regs_once, [] {
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, bwd_kernel<D, SCORE, MODE>) == cudaSuccess) regs = fa.numRegs;
+  });
+  if (regs < 0 || 256LL * kRegsCompute + 128LL * kRegsOther > (long long)regs * kThreads)
+    return cudaErrorInvalidConfiguration;
   const int grid = units < sm_count() ? units : sm_count();
   if (grid == 0) return cudaSuccess;
   bwd_kernel<D, SCORE, MODE><<<grid, kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, mdo, a);

@@ -175,25 +175,31 @@ __device__ __forceinline__ bool elementwise_tile(const Unit& U, int j, int kt, i
   return U.partial(j) || (kt + 1) * kTile > Skv;
 }
 
-// TMA loads of one 128-row K or V tile of (b, kv head hk) at key tile kt:
-// one box per 64 columns, or, from a paged cache, one box per page and 64
-// columns (pages past the last one holding keys repeat it: their rows are
-// masked). The boxes of page q land q * page_size rows into the tile, a
-// multiple of the 8-row swizzle period.
+// TMA loads of one 128-row K or V tile of (b, kv head hk) at key tile kt,
+// called by the whole producer warp (issue: whether copies are issued at
+// all): one box per 64 columns, issued by lane 0, or, from a paged cache, one
+// box per page and 64 columns (pages past the last one holding keys repeat
+// it: their rows are masked), lane q reading page q's table entry and
+// issuing its boxes, so the table reads of a tile overlap instead of each
+// waiting for the previous one. The boxes of page q land q * page_size rows
+// into the tile, a multiple of the 8-row swizzle period.
 template <int kBoxes, int kBoxBytes, bool kPaged>
 __device__ __forceinline__ void load_kv_tile(uint8_t* dst, const CUtensorMap* map,
                                              uint64_t* bar, const int* page_table, int ps,
                                              int pages_per_seq, int Skv, int Hkv, int b, int hk,
-                                             int kt) {
+                                             int kt, int lane, bool issue) {
   if constexpr (!kPaged) {
+    if (issue && lane == 0) {
 #pragma unroll
-    for (int bx = 0; bx < kBoxes; ++bx)
-      tma_load_3d(dst + bx * kBoxBytes, map, bar, bx * 64, kt * kTile, b * Hkv + hk);
+      for (int bx = 0; bx < kBoxes; ++bx)
+        tma_load_3d(dst + bx * kBoxBytes, map, bar, bx * 64, kt * kTile, b * Hkv + hk);
+    }
     return;
   }
-  const int per = kTile / ps;
+  const int per = kTile / ps;  // <= 8 pages per tile (page size >= 16)
   const int last = (Skv + ps - 1) / ps - 1;
-  for (int q = 0; q < per; ++q) {
+  if (issue && lane < per) {
+    const int q = lane;
     const int lp = min(kt * per + q, last);
     const int phys = MATTN_IN_BOUNDS(kSiteFwdPage, lp, pages_per_seq)
                          ? page_table[(size_t)b * pages_per_seq + lp]
@@ -509,7 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- producer
     // The whole warp runs the loop (waits stay converged); lane 0 issues.
     // With ATTN_FAULT_NO_LOADS nothing is issued and the consumers' waits run out.
-    const bool leader = lane == 0 && !(p.fault_inject & ATTN_FAULT_NO_LOADS);
+    const bool issue = !(p.fault_inject & ATTN_FAULT_NO_LOADS);
+    const bool leader = lane == 0 && issue;
     uint32_t slot_it = 0, q_it = 0;
     bool ok = true;
     for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
@@ -546,13 +553,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __all_sync(0xffffffffu,
                           wait_bounded(slot_empty + slot, ((slot_it / C::kSlots) & 1) ^ 1, wd));
           if (!ok) break;
-          if (leader) {
-            mbar_arrive_expect_tx(slot_full + slot, C::kTileBytes);
-            load_kv_tile<C::kBoxes, C::kBoxBytes, PAGED>(sSlots + slot * C::kTileBytes,
-                                                  is_v ? &tm_v : &tm_k, slot_full + slot,
-                                                  p.page_table, p.page_size, p.pages_per_seq,
-                                                  p.Skv, p.Hkv, U.b, hks[x], kt);
-          }
+          if (leader) mbar_arrive_expect_tx(slot_full + slot, C::kTileBytes);
+          __syncwarp();
+          load_kv_tile<C::kBoxes, C::kBoxBytes, PAGED>(sSlots + slot * C::kTileBytes,
+                                                is_v ? &tm_v : &tm_k, slot_full + slot,
+                                                p.page_table, p.page_size, p.pages_per_seq,
+                                                p.Skv, p.Hkv, U.b, hks[x], kt, lane, issue);
           __syncwarp();
           ++slot_it;
         }
@@ -1060,6 +1066,19 @@ cudaError_t launch_typed(const FwdProblem& p, cudaStream_t stream) {
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   });
   if (attr_err != cudaSuccess) return attr_err;
+  // setmaxnreg.inc draws on the registers the launch holds: refuse to launch
+  // if the compiled register count cannot cover the split (the increase
+  // would wait forever)
+  static int regs = -1;
+  static std::once_flag regs_once;
+  std::call_once(regs_once, [] {
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, fwd_tc_kernel<D, SCORE, PAGED>) == cudaSuccess)
+      regs = fa.numRegs;
+  });
+  if (regs < 0 || 2LL * kSoftmaxThreads * kRegsSoftmax + 128LL * kRegsOther >
+                      (long long)regs * kThreads)
+    return cudaErrorInvalidConfiguration;
   const int units = p.B * ((p.Sq + kTile - 1) / kTile) * ((p.Hq + 1) / 2);
   const int grid = units < sm_count() ? units : sm_count();
   if (grid == 0) return cudaSuccess;
