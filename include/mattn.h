@@ -269,8 +269,10 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq);
  *   dv sum over the query heads of their group).
  * `workspace` is device memory of attn_bwd_workspace_bytes() bytes. No
  * atomics: results are bitwise reproducible. Supported: ATTN_BF16, D = 128 and
- * 64, Sq and Skv multiples of 128; a block mask built with transposed = 1 (or
- * NULL). */
+ * 64, any Sq, Skv >= 1 (a last tile that runs past Sq or Skv reads zero rows,
+ * its padding keys are masked and its padding rows are not stored); a block
+ * mask built with transposed = 1 (or NULL). Not supported (ATTN_ERR_UNSUPPORTED):
+ * paged K/V, position offsets, the relative-position bias. */
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dO, void* dq, void* dk, void* dv,
                      void* workspace, size_t workspace_bytes,

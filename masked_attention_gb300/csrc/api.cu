@@ -437,7 +437,6 @@ attn_status bwd_check_args(BwdProblem& bp, const void* q, const void* k, const v
   if (variant & ATTN_SCORE_RELBIAS) return ATTN_ERR_UNSUPPORTED;  // forward only
   if (p->q_offset || p->kv_offset) return ATTN_ERR_UNSUPPORTED;   // forward only
   if (p->page_table) return ATTN_ERR_UNSUPPORTED;                 // forward only
-  if (Sq % kTile != 0 || Skv % kTile != 0) return ATTN_ERR_UNSUPPORTED;
   if (B == 0 || Sq == 0 || Skv == 0) return ATTN_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
@@ -532,6 +531,7 @@ const DebugTu kDebugTus[] = {
     {debug_fetch_fwd_tc_rb, debug_clear_fwd_tc_rb},
     {debug_fetch_fwd_tc_paged, debug_clear_fwd_tc_paged},
     {debug_fetch_bwd_tc, debug_clear_bwd_tc},
+    {debug_fetch_bwd_tc_ragged, debug_clear_bwd_tc_ragged},
     {debug_fetch_decode, debug_clear_decode},
     {debug_fetch_combine, debug_clear_combine},
     {debug_fetch_mask_build, debug_clear_mask_build},

@@ -111,9 +111,9 @@ def test_argument_errors_return_before_launch(M):
     assert call_fwd(M, variant=M.MASK_DOCUMENT) == M.ATTN_ERR_INVALID_ARG
     assert call_fwd(M, variant=M.MASK_PREFIX) == M.ATTN_ERR_INVALID_ARG
     assert call_fwd(M, q=0x10008) == M.ATTN_ERR_MISALIGNED
-    # the bf16 backward still needs 128-multiples (the forward takes any length)
-    p = M._params(0, 0.0, 0, 0.0, None, None, None, None, None, 0)
-    st = M.lib().attn_bwd(*([0x10000] * 10), 1 << 20, 1, 2, 2, 200, 128, 64, M.MASK_CAUSAL,
+    # the backward takes any length but not position offsets (forward only)
+    p = M._params(0, 0.0, 0, 0.0, None, None, None, None, None, 0, q_offset=128)
+    st = M.lib().attn_bwd(*([0x10000] * 10), 1 << 20, 1, 2, 2, 200, 328, 64, M.MASK_CAUSAL,
                           ctypes.byref(p), None)
     assert st == M.ATTN_ERR_UNSUPPORTED
     # the relative-position bias needs its table, and the backward does not take it

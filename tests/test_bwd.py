@@ -66,6 +66,30 @@ def test_bwd_reduced(name):
     check_grads(w, dq, dk, dv)
 
 
+# Lengths that are not multiples of the 128-row tile: the last query and key
+# tiles run past Sq and Skv (zero-filled rows, padding keys masked, padding
+# rows not stored); Sq != Skv; a prefix longer than the keys; one position.
+RAGGED = {
+    "ragged_full_d64": dict(B=2, Hq=2, Hkv=1, Sq=200, Skv=333, D=64),
+    "ragged_causal_d128": dict(B=1, Hq=2, Hkv=2, S=300, D=128, causal=True),
+    "ragged_causal_alibi_softcap_d128": dict(B=1, Hq=4, Hkv=2, S=451, D=128, causal=True,
+                                             alibi=True, softcap=30.0),
+    "ragged_doc_window_d64": dict(B=2, Hq=2, Hkv=2, S=517, D=64, causal=True, window=150,
+                                  document=True, doc_lo=60, doc_hi=200),
+    "ragged_prefix_past_keys_d128": dict(B=1, Hq=2, Hkv=1, Sq=130, Skv=390, D=128,
+                                         causal=True, prefix=True, prefix_len=[450]),
+    "single_position_d64": dict(B=1, Hq=1, Hkv=1, S=1, D=64, causal=True),
+}
+
+
+@pytest.mark.parametrize("use_block_mask", [True, False])
+@pytest.mark.parametrize("name", sorted(RAGGED))
+def test_bwd_ragged(name, use_block_mask):
+    w = make_workload(0, seed=600 + sorted(RAGGED).index(name), backward=True, **RAGGED[name])
+    _, dq, dk, dv = run_bwd(w, use_block_mask=use_block_mask)
+    check_grads(w, dq, dk, dv)
+
+
 @pytest.mark.parametrize("name", ["causal_d128", "doc_window_causal_d128"])
 def test_bwd_without_block_mask(name):
     w = make_workload(0, seed=500 + sorted(CASES).index(name), backward=True, **CASES[name])
