@@ -159,8 +159,7 @@ typedef struct attn_params {
    * key column c of this call sit at absolute positions q_offset + r and
    * kv_offset + c, which every mask term, the ALiBi bias and the document ids
    * use. Results over disjoint key shards merge with attn_combine(). >= 0.
-   * Forward and block mask only (attn_bwd: ATTN_ERR_UNSUPPORTED when either
-   * is nonzero), not combined with ATTN_SCORE_RELBIAS. */
+   * Forward, backward and block mask; not combined with ATTN_SCORE_RELBIAS. */
   int q_offset;
   int kv_offset;
   /* Row length of doc_id: 0 selects L = max(q_offset + Sq, kv_offset + Skv);
@@ -271,8 +270,9 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq);
  * atomics: results are bitwise reproducible. Supported: ATTN_BF16, D = 128 and
  * 64, any Sq, Skv >= 1 (a last tile that runs past Sq or Skv reads zero rows,
  * its padding keys are masked and its padding rows are not stored); a block
- * mask built with transposed = 1 (or NULL). Not supported (ATTN_ERR_UNSUPPORTED):
- * paged K/V, position offsets, the relative-position bias. */
+ * mask built with transposed = 1 (or NULL); position offsets (attn_params
+ * q_offset, kv_offset), with a block mask built for the same offsets. Not
+ * supported (ATTN_ERR_UNSUPPORTED): paged K/V, the relative-position bias. */
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dO, void* dq, void* dk, void* dv,
                      void* workspace, size_t workspace_bytes,

@@ -131,16 +131,20 @@ struct BUnit {
   }
 };
 
-template <int MODE, bool RAGGED>
+template <int MODE, bool GENERAL>
 __device__ __forceinline__ BUnit decode_bwd(const BwdArgs& a, int u) {
   const FwdProblem& p = a.f;
-  const int nq = RAGGED ? (p.Sq + kTile - 1) / kTile : p.Sq / kTile;
-  const int nkv = RAGGED ? (p.Skv + kTile - 1) / kTile : p.Skv / kTile;
+  const int nq = GENERAL ? (p.Sq + kTile - 1) / kTile : p.Sq / kTile;
+  const int nkv = GENERAL ? (p.Skv + kTile - 1) / kTile : p.Skv / kTile;
+  // without a block mask the causal tile bound holds only at offset 0 (else
+  // every tile is visited and masked element by element)
+  const bool at_zero = !GENERAL || (p.mask.q_off == 0 && p.mask.kv_off == 0);
   const int heads = MODE == kDQ ? p.Hq : p.Hkv;
   const int rank = u / heads, h = u % heads;
   const int n_outer = MODE == kDQ ? nq : nkv;
   const int n_inner = MODE == kDQ ? nkv : nq;
-  const bool causal_bound = (p.variant & ATTN_MASK_CAUSAL) && !(p.variant & ATTN_MASK_PREFIX);
+  const bool causal_bound =
+      (p.variant & ATTN_MASK_CAUSAL) && !(p.variant & ATTN_MASK_PREFIX) && at_zero;
   int row;
   if (a.lists.full_cnt) {
     row = a.lists.order[rank];
@@ -175,10 +179,12 @@ __device__ __forceinline__ BUnit decode_bwd(const BwdArgs& a, int u) {
   return U;
 }
 
-template <int MODE>
+template <int MODE, bool GENERAL>
 __device__ __forceinline__ int dense_first(const BwdArgs& a, const BUnit& U) {
   const FwdProblem& p = a.f;
-  const bool causal_bound = (p.variant & ATTN_MASK_CAUSAL) && !(p.variant & ATTN_MASK_PREFIX);
+  const bool at_zero = !GENERAL || (p.mask.q_off == 0 && p.mask.kv_off == 0);
+  const bool causal_bound =
+      (p.variant & ATTN_MASK_CAUSAL) && !(p.variant & ATTN_MASK_PREFIX) && at_zero;
   return (!a.lists.full_cnt && MODE == kDKV && causal_bound) ? U.tile : 0;
 }
 
@@ -279,13 +285,15 @@ __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint64_t a_desc, uint6
   mma_ss_warp<K>(d_tmem, a, b, idesc, 0u);
 }
 
-// RAGGED: Sq or Skv is not a multiple of 128 (a separate instantiation, so
-// the kernel for whole tiles keeps its code unchanged): 3-D tensor maps read
+// GENERAL: Sq or Skv is not a multiple of 128, or the call's queries and
+// keys sit at position offsets (a separate instantiation, so the kernel for
+// whole tiles at offset 0 keeps its code unchanged). 3-D tensor maps read
 // zeros past the sequence, the extras of a tile that runs past it are loaded
-// by the producer's lanes with bounds, padding keys are masked in dQ,
-// padding query rows get LSE +inf in dK/dV (their P is 0), and rows past the
-// sequence are not stored.
-template <int D, int SCORE, int MODE, bool RAGGED>
+// by the producer's lanes with bounds, padding keys are masked in dQ, padding
+// query rows get LSE +inf in dK/dV (their P is 0), rows past the sequence are
+// not stored; every mask term, ALiBi and the document ids use the absolute
+// positions q_offset + i and kv_offset + j.
+template <int D, int SCORE, int MODE, bool GENERAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -358,8 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_base_smem;
 
-  const int nq = RAGGED ? (p.Sq + kTile - 1) / kTile : p.Sq / kTile;
-  const int nkv = RAGGED ? (p.Skv + kTile - 1) / kTile : p.Skv / kTile;
+  const int nq = GENERAL ? (p.Sq + kTile - 1) / kTile : p.Sq / kTile;
+  const int nkv = GENERAL ? (p.Skv + kTile - 1) / kTile : p.Skv / kTile;
   const int num_units = MODE == kDQ ? p.B * nq * p.Hq : p.B * nkv * p.Hkv;
   const int group = p.Hq / p.Hkv;
 
@@ -371,10 +379,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // With ATTN_FAULT_NO_LOADS nothing is issued and the consumers' waits run out.
     const bool issue = !(p.fault_inject & ATTN_FAULT_NO_LOADS);
     const bool leader = lane == 0 && issue;
-    // RAGGED: the streamed rows' extras start 16-byte aligned for every tile
+    // GENERAL: the streamed rows' extras start 16-byte aligned for every tile
     // when the row lengths are multiples of 4 (bulk copies need that)
     const bool rows_al = (p.Sq & 3) == 0;
-    const bool doc_al = (p.mask.doc_len & 3) == 0;
+    const int doc_off = MODE == kDQ ? p.mask.kv_off : p.mask.q_off;  // streamed rows' offset
+    const bool doc_al = (p.mask.doc_len & 3) == 0 && (doc_off & 3) == 0;
     const int len = MODE == kDQ ? p.Skv : p.Sq;
     (void)rows_al;
     (void)doc_al;
@@ -383,10 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t slot_it = 0, fix_it = 0;
     bool ok = true, pending1 = false;  // pending1: tile slot_it's second half issued alone
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const BUnit U = decode_bwd<MODE, RAGGED>(a, u);
+      const BUnit U = decode_bwd<MODE, GENERAL>(a, u);
       const int n = U.n();
       if (n == 0) continue;
-      const int first = dense_first<MODE>(a, U);
+      const int first = dense_first<MODE, GENERAL>(a, U);
       ok = __all_sync(0xffffffffu, wait_bounded(fix_empty, (fix_it & 1) ^ 1, wd));
       if (!ok) break;
       if (leader) {
@@ -394,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dQ: Q and dO rows of (b, h, tile); dKV: K and V rows of (b, hk, tile)
         const CUtensorMap* m0 = MODE == kDQ ? &tm_q : &tm_k;
         const CUtensorMap* m1 = MODE == kDQ ? &tm_do : &tm_v;
-        if constexpr (RAGGED) {
+        if constexpr (GENERAL) {
           const int slice = MODE == kDQ ? U.b * p.Hq + U.h : U.b * p.Hkv + U.h;
           for (int bx = 0; bx < C::kBoxes; ++bx) {
             tma_load_3d(sFix + bx * C::kBoxBytes, m0, fix_full, bx * 64, U.tile * kTile, slice);
@@ -425,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (leader) {
           mbar_arrive_expect_tx(slot_full1 + slot, C::kTileBytes);
-          if constexpr (RAGGED) {  // V rows of (b, hk, t) or dO rows of (b, h, t)
+          if constexpr (GENERAL) {  // V rows of (b, hk, t) or dO rows of (b, h, t)
             const int slice =
                 MODE == kDQ ? U.b * p.Hkv + U.h / group : U.b * p.Hq + U.h * group + hoff;
             for (int bx = 0; bx < C::kBoxes; ++bx)
@@ -448,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pending1 = true;
         ok = __all_sync(0xffffffffu, wait_bounded(slot_empty0 + slot, ph, wd));
         if (!ok) break;
-        if constexpr (RAGGED) {
+        if constexpr (GENERAL) {
           // The streamed rows' document ids (keys for dQ, queries for dKV)
           // and, for dKV, their LSE and Delta go to the slot's extras: by
           // asynchronous bulk copies when the tile lies inside the sequence
@@ -457,8 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // LSE +inf, so its P is 0, and Delta 0); the leader's arrive below
           // releases these stores with the slot.
           const bool whole = (t + 1) * kTile <= len;
-          const size_t doc0 = has_doc ? (size_t)U.b * p.mask.doc_len + t * kTile : 0;
-          const bool bulk_doc = has_doc && doc_al && whole && (t + 1) * kTile <= p.mask.doc_len;
+          const size_t doc0 =
+              has_doc ? (size_t)U.b * p.mask.doc_len + doc_off + t * kTile : 0;
+          const bool bulk_doc =
+              has_doc && doc_al && whole && doc_off + (t + 1) * kTile <= p.mask.doc_len;
           const size_t qrow0 =
               MODE == kDKV ? (size_t)(U.b * p.Hq + U.h * group + hoff) * p.Sq + t * kTile : 0;
           const bool bulk_rows = MODE == kDKV && rows_al && whole;
@@ -471,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int c = lane + 32 * k, pos = t * kTile + c;
               const bool in = pos < len;
               if (has_doc && !bulk_doc)
-                xdoc[c] = (in && pos < p.mask.doc_len) ? p.mask.doc_id[doc0 + c] : -1;
+                xdoc[c] = (in && doc_off + pos < p.mask.doc_len) ? p.mask.doc_id[doc0 + c] : -1;
               if (MODE == kDKV && !bulk_rows) {
                 xlse[c] = in ? p.lse[qrow0 + c] : INFINITY;
                 xdel[c] = in ? a.delta[qrow0 + c] : 0.0f;
@@ -567,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_warp(dp_full);
     };
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const BUnit U = decode_bwd<MODE, RAGGED>(a, u);
+      const BUnit U = decode_bwd<MODE, GENERAL>(a, u);
       const int n = U.n();
       if (n == 0) continue;
       ok = __all_sync(0xffffffffu, wait_bounded(fix_full, fix_it & 1, wd));
@@ -670,9 +681,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t slot_it = 0, s_it = 0, acc_it = 0, dx_it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-      const BUnit U = decode_bwd<MODE, RAGGED>(a, u);
+      const BUnit U = decode_bwd<MODE, GENERAL>(a, u);
       const int n = U.n();
-      const int first = dense_first<MODE>(a, U);
+      const int first = dense_first<MODE, GENERAL>(a, U);
       // the thread's own row: a query row (dQ) or a key row (dKV)
       const int r = U.tile * kTile + t;
       constexpr int kHalfD = D / 2;  // accumulator columns stored by each warpgroup
@@ -680,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint4 z = make_uint4(0, 0, 0, 0);
         if (MODE == kDQ) {
           const size_t qrow = (size_t)(U.b * p.Hq + U.h) * p.Sq + r;
-          if ((RAGGED && r >= p.Sq) || !MATTN_IN_BOUNDS(kSiteBwdGrad, qrow, (size_t)p.B * p.Hq * p.Sq))
+          if ((GENERAL && r >= p.Sq) || !MATTN_IN_BOUNDS(kSiteBwdGrad, qrow, (size_t)p.B * p.Hq * p.Sq))
             continue;
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dq) + qrow * D +
                                                 g * kHalfD);
@@ -688,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (g == 0) a.delta_out[qrow] = 0.0f;
         } else {
           const size_t off = ((size_t)(U.b * p.Hkv + U.h) * p.Skv + r) * D + g * kHalfD;
-          if ((RAGGED && r >= p.Skv) ||
+          if ((GENERAL && r >= p.Skv) ||
               !MATTN_IN_BOUNDS(kSiteBwdGrad, off / D, (size_t)p.B * p.Hkv * p.Skv))
             continue;
           uint4* dk = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk) + off);
@@ -698,18 +709,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const int* docb = has_doc ? p.mask.doc_id + (size_t)U.b * p.mask.doc_len : nullptr;
-      const int my_doc =
-          (docb && (!RAGGED || r < p.mask.doc_len) && MATTN_IN_BOUNDS(kSiteBwdDoc, r, p.mask.doc_len))
-              ? docb[r]
-              : 0;
+      // GENERAL: this row's absolute position (query rows: q_offset + r; key rows: kv_offset + r)
+      const int r_abs = GENERAL ? r + (MODE == kDQ ? p.mask.q_off : p.mask.kv_off) : r;
+      const int my_doc = (docb && (!GENERAL || r_abs < p.mask.doc_len) &&
+                          MATTN_IN_BOUNDS(kSiteBwdDoc, r_abs, p.mask.doc_len))
+                             ? docb[r_abs]
+                             : 0;
+      const int dqk = GENERAL ? p.mask.q_off - p.mask.kv_off : 0;  // absolute i - j = (i - j) + dqk
+      (void)dqk;
       const int P = (p.variant & ATTN_MASK_PREFIX) ? p.mask.prefix_len[U.b] : INT_MIN;
       float row_lse2 = 0.0f, row_delta = 0.0f, row_dhat = 0.0f;
       if (MODE == kDQ) {
         const size_t qrow = (size_t)(U.b * p.Hq + U.h) * p.Sq + r;
-        // RAGGED: a row past Sq (the last tile's padding) gets LSE +inf: its P is 0
+        // GENERAL: a row past Sq (the last tile's padding) gets LSE +inf: its P is 0
         const bool in =
-            (!RAGGED || r < p.Sq) && MATTN_IN_BOUNDS(kSiteBwdRow, qrow, (size_t)p.B * p.Hq * p.Sq);
-        const float l = in ? p.lse[qrow] : (RAGGED ? INFINITY : 0.0f);
+            (!GENERAL || r < p.Sq) && MATTN_IN_BOUNDS(kSiteBwdRow, qrow, (size_t)p.B * p.Hq * p.Sq);
+        const float l = in ? p.lse[qrow] : (GENERAL ? INFINITY : 0.0f);
         row_lse2 = l == -INFINITY ? INFINITY : l * kLog2e;  // empty row: every p is 0
         row_dhat = in ? a.delta[qrow] : 0.0f;  // estimate from the bf16 O (delta_kernel)
       }
@@ -718,8 +733,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool partial;
         U.at(it, hoff, tt, partial);
         tt += first;
-        // RAGGED, dQ: a key tile that runs past Skv is masked element by element
-        if (RAGGED && MODE == kDQ && (tt + 1) * kTile > p.Skv) partial = true;
+        // GENERAL, dQ: a key tile that runs past Skv is masked element by element
+        if (GENERAL && MODE == kDQ && (tt + 1) * kTile > p.Skv) partial = true;
         const int h = MODE == kDQ ? U.h : U.h * group + hoff;
         const uint32_t seq = slot_it + it;
         const uint8_t* base = sSlots + (seq % C::kSlots) * C::kSlotBytes;
@@ -738,15 +753,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // mask bounds on the column c of this warpgroup's 64 (see below)
         int lo = INT_MIN, hi = INT_MAX, pre = INT_MIN;
         if (partial) {
-          if (MODE == kDQ) {  // row i = r, column j = c0 + c
+          if constexpr (GENERAL) {  // absolute positions; keys past Skv: none kept
+            if (MODE == kDQ) {  // row i = r, column j = c0 + c
+              if (p.variant & ATTN_MASK_CAUSAL) hi = r - c0 + dqk + 1;
+              if (p.variant & ATTN_MASK_WINDOW) lo = r - c0 + dqk - p.mask.window + 1;
+              hi = min(hi, p.Skv - c0);
+              if (P != INT_MIN) pre = min(P - p.mask.kv_off, p.Skv) - c0;
+            } else {            // row j = r, column i = c0 + c
+              if (p.variant & ATTN_MASK_CAUSAL) lo = r - c0 - dqk;
+              if (p.variant & ATTN_MASK_WINDOW) hi = r - c0 - dqk + p.mask.window;
+              if (P != INT_MIN && r_abs < P) pre = INT_MAX;
+            }
+          } else if (MODE == kDQ) {  // row i = r, column j = c0 + c
             if (p.variant & ATTN_MASK_CAUSAL) hi = r - c0 + 1;
             if (p.variant & ATTN_MASK_WINDOW) lo = r - c0 - p.mask.window + 1;
-            if constexpr (RAGGED) {  // keys past Skv: none kept
-              hi = min(hi, p.Skv - c0);
-              if (P != INT_MIN) pre = min(P, p.Skv) - c0;
-            } else {
-              if (P != INT_MIN) pre = P - c0;
-            }
+            if (P != INT_MIN) pre = P - c0;
           } else {            // row j = r, column i = c0 + c
             if (p.variant & ATTN_MASK_CAUSAL) lo = r - c0;
             if (p.variant & ATTN_MASK_WINDOW) hi = r - c0 + p.mask.window;
@@ -754,7 +775,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // (j - i) = base_ji + sgn * c for the column c of this warpgroup's 64
-        const int base_ji = MODE == kDQ ? c0 - r : r - c0;
+        // (absolute positions: minus dqk)
+        const int base_ji = (MODE == kDQ ? c0 - r : r - c0) - (GENERAL ? dqk : 0);
         const float sgn = MODE == kDQ ? 1.0f : -1.0f;
         // P (and P g) from S, 16 columns at a time, two columns per packed
         // instruction; v keeps P g for dS. An empty row (LSE = -inf) occurs
@@ -962,7 +984,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float delta = dx[t] + dx[kTile + t];
         const size_t qrow = (size_t)(U.b * p.Hq + U.h) * p.Sq + r;
         const bool in =
-            (!RAGGED || r < p.Sq) && MATTN_IN_BOUNDS(kSiteBwdGrad, qrow, (size_t)p.B * p.Hq * p.Sq);
+            (!GENERAL || r < p.Sq) && MATTN_IN_BOUNDS(kSiteBwdGrad, qrow, (size_t)p.B * p.Hq * p.Sq);
         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + (in ? qrow : 0) * D + g * kHalfD;
         const float corr = delta - row_dhat;
 #pragma unroll
@@ -989,7 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t off = ((size_t)(U.b * p.Hkv + U.h) * p.Skv + r) * D + g * kHalfD;
         // every thread loads its accumulator (a warp-wide TMEM load); the
         // debug build skips the stores of a row outside dK / dV
-        const bool in = (!RAGGED || r < p.Skv) &&
+        const bool in = (!GENERAL || r < p.Skv) &&
                         MATTN_IN_BOUNDS(kSiteBwdGrad, off / D, (size_t)p.B * p.Hkv * p.Skv);
         store_half(colAcc + g * kHalfD, static_cast<__nv_bfloat16*>(a.dv) + off, 1.0f, in);
         store_half(colAcc + D + g * kHalfD, static_cast<__nv_bfloat16*>(a.dk) + off, scale, in);
@@ -1009,7 +1031,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int SCORE, int MODE, bool RAGGED>
+template <int D, int SCORE, int MODE, bool GENERAL>
 cudaError_t launch_one(const BwdArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, const CUtensorMap& mdo, int units,
                        cudaStream_t stream) {
@@ -1017,7 +1039,7 @@ cudaError_t launch_one(const BwdArgs& a, const CUtensorMap& mq, const CUtensorMa
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(bwd_kernel<D, SCORE, MODE, RAGGED>,
+    attr_err = cudaFuncSetAttribute(bwd_kernel<D, SCORE, MODE, GENERAL>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -1028,17 +1050,17 @@ cudaError_t launch_one(const BwdArgs& a, const CUtensorMap& mq, const CUtensorMa
   static std::once_flag regs_once;
   std::call_once(regs_once, [] {
     cudaFuncAttributes fa{};
-    if (cudaFuncGetAttributes(&fa, bwd_kernel<D, SCORE, MODE, RAGGED>) == cudaSuccess) regs = fa.numRegs;
+    if (cudaFuncGetAttributes(&fa, bwd_kernel<D, SCORE, MODE, GENERAL>) == cudaSuccess) regs = fa.numRegs;
   });
   if (regs < 0 || 256LL * kRegsCompute + 128LL * kRegsOther > (long long)regs * kThreads)
     return cudaErrorInvalidConfiguration;
   const int grid = units < sm_count() ? units : sm_count();
   if (grid == 0) return cudaSuccess;
-  bwd_kernel<D, SCORE, MODE, RAGGED><<<grid, kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, mdo, a);
+  bwd_kernel<D, SCORE, MODE, GENERAL><<<grid, kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, mdo, a);
   return cudaGetLastError();
 }
 
-template <int D, int SCORE, bool RAGGED>
+template <int D, int SCORE, bool GENERAL>
 cudaError_t launch_typed(const BwdProblem& bp, cudaStream_t stream) {
   const FwdProblem& f = bp.f;
   const size_t rows = (size_t)f.B * f.Hq * f.Sq;
@@ -1048,7 +1070,7 @@ cudaError_t launch_typed(const BwdProblem& bp, cudaStream_t stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv, mdo;
-  if constexpr (RAGGED) {  // 3-D views [B*H][S][D]: a tile past the sequence reads zeros
+  if constexpr (GENERAL) {  // 3-D views [B*H][S][D]: a tile past the sequence reads zeros
     if (!make_map_bf16_3d(&mq, f.q, (long long)f.B * f.Hq, f.Sq, D) ||
         !make_map_bf16_3d(&mk, f.k, (long long)f.B * f.Hkv, f.Skv, D) ||
         !make_map_bf16_3d(&mv, f.v, (long long)f.B * f.Hkv, f.Skv, D) ||
@@ -1063,10 +1085,10 @@ cudaError_t launch_typed(const BwdProblem& bp, cudaStream_t stream) {
   }
   BwdArgs a{f, bp.dO, bp.dq, bp.dk, bp.dv, bp.delta, bp.delta, f.lists};
   const int nq = (f.Sq + kTile - 1) / kTile, nkv = (f.Skv + kTile - 1) / kTile;
-  e = launch_one<D, SCORE, kDQ, RAGGED>(a, mq, mk, mv, mdo, f.B * nq * f.Hq, stream);
+  e = launch_one<D, SCORE, kDQ, GENERAL>(a, mq, mk, mv, mdo, f.B * nq * f.Hq, stream);
   if (e != cudaSuccess) return e;
   a.lists = bp.t_lists;
-  return launch_one<D, SCORE, kDKV, RAGGED>(a, mq, mk, mv, mdo, f.B * nkv * f.Hkv, stream);
+  return launch_one<D, SCORE, kDKV, GENERAL>(a, mq, mk, mv, mdo, f.B * nkv * f.Hkv, stream);
 }
 
 }  // namespace

@@ -1,6 +1,7 @@
 // Launches of the backward (kernel in bwd_tc_kernel.cuh) for sequence
-// lengths that are not multiples of the 128-row tile (the RAGGED
-// instantiation; compiled in its own file, so the builds run in parallel).
+// lengths that are not multiples of the 128-row tile or calls at position
+// offsets (the GENERAL instantiation; compiled in its own file, so the
+// builds run in parallel).
 #include "bwd_tc_kernel.cuh"
 
 namespace mattn {

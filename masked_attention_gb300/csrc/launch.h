@@ -89,7 +89,7 @@ cudaError_t launch_fwd_tc(const FwdProblem& p, cudaStream_t stream);
 cudaError_t launch_fwd_tc_rb(const FwdProblem& p, cudaStream_t stream);     // relative bias
 cudaError_t launch_fwd_tc_paged(const FwdProblem& p, cudaStream_t stream);  // paged K/V
 cudaError_t launch_bwd_tc(const BwdProblem& p, cudaStream_t stream);
-// Sq or Skv not a multiple of 128 (bwd_tc_ragged.cu).
+// Sq or Skv not a multiple of 128, or position offsets (bwd_tc_ragged.cu).
 cudaError_t launch_bwd_tc_ragged(const BwdProblem& p, cudaStream_t stream);
 
 // The checks attn_bwd makes on everything but its workspace (no CUDA call);

@@ -111,8 +111,9 @@ def test_argument_errors_return_before_launch(M):
     assert call_fwd(M, variant=M.MASK_DOCUMENT) == M.ATTN_ERR_INVALID_ARG
     assert call_fwd(M, variant=M.MASK_PREFIX) == M.ATTN_ERR_INVALID_ARG
     assert call_fwd(M, q=0x10008) == M.ATTN_ERR_MISALIGNED
-    # the backward takes any length but not position offsets (forward only)
+    # the backward takes any length and position offsets, but not a paged cache
     p = M._params(0, 0.0, 0, 0.0, None, None, None, None, None, 0, q_offset=128)
+    p.page_table, p.page_size, p.pages_per_seq, p.num_pages = 0x30000, 64, 8, 8
     st = M.lib().attn_bwd(*([0x10000] * 10), 1 << 20, 1, 2, 2, 200, 328, 64, M.MASK_CAUSAL,
                           ctypes.byref(p), None)
     assert st == M.ATTN_ERR_UNSUPPORTED
@@ -147,9 +148,11 @@ def test_offset_and_merge_argument_errors(M):
     st = L.attn_fwd(*([0x10000] * 5), 1, 2, 2, 128, 128, 64, M.MASK_DOCUMENT, ctypes.byref(p),
                     None)
     assert st == M.ATTN_ERR_INVALID_ARG
-    p = M._params(0, 0.0, 0, 0.0, None, None, None, None, None, 0, kv_offset=128)
-    st = L.attn_bwd(*([0x10000] * 10), 1 << 20, 1, 2, 2, 128, 128, 64, M.MASK_CAUSAL,
-                    ctypes.byref(p), None)
+    # the backward takes offsets, not with the relative-position bias
+    p = M._params(0, 0.0, 0, 0.0, None, None, None, None, None, 0, rel_bias=0x20000,
+                  kv_offset=128)
+    st = L.attn_bwd(*([0x10000] * 10), 1 << 20, 1, 2, 2, 128, 128, 64,
+                    M.MASK_CAUSAL | M.SCORE_RELBIAS, ctypes.byref(p), None)
     assert st == M.ATTN_ERR_UNSUPPORTED
     # a block mask built for other offsets does not describe the call
     bm = M.attn_block_mask()

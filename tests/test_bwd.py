@@ -14,7 +14,7 @@ import pytest
 from oracle import attention_backward
 from synth import make_workload
 from tests.helpers import (DeviceRun, check_bf16, check_canaries, guarded_empty,
-                           guarded_like, oracle_spec)
+                           guarded_like, oracle_spec, variant_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -112,3 +112,60 @@ def test_bwd_deterministic():
     for _ in range(2):
         _, a2, b2, c2 = run_bwd(w)
         assert torch.equal(a, a2) and torch.equal(b, b2) and torch.equal(c, c2)
+
+
+# One query shard against one key shard of a longer sequence (context
+# parallelism): the call's rows and keys sit at absolute positions
+# q_offset + i and kv_offset + j of the whole sequence, which every mask
+# term, ALiBi and the document ids use. The gradients are those of this
+# call's partial attention (its own O and LSE), against the oracle's with the
+# same offsets. (whole-sequence overrides, (q_lo, q_hi), (kv_lo, kv_hi))
+SHARDS = {
+    "doc_window_causal_d128": (dict(B=1, Hq=2, Hkv=2, S=1024, D=128, causal=True, window=300,
+                                    document=True, doc_lo=100, doc_hi=400), (512, 1024), (256, 768)),
+    "causal_alibi_softcap_ragged_d64": (dict(B=1, Hq=2, Hkv=1, S=800, D=64, causal=True,
+                                             alibi=True, softcap=20.0), (300, 700), (100, 600)),
+    "gqa_prefix_causal_d128": (dict(B=2, Hq=4, Hkv=2, S=600, D=128, causal=True, prefix=True,
+                                    prefix_len=[250, 420]), (200, 456), (0, 333)),
+    "full_alibi_keys_after_queries_d64": (dict(B=1, Hq=2, Hkv=2, S=640, D=64, alibi=True),
+                                          (128, 256), (384, 640)),
+}
+
+
+@pytest.mark.parametrize("use_block_mask", [True, False])
+@pytest.mark.parametrize("name", sorted(SHARDS))
+def test_bwd_position_offsets(name, use_block_mask):
+    import dataclasses
+    import torch
+    import masked_attention_gb300 as M
+    over, (qa, qb), (ka, kb) = SHARDS[name]
+    w = make_workload(0, seed=650 + sorted(SHARDS).index(name), backward=True, **over)
+    dev = "cuda"
+    q = w.q[:, :, qa:qb].contiguous()
+    do = w.do[:, :, qa:qb].contiguous()
+    k = w.k[:, :, ka:kb].contiguous()
+    v = w.v[:, :, ka:kb].contiguous()
+    variant = variant_bits(w)
+    doc = torch.from_numpy(w.doc_id).to(dev) if w.document else None
+    pre = torch.from_numpy(w.prefix_len).to(dev) if w.prefix else None
+    kw = dict(window=w.window or 0, softcap=w.softcap or 0.0, doc_id=doc, prefix_len=pre,
+              q_offset=qa, kv_offset=ka)
+    bm = None
+    if use_block_mask:
+        bm = M.build_block_mask(variant & 0xF, w.B, qb - qa, kb - ka, window=w.window or 0,
+                                doc_id=doc, prefix_len=pre, q_offset=qa, kv_offset=ka,
+                                transposed=True)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o = guarded_like(qd)
+    lse = guarded_empty((w.B, w.Hq, qb - qa), torch.float32)
+    M.attn_fwd(qd, kd, vd, o, lse, variant, block_mask=bm, **kw)
+    dq, dk, dv = guarded_like(qd), guarded_like(kd), guarded_like(vd)
+    ws = guarded_empty((M.attn_bwd_workspace_bytes(w.B, w.Hq, qb - qa),), torch.uint8)
+    M.attn_bwd(qd, kd, vd, o, lse, dod, dq, dk, dv, ws, variant, block_mask=bm, **kw)
+    torch.cuda.synchronize()
+    assert M.attn_check_status() == M.ATTN_OK
+    check_canaries()
+    spec = dataclasses.replace(oracle_spec(w), q_offset=qa, kv_offset=ka)
+    dQ, dK, dV, _, _ = attention_backward(q, k, v, do, spec)
+    for nm, got, ref in (("dq", dq, dQ), ("dk", dk, dK), ("dv", dv, dV)):
+        check_bf16(got.float().cpu().numpy(), ref, f"{nm} shard {name}")

@@ -395,6 +395,44 @@ def test_backward_matches_finite_differences(spec):
         assert np.max(np.abs(num - g)) < 1e-6 * max(1.0, np.max(np.abs(g))), name
 
 
+# Shards of a longer sequence (context parallelism): the queries and keys sit
+# at absolute positions q_offset + i and kv_offset + j, Sq != Skv, and every
+# position-dependent term (causal, window, prefix, document ids, ALiBi) uses
+# the absolute positions.
+OFFSET_GRAD_SPECS = [
+    Spec(causal=True, q_offset=9, kv_offset=6),
+    Spec(causal=True, window=4, alibi=True, softcap=2.0, q_offset=9, kv_offset=6),
+    Spec(causal=True, prefix_len=np.array([8]), q_offset=9, kv_offset=6),
+    Spec(causal=True, doc_id=np.array([[0] * 11 + [1] * 5]), q_offset=9, kv_offset=6),
+    Spec(alibi=True, q_offset=2, kv_offset=11),
+]
+
+
+@pytest.mark.parametrize("spec", OFFSET_GRAD_SPECS)
+def test_backward_with_offsets_matches_finite_differences(spec):
+    B, Hq, Hkv, Sq, Skv, D = 1, 4, 2, 5, 7, 3
+    q, k, v = rnd((B, Hq, Sq, D), 146), rnd((B, Hkv, Skv, D), 147), rnd((B, Hkv, Skv, D), 148)
+    do = rnd((B, Hq, Sq, D), 149)
+    dQ, dK, dV, _, _ = attention_backward(q, k, v, do, spec)
+
+    def loss(q_, k_, v_):
+        O = attention_forward(q_, k_, v_, spec)[0]
+        return float(np.sum(np.where(np.isfinite(O), O, 0.0) * do))
+
+    h = 1e-6
+    for name, x, g in (("q", q, dQ), ("k", k, dK), ("v", v, dV)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p, args_m = [q, k, v], [q, k, v]
+            pos = "qkv".index(name)
+            args_p[pos], args_m[pos] = xp, xm
+            num[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        assert np.max(np.abs(num - g)) < 1e-6 * max(1.0, np.max(np.abs(g))), name
+
+
 def test_backward_identical_keys_give_zero_dq():
     """With the identity score_mod every row of dS sums to zero, so if all keys
     are the same vector, dQ_i = scale * (sum_j dS_ij) k = 0."""
