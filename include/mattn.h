@@ -271,8 +271,11 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq);
  * 64, any Sq, Skv >= 1 (a last tile that runs past Sq or Skv reads zero rows,
  * its padding keys are masked and its padding rows are not stored); a block
  * mask built with transposed = 1 (or NULL); position offsets (attn_params
- * q_offset, kv_offset), with a block mask built for the same offsets. Not
- * supported (ATTN_ERR_UNSUPPORTED): paged K/V, the relative-position bias. */
+ * q_offset, kv_offset), with a block mask built for the same offsets: the
+ * gradients of this call's own attention (its o and lse over its keys); the
+ * relative-position bias (a constant of the call: no gradient flows to the
+ * table), not together with offsets. Not supported (ATTN_ERR_UNSUPPORTED):
+ * paged K/V. */
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      const float* lse, const void* dO, void* dq, void* dk, void* dv,
                      void* workspace, size_t workspace_bytes,

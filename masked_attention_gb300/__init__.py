@@ -403,17 +403,19 @@ def attn_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, variant: int = 0, *,
              scale: float = 0.0, window: int = 0, softcap: float = 0.0, alibi_slopes=None,
              doc_id=None, prefix_len=None, block_mask: Optional[BlockMask] = None, status=None,
              timeout_ns: int = 0, fault_inject: int = 0, q_offset: int = 0, kv_offset: int = 0,
-             stream=None) -> None:
+             rel_bias=None, stream=None) -> None:
     """dQ, dK, dV of ``sum(dO * O)``; writes ``dq``, ``dk``, ``dv`` in place.
     ``workspace``: a CUDA tensor of at least ``attn_bwd_workspace_bytes`` bytes.
     ``q_offset``/``kv_offset``: absolute positions of query row 0 and key 0
-    (one shard of a longer sequence; the block mask must be built for them)."""
+    (one shard of a longer sequence; the block mask must be built for them).
+    ``rel_bias``: the forward's relative-position bias table (no gradient)."""
     import torch
     B, Hq, Sq, D = q.shape
     Hkv, Skv = k.shape[1], k.shape[2]
     dtype = F32 if q.dtype == torch.float32 else BF16
     p = _params(dtype, scale, window, softcap, alibi_slopes, doc_id, prefix_len, block_mask,
-                status, timeout_ns, fault_inject, q_offset=q_offset, kv_offset=kv_offset)
+                status, timeout_ns, fault_inject, rel_bias=rel_bias, q_offset=q_offset,
+                kv_offset=kv_offset)
     ws_bytes = workspace.numel() * workspace.element_size()
     st = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
                         _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, B, Hq, Hkv, Sq, Skv, D,
@@ -425,7 +427,8 @@ def attn_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, variant: int = 0, *,
                      scale: float = 0.0, window: int = 0, softcap: float = 0.0,
                      alibi_slopes=None, doc_id=None, prefix_len=None,
                      block_mask: Optional[BlockMask] = None, status=None, timeout_ns: int = 0,
-                     q_offset: int = 0, kv_offset: int = 0, stream=None) -> None:
+                     q_offset: int = 0, kv_offset: int = 0, rel_bias=None,
+                     stream=None) -> None:
     """attn_bwd without a workspace argument, for callers that cannot allocate
     device memory: the library's own fixed array holds the row terms (at most
     B*Hq*Sq = 2,097,152; see include/mattn.h). Writes dq, dk, dv in place."""
@@ -434,7 +437,8 @@ def attn_bwd_noalloc(q, k, v, o, lse, do, dq, dk, dv, variant: int = 0, *,
     Hkv, Skv = k.shape[1], k.shape[2]
     dtype = F32 if q.dtype == torch.float32 else BF16
     p = _params(dtype, scale, window, softcap, alibi_slopes, doc_id, prefix_len, block_mask,
-                status, timeout_ns, q_offset=q_offset, kv_offset=kv_offset)
+                status, timeout_ns, rel_bias=rel_bias, q_offset=q_offset,
+                kv_offset=kv_offset)
     st = lib().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
                                 _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Skv, D, variant,
                                 ctypes.byref(p), _stream(stream))

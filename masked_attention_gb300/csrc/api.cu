@@ -434,7 +434,6 @@ attn_status bwd_check_args(BwdProblem& bp, const void* q, const void* k, const v
                                 Hq, Hkv, Sq, Skv, D, variant, p);
   if (st != ATTN_OK) return st;
   if (p->dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
-  if (variant & ATTN_SCORE_RELBIAS) return ATTN_ERR_UNSUPPORTED;  // forward only
   if (p->page_table) return ATTN_ERR_UNSUPPORTED;                 // forward only
   if (B == 0 || Sq == 0 || Skv == 0) return ATTN_ERR_UNSUPPORTED;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;

@@ -777,6 +777,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (j - i) = base_ji + sgn * c for the column c of this warpgroup's 64
         // (absolute positions: minus dqk)
         const int base_ji = (MODE == kDQ ? c0 - r : r - c0) - (GENERAL ? dqk : 0);
+        // relative-position bias (SCORE bit 4, general instantiation only, no
+        // offsets): the table entry of distance i - j is rb0 + rbs * c,
+        // clamped to the table (the clamped entries belong to padding rows or
+        // keys, which are masked or have P = 0)
+        const float* rbt =
+            (SCORE & 4) ? p.score.rel_bias + (size_t)h * p.score.rb_len : nullptr;
+        const int rb0 = -base_ji + p.score.rb_zero;
+        const int rbs = MODE == kDQ ? -1 : 1;
+        (void)rbt;
+        (void)rb0;
+        (void)rbs;
         const float sgn = MODE == kDQ ? 1.0f : -1.0f;
         // P (and P g) from S, 16 columns at a time, two columns per packed
         // instruction; v keeps P g for dS. An empty row (LSE = -inf) occurs
@@ -823,13 +834,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 8; ++e) {
               const int c = 16 * q + 2 * e;
               const float2 sv = make_float2(v[c], v[c + 1]);
+              float2 rbv = make_float2(0.0f, 0.0f);
+              if constexpr ((SCORE & 4) != 0) {
+                const int last = p.score.rb_len - 1;
+                const int i0 = min(max(rb0 + rbs * c, 0), last);
+                const int i1 = min(max(rb0 + rbs * (c + 1), 0), last);
+                rbv = make_float2(__ldg(rbt + i0), __ldg(rbt + i1));
+              }
               float2 arg;
               if constexpr ((SCORE & 2) == 0) {
-                // log2-unit score: s sl2 (+ ALiBi) - LSE2, one packed FMA each
+                // log2-unit score: s sl2 (+ ALiBi) (+ bias) - LSE2, one packed FMA each
                 float2 bias = nl[e];
                 if constexpr ((SCORE & 1) != 0)
                   bias = ffma2(make_float2(a1, a1), make_float2(float(c), float(c + 1)),
                                fadd2(bias, make_float2(a0, a0)));
+                if constexpr ((SCORE & 4) != 0)
+                  bias = ffma2(rbv, make_float2(kLog2e, kLog2e), bias);
                 arg = ffma2(sv, make_float2(sl2, sl2), bias);
                 gg[e] = make_float2(1.0f, 1.0f);
               } else {
@@ -838,6 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   x = ffma2(make_float2(slope * sgn, slope * sgn),
                             make_float2(float(c), float(c + 1)),
                             fadd2(x, make_float2(slope * float(base_ji), slope * float(base_ji))));
+                if constexpr ((SCORE & 4) != 0) x = fadd2(x, rbv);  // the bias enters before the cap
                 pr[e] = fmul2(x, make_float2(inv_cap, inv_cap));  // tanh argument
               }
               if constexpr ((SCORE & 2) == 0) pr[e] = arg;

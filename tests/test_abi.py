@@ -117,12 +117,12 @@ def test_argument_errors_return_before_launch(M):
     st = M.lib().attn_bwd(*([0x10000] * 10), 1 << 20, 1, 2, 2, 200, 328, 64, M.MASK_CAUSAL,
                           ctypes.byref(p), None)
     assert st == M.ATTN_ERR_UNSUPPORTED
-    # the relative-position bias needs its table, and the backward does not take it
+    # the relative-position bias needs its table, in the backward too
     assert call_fwd(M, variant=M.SCORE_RELBIAS) == M.ATTN_ERR_INVALID_ARG
-    p = M._params(0, 0.0, 0, 0.0, None, None, None, None, None, 0, rel_bias=0x20000)
+    p = M._params(0, 0.0, 0, 0.0, None, None, None, None, None, 0)
     st = M.lib().attn_bwd(*([0x10000] * 10), 1 << 20, 1, 2, 2, 128, 128, 64,
                           M.MASK_CAUSAL | M.SCORE_RELBIAS, ctypes.byref(p), None)
-    assert st == M.ATTN_ERR_UNSUPPORTED
+    assert st == M.ATTN_ERR_INVALID_ARG
     assert call_fwd(M, dtype=7) == M.ATTN_ERR_UNSUPPORTED
     assert call_fwd(M, scale=float("nan")) == M.ATTN_ERR_INVALID_ARG
 

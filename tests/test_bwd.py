@@ -68,7 +68,8 @@ def test_bwd_reduced(name):
 
 # Lengths that are not multiples of the 128-row tile: the last query and key
 # tiles run past Sq and Skv (zero-filled rows, padding keys masked, padding
-# rows not stored); Sq != Skv; a prefix longer than the keys; one position.
+# rows not stored); Sq != Skv; a prefix longer than the keys; one position;
+# and the relative-position bias (which runs the same general kernels).
 RAGGED = {
     "ragged_full_d64": dict(B=2, Hq=2, Hkv=1, Sq=200, Skv=333, D=64),
     "ragged_causal_d128": dict(B=1, Hq=2, Hkv=2, S=300, D=128, causal=True),
@@ -79,6 +80,11 @@ RAGGED = {
     "ragged_prefix_past_keys_d128": dict(B=1, Hq=2, Hkv=1, Sq=130, Skv=390, D=128,
                                          causal=True, prefix=True, prefix_len=[450]),
     "single_position_d64": dict(B=1, Hq=1, Hkv=1, S=1, D=64, causal=True),
+    # the relative-position bias table (a constant of the call: no gradient to it)
+    "relbias_causal_d128": dict(B=1, Hq=2, Hkv=2, S=384, D=128, causal=True, relbias=True),
+    "relbias_alibi_softcap_gqa_ragged_d64": dict(B=2, Hq=4, Hkv=2, S=300, D=64, causal=True,
+                                                 alibi=True, softcap=15.0, relbias=True),
+    "relbias_full_d128": dict(B=1, Hq=2, Hkv=1, Sq=200, Skv=256, D=128, relbias=True),
 }
 
 
