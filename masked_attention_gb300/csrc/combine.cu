@@ -65,11 +65,12 @@ __device__ __forceinline__ uint4 pack16(const float* x) {
 }
 
 // NP: parts the kernel is built for (2, 4 or 8, n <= NP; 0: any n, in
-// chunks of 8). A lane keeps 8 loads of 16 bytes in flight: G = 8 / NP row
-// groups of the warp, each with its NP parts, per pass. (Measured on the
-// merge of 2 to 8 parts of 262,144 rows at D = 128: 8 loads per lane beat 4
-// at 3 and 4 parts by 15-25 %, and loading the first pass's part rows before
-// their LSEs are known was 10-40 % slower.)
+// chunks of 8). A lane keeps 8 loads of 16 bytes in flight (4 for two
+// parts): G = 8 / NP row groups of the warp (2 for two parts), each with its
+// NP parts, per pass. (Measured on the merge of 2 to 8 parts of 262,144 rows
+// at D = 128: 8 loads per lane beat 4 at 3 and 4 parts by 15-25 % and lost
+// to it by 5 % at 2 parts; loading the first pass's part rows before their
+// LSEs are known was 10-40 % slower.)
 template <int D, bool kBf16, int NP, bool kOutBf16 = kBf16>
 __global__ void __launch_bounds__(kCombineThreads)
     combine_kernel(const void* __restrict__ o_parts, const float* __restrict__ lse_parts, int n,
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(kCombineThreads)
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   constexpr int kVec = 16 / kElem;  // elements per lane
   constexpr int P = NP == 0 ? 8 : NP;
-  constexpr int G = 8 / P;  // row groups per pass
+  constexpr int G = P == 2 ? 2 : 8 / P;  // row groups per pass
   const int lane = threadIdx.x & 31;
   const int sub = lane / kLanesPerRow, sl = lane % kLanesPerRow;
   const long long nwarps = (long long)gridDim.x * (kCombineThreads / 32);
@@ -221,7 +222,7 @@ template <int D, bool kBf16, int NP, bool kOutBf16 = kBf16>
 cudaError_t launch_np(const void* o_parts, const float* lse_parts, int n, long long rows,
                       void* o, float* lse, cudaStream_t s) {
   constexpr int kRowsPerWarp = 32 / (D * (kBf16 ? 2 : 4) / 16);
-  constexpr int G = 8 / (NP == 0 ? 8 : NP);
+  constexpr int G = NP == 2 ? 2 : 8 / (NP == 0 ? 8 : NP);
   const long long rows_per_block = (long long)(kCombineThreads / 32) * kRowsPerWarp * G;
   long long blocks = (rows + rows_per_block - 1) / rows_per_block;
   static int per_sm = 0;
