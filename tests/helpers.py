@@ -90,7 +90,10 @@ class DeviceRun:
 # |ref| >= 4 a bf16 value lies on a grid of spacing 1/32 or coarser, so even
 # the correctly rounded result can be 1/64 = 0.0156 away from ref: such an
 # element is exempt from the flat bound when it is within one bf16 ulp of
-# ref. Exempt elements are counted and printed, and their number is capped.
+# ref. Exempt elements are counted and printed, and their number is capped:
+# at most max(16, 0.1 % of the checked elements) beyond the elements where
+# the correctly rounded exact result itself misses the bound (those are
+# counted from ref and printed too).
 BF16_ABS_TOL = 1e-2
 EXEMPT_MIN_ABS = 4.0
 EXEMPT_MAX_FRAC = 1e-3   # at most 0.1 % of the checked elements ...
@@ -101,6 +104,13 @@ def bf16_ulp(ref):
     """Spacing of the bf16 grid at |ref| (8 significant bits)."""
     a = np.abs(np.asarray(ref, dtype=np.float64))
     return np.where(a > 0, 2.0 ** (np.floor(np.log2(np.maximum(a, 1e-30))) - 7), 0.0)
+
+
+def bf16_round(x):
+    """x rounded to bf16 (round to nearest even), back in fp64."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(np.asarray(x, dtype=np.float32)))
+    return t.to(torch.bfloat16).to(torch.float64).numpy()
 
 
 def check_bf16(got, ref, what="", valid=None, tol=BF16_ABS_TOL) -> dict:
@@ -118,14 +128,19 @@ def check_bf16(got, ref, what="", valid=None, tol=BF16_ABS_TOL) -> dict:
     bad = over & ~exempt
     n = int(valid.sum())
     n_exempt = int(exempt.sum())
-    cap = max(EXEMPT_MIN_CAP, int(EXEMPT_MAX_FRAC * n))
+    # elements where even the exact result rounded to bf16 misses the bound:
+    # no bf16 output can meet it there, so they are added to the cap
+    n_forced = int(((np.abs(bf16_round(ref) - ref) > tol) & valid &
+                    (np.abs(ref) >= EXEMPT_MIN_ABS)).sum())
+    cap = max(EXEMPT_MIN_CAP, int(EXEMPT_MAX_FRAC * n)) + n_forced
     vals = err[valid]
     stats = dict(what=what, n=n, max_err=float(vals.max()) if n else 0.0,
                  max_err_not_exempt=float(np.where(exempt, 0.0, err)[valid].max()) if n else 0.0,
-                 exempt=n_exempt, cap=cap)
+                 exempt=n_exempt, forced=n_forced, cap=cap)
     print(f"[bf16 {what}] checked {n}, max|err| {stats['max_err']:.4g}, "
           f"max|err| outside the exemption {stats['max_err_not_exempt']:.4g}, "
-          f"exempt (|ref| >= 4, within 1 ulp) {n_exempt} (cap {cap})")
+          f"exempt (|ref| >= 4, within 1 ulp) {n_exempt} (cap {cap}, of which "
+          f"{n_forced} where the correctly rounded result misses the bound)")
     assert not bad.any(), (what, float(err[bad].max()), int(bad.sum()))
     assert n_exempt <= cap, (what, n_exempt, cap)
     return stats
