@@ -7,26 +7,28 @@
 // page: "FlexAttention" section, the variant list, and the item on exploiting
 // mask sparsity). The score matrix never leaves the SM.
 //
-// Work unit: one 128-row query tile of two query heads (2h, 2h+1) of one batch
-// element; both heads see the same key-tile list because the mask does not
-// depend on the head. Units are taken longest-first (block-mask `order`) by a
-// persistent grid of one CTA per SM.
+// Work unit: two 128-row query tiles ("rows" A and B) that read the same K/V
+// tiles: one query tile of two query heads (2h, 2h+1) of one batch element,
+// which see the same key-tile list because the mask does not depend on the
+// head, or, for multi-head attention without block-mask lists, the query
+// tiles 2q and 2q+1 of one head. Units are taken longest-first (block-mask
+// `order`) by a persistent grid of one CTA per SM.
 //
 // Warp roles (384 threads, three warpgroups):
-//   warps 0-3  softmax for head A (thread t owns query row t: TMEM lane t)
-//   warps 4-7  softmax for head B
+//   warps 0-3  softmax for row A (thread t owns query row t: TMEM lane t)
+//   warps 4-7  softmax for row B
 //   warp  8    TMA producer: Q tiles once per unit, then K/V tiles into a ring
 //   warp  9    MMA issuer (one thread) and TMEM owner
-//   warp  10   second MMA issuer at D = 64 (head B), idle at D = 128
+//   warp  10   second MMA issuer at D = 64 (row B), idle at D = 128
 //   warp  11   idle
 // The third warpgroup hands registers to the softmax warpgroups (setmaxnreg).
 // Tensor memory (512 columns): S_A [0,128), S_B [128,256), O_A, O_B (D columns
 // each) from 256. P (bf16) overwrites the first 64 columns of its S tile and
 // is the A operand of the P.V product, read straight from TMEM.
 //
-// Per key tile j and head X:  S_X = Q_X K_j^T (SS MMA) -> softmax warps read
-// S_X, write P_X -> O_X += P_X V_j (TS MMA). The MMA warp alternates heads so
-// one head's softmax overlaps the other head's products.
+// Per key tile j and row X:  S_X = Q_X K_j^T (SS MMA) -> softmax warps read
+// S_X, write P_X -> O_X += P_X V_j (TS MMA). The MMA warp alternates rows so
+// one row's softmax overlaps the other row's products.
 #pragma once
 
 #include <cmath>
@@ -94,7 +96,13 @@ struct Cfg {
 };
 
 struct Unit {
-  int b, qt, h[2];  // h[1] < 0: single-head unit
+  // Row slot x (softmax warpgroup x) is query tile qt[x] of query head h[x];
+  // h[1] < 0: a single-row unit.
+  int b, qt[2], h[2];
+  // Row slot x's fields by selection, not by indexing: an index that is not a
+  // compile-time constant would put the whole unit in local memory.
+  __device__ __forceinline__ int head(int x) const { return x ? h[1] : h[0]; }
+  __device__ __forceinline__ int qtile(int x) const { return x ? qt[1] : qt[0]; }
   int n_full, n_part;
   const int* lf;
   const int* lp;
@@ -126,10 +134,52 @@ __device__ __forceinline__ int zigzag_unit(int r) {
   return r * (int)gridDim.x + c;
 }
 
-__device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp) {
+// Two kinds of unit. Multi-head attention without block-mask lists pairs the
+// query tiles 2q and 2q + 1 of one head: both rows read the same K/V tiles,
+// so each tile is loaded into shared memory once for two products, as the
+// heads of a GQA group share theirs. The pair visits the union of its rows'
+// key tiles (the later row's causal range); the earlier row masks the tile
+// past its own range element by element like any other masked column.
+// Otherwise a unit is one query tile of the query heads 2h and 2h + 1, which
+// see the same key-tile list because the mask does not depend on the head.
+// Pairs only at D = 128: at D = 64 (separate P, one MMA warp per row) they
+// measured slower than head pairs (causal ALiBi B4 H16 S2048: 91 against 81 us).
+template <int D>
+__host__ __device__ __forceinline__ bool pair_tiles(const FwdProblem& p) {
+  return D == 128 && p.Hq == p.Hkv && p.lists.full_cnt == nullptr;
+}
+
+template <int D>
+__host__ __device__ __forceinline__ int count_units(const FwdProblem& p) {
+  const int nq = (p.Sq + kTile - 1) / kTile;
+  return pair_tiles<D>(p) ? p.B * ((nq + 1) / 2) * p.Hq : p.B * nq * ((p.Hq + 1) / 2);
+}
+
+template <int D>
+__device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u) {
   const int nq = (p.Sq + kTile - 1) / kTile, nkv = (p.Skv + kTile - 1) / kTile;
-  const int rank = u / nhp, hp = u % nhp;
   const bool causal_bound = (p.variant & ATTN_MASK_CAUSAL) && !(p.variant & ATTN_MASK_PREFIX);
+  Unit U;
+  if (pair_tiles<D>(p)) {
+    const int npair = (nq + 1) / 2;
+    const int rank = u / p.Hq, h = u % p.Hq;
+    const int qp = causal_bound ? npair - 1 - rank / p.B : rank % npair;  // longest first
+    U.b = causal_bound ? rank % p.B : rank / npair;
+    U.qt[0] = 2 * qp;
+    U.qt[1] = 2 * qp + 1;
+    U.h[0] = h;
+    U.h[1] = U.qt[1] < nq ? h : -1;
+    const int rows_end = min((U.qtile(U.h[1] >= 0) + 1) * kTile, p.Sq);
+    const int last = causal_bound ? causal_tiles(p.mask, rows_end - 1, nkv) : nkv;
+    const bool masked = (p.variant & ATTN_MASK_BITS) != 0;
+    U.n_full = masked ? 0 : last;
+    U.n_part = masked ? last : 0;
+    U.lf = U.lp = nullptr;
+    U.nkv = nkv;
+    return U;
+  }
+  const int nhp = (p.Hq + 1) / 2;
+  const int rank = u / nhp, hp = u % nhp;
   int row;
   if (p.lists.full_cnt) {
     row = p.lists.order[rank];
@@ -139,9 +189,8 @@ __device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp)
   } else {
     row = rank;
   }
-  Unit U;
   U.b = row / nq;
-  U.qt = row % nq;
+  U.qt[0] = U.qt[1] = row % nq;
   U.h[0] = 2 * hp;
   U.h[1] = 2 * hp + 1 < p.Hq ? 2 * hp + 1 : -1;
   if (p.lists.full_cnt) {
@@ -153,8 +202,8 @@ __device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u, int nhp)
     if (!MATTN_IN_BOUNDS(kSiteFwdList, U.n_part, min(nkv, p.lists.nkv) + 1 - U.n_full))
       U.n_part = 0;
   } else {
-    const int last = causal_bound ? causal_tiles(p.mask, min((U.qt + 1) * kTile, p.Sq) - 1, nkv)
-                                  : nkv;
+    const int last =
+        causal_bound ? causal_tiles(p.mask, min((U.qt[0] + 1) * kTile, p.Sq) - 1, nkv) : nkv;
     const bool masked = (p.variant & ATTN_MASK_BITS) != 0;
     U.n_full = masked ? 0 : last;
     U.n_part = masked ? last : 0;
@@ -223,7 +272,27 @@ struct TileCtx {
   // nullptr: row i = (first row of the warp) + lane and column c read entry
   // 127 + lane - c, the table value for distance i - j.
   const float* rb;
+  // Soft-cap without the bias terms: |s| <= plim (|s / cap| <= 1) allows the
+  // polynomial form s * Q(s^2) of cap * log2(e) * tanh(s / cap) (tanh_poly).
+  float plim;
+  float pa[4];
 };
+
+// Odd polynomial for tanh on [-1, 1]: tanh(y) ~ y * sum_k c_k * y^(2k),
+// a least-squares fit of tanh(y) / y in y^2 on Chebyshev nodes of [0, 1],
+// reweighted toward the minimax relative error: at most 8.2e-5 relative
+// (fp32 Horner evaluation included), below the 2^-10.9 of tanh.approx.
+
+// Coefficients of s * Q(s^2) = cap * log2(e) * tanh(s * sc) for |s * sc| <= 1,
+// with sc = scale / cap: a_k = c_k * sc^(2k+1) * cap * log2(e).
+__device__ __forceinline__ void tanh_poly_coeffs(float sc, float cl2, float* a) {
+  const float sc2 = sc * sc;
+  const float f0 = sc * cl2, f1 = f0 * sc2, f2 = f1 * sc2, f3 = f2 * sc2;
+  a[0] = 0.99991864f * f0;
+  a[1] = -0.3306548f * f1;
+  a[2] = 0.11889856f * f2;
+  a[3] = -0.02663025f * f3;
+}
 
 __device__ __forceinline__ float rb_at(const TileCtx& t, int c) {
   return t.rb[127 + (int)(threadIdx.x & 31) - c];
@@ -323,24 +392,54 @@ __device__ __forceinline__ void transform_cols(float* s, int c0, const TileCtx& 
       for (int c = 0; c < N; ++c) s[c] = fmaf(rb_at(t, c0 + c), kLog2e, s[c]);
     }
   } else {
-    const float b0 = t.slope * (t.base + float(c0));
-    const float2 cl = make_float2(t.cl2, t.cl2), sh2 = make_float2(-shift, -shift);
+    bool poly = false;
+    if constexpr (SCORE == 2) {
+      // Soft-cap alone: where every |s| of the warp's columns is in the
+      // polynomial's range, tanh is evaluated as s * Q(s^2) with packed FMAs
+      // instead of on the special-function unit, which the exponentiation
+      // also needs (tanh.approx takes twice the issue time of ex2.approx
+      // there); otherwise the whole call takes the tanh.approx path below.
+      float mx = 0.0f;
 #pragma unroll
-    for (int c = 0; c < N; c += 2) {
-      float2 y;
-      if constexpr ((SCORE & 3) == 2) {
-        y = fmul2(make_float2(s[c], s[c + 1]), make_float2(t.sc, t.sc));
-      } else {
-        y.x = fmaf(s[c], t.scale, fmaf(t.slope, float(c), b0)) * t.inv_cap;
-        y.y = fmaf(s[c + 1], t.scale, fmaf(t.slope, float(c + 1), b0)) * t.inv_cap;
+      for (int c = 0; c < N; ++c) mx = fmaxf(mx, fabsf(s[c]));
+      if (__all_sync(0xffffffffu, mx <= t.plim)) {
+        const float2 a0 = make_float2(t.pa[0], t.pa[0]), a1 = make_float2(t.pa[1], t.pa[1]),
+                     a2 = make_float2(t.pa[2], t.pa[2]), a3 = make_float2(t.pa[3], t.pa[3]);
+        const float2 sh2 = make_float2(-shift, -shift);
+#pragma unroll
+        for (int c = 0; c < N; c += 2) {
+          const float2 x = make_float2(s[c], s[c + 1]);
+          const float2 u = fmul2(x, x);
+          float2 q = ffma2(a3, u, a2);
+          q = ffma2(q, u, a1);
+          q = ffma2(q, u, a0);
+          const float2 e = ffma2(q, x, sh2);
+          s[c] = e.x;
+          s[c + 1] = e.y;
+        }
+        poly = true;
       }
-      if constexpr (kRB) {  // the bias enters before the cap
-        y.x = fmaf(rb_at(t, c0 + c), t.inv_cap, y.x);
-        y.y = fmaf(rb_at(t, c0 + c + 1), t.inv_cap, y.y);
+    }
+    if (!poly) {
+      const float b0 = t.slope * (t.base + float(c0));
+      const float2 cl = make_float2(t.cl2, t.cl2), sh2 = make_float2(-shift, -shift);
+#pragma unroll
+      for (int c = 0; c < N; c += 2) {
+        float2 y;
+        if constexpr ((SCORE & 3) == 2) {
+          y = fmul2(make_float2(s[c], s[c + 1]), make_float2(t.sc, t.sc));
+        } else {
+          y.x = fmaf(s[c], t.scale, fmaf(t.slope, float(c), b0)) * t.inv_cap;
+          y.y = fmaf(s[c + 1], t.scale, fmaf(t.slope, float(c + 1), b0)) * t.inv_cap;
+        }
+        if constexpr (kRB) {  // the bias enters before the cap
+          y.x = fmaf(rb_at(t, c0 + c), t.inv_cap, y.x);
+          y.y = fmaf(rb_at(t, c0 + c + 1), t.inv_cap, y.y);
+        }
+        const float2 e = ffma2(make_float2(tanh_approx(y.x), tanh_approx(y.y)), cl, sh2);
+        s[c] = e.x;
+        s[c + 1] = e.y;
       }
-      const float2 e = ffma2(make_float2(tanh_approx(y.x), tanh_approx(y.y)), cl, sh2);
-      s[c] = e.x;
-      s[c + 1] = e.y;
     }
   }
   // mask_mod on a partial tile: keep (lo < c <= hi and same document) or
@@ -505,8 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_base_smem;
 
-  const int nhp = (p.Hq + 1) / 2;
-  const int num_units = p.B * ((p.Sq + kTile - 1) / kTile) * nhp;
+  const int num_units = count_units<D>(p);
   const int group = p.Hq / p.Hkv;
 
   if (warp >= 8) {
@@ -523,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
       const int u = zigzag_unit(r);
       if (u >= num_units) continue;
-      const Unit U = decode_unit(p, u, nhp);
+      const Unit U = decode_unit<D>(p, u);
       const int n = U.n();
       if (n == 0) continue;
       const bool two = U.h[1] >= 0;
@@ -534,17 +632,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) {
         mbar_arrive_expect_tx(q_full, (two ? 2 : 1) * C::kTileBytes);
         for (int x = 0; x < (two ? 2 : 1); ++x) {
-          const int slice = U.b * p.Hq + U.h[x];
+          const int slice = U.b * p.Hq + U.head(x);
           for (int bx = 0; bx < C::kBoxes; ++bx)
             tma_load_3d(sQ + x * C::kTileBytes + bx * C::kBoxBytes, &tm_q, q_full, bx * 64,
-                        U.qt * kTile, slice);
+                        U.qtile(x) * kTile, slice);
         }
       }
       __syncwarp();
       ++q_it;
       for (int j = 0; j < n && ok; ++j) {
         const int kt = U.kt(j);
-        const int hks[2] = {hk0, hk1};
         // order: K_A, [K_B], V_A, [V_B]
         for (int t = 0; t < (shared ? 2 : 4) && ok; ++t) {
           const int per = shared ? 1 : 2;
@@ -559,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           load_kv_tile<C::kBoxes, C::kBoxBytes, PAGED>(sSlots + slot * C::kTileBytes,
                                                 is_v ? &tm_v : &tm_k, slot_full + slot,
                                                 p.page_table, p.page_size, p.pages_per_seq,
-                                                p.Skv, p.Hkv, U.b, hks[x], kt, lane, issue);
+                                                p.Skv, p.Hkv, U.b, x ? hk1 : hk0, kt, lane, issue);
           __syncwarp();
           ++slot_it;
         }
@@ -590,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
         const int u = zigzag_unit(r);
         if (u >= num_units) continue;
-        const Unit U = decode_unit(p, u, nhp);
+        const Unit U = decode_unit<D>(p, u);
         const int n = U.n();
         if (n == 0) continue;
         const int nx = U.h[1] >= 0 ? 2 : 1;
@@ -698,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
         const int u = zigzag_unit(r);
         if (u >= num_units) continue;
-        const Unit U = decode_unit(p, u, nhp);
+        const Unit U = decode_unit<D>(p, u);
         const int n = U.n();
         if (n == 0) continue;
         const int nx = U.h[1] >= 0 ? 2 : 1;
@@ -795,16 +892,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.score.scale * kLog2e;              // raw score -> log2 units
     const float sc = p.score.scale / p.score.softcap;      // raw score -> tanh argument
     const float cl2 = p.score.softcap * kLog2e;            // tanh -> log2 units
+    float pa[4];
+    tanh_poly_coeffs(sc, cl2, pa);
+    const float plim = p.score.softcap / p.score.scale;    // |s| <= plim: |s / cap| <= 1
     uint32_t s_it = 0, o_it = 0;
     bool ok = true;
     for (int rr = 0; rr * (int)gridDim.x < num_units && ok; ++rr) {
       const int u = zigzag_unit(rr);
       if (u >= num_units) continue;
-      const Unit U = decode_unit(p, u, nhp);
-      const int h = U.h[x];
+      const Unit U = decode_unit<D>(p, u);
+      const int h = U.head(x);
       if (h < 0) continue;
       const int n = U.n();
-      const int i = U.qt * kTile + t;
+      const int i = U.qtile(x) * kTile + t;
       const bool row_in = i < p.Sq;  // a last query tile may run past Sq
       const size_t orow = ((size_t)(U.b * p.Hq + h) * p.Sq + i);
       __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + orow * D;
@@ -841,7 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // relative-position bias of this head: windows copied one tile ahead
       const float* rtab =
           (SCORE & 4) ? p.score.rel_bias + (size_t)h * p.score.rb_len : nullptr;
-      const int rb_first = U.qt * kTile + (warp & 3) * 32 - 127 + p.score.rb_zero;  // minus j0
+      const int rb_first = U.qtile(x) * kTile + (warp & 3) * 32 - 127 + p.score.rb_zero;  // minus j0
       if (rtab) rb_fill<C::kRbWindow>(wrb, rtab, p.score.rb_len, rb_first - kt_cur * kTile);
       int dcur[4] = {0, 0, 0, 0};
       if (docb && elementwise_tile(U, 0, kt_cur, p.Skv)) {
@@ -888,7 +988,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    min((p.variant & ATTN_MASK_CAUSAL) ? i + dqk - j0 : INT_MAX, p.Skv - 1 - j0),
                    (p.variant & ATTN_MASK_WINDOW) ? i + dqk - j0 - p.mask.window : INT_MIN,
                    P == INT_MIN ? INT_MIN : min(P - p.mask.kv_off, p.Skv) - j0,
-                   docb ? wdoc : nullptr, doc_i, 0u, rb_win};
+                   docb ? wdoc : nullptr, doc_i, 0u, rb_win, plim,
+                   {pa[0], pa[1], pa[2], pa[3]}};
         if (partial) tc.modes = chunk_modes(tc);  // before the wait: off the critical path
         ok = __all_sync(0xffffffffu, wait_bounded(s_full + x, s_it & 1, wd));
         if (!ok) break;
@@ -908,18 +1009,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           load_cols(colS, v0, 2);
           tmem_ld32(colS + 64, *reinterpret_cast<uint32_t(*)[32]>(v1));
           tmem_ld32(colS + 96, *reinterpret_cast<uint32_t(*)[32]>(v1 + 32));
-          if (j == 0) {
-            // A unit's first tile has no reference yet: both halves are
-            // transformed first and the tile's own row maximum becomes the
-            // reference (0 where the whole row is masked), so the largest
-            // weight is exactly 1 as in the max pass below.
+          if (__all_sync(0xffffffffu, m_ref == -INFINITY)) {
+            // No row of the warp has a reference yet (a unit's first tile,
+            // or every earlier tile was masked for all of them): both halves
+            // are transformed first and the tile's own row maximum becomes
+            // the reference, so the largest weight is exactly 1 as in the max
+            // pass below. A row masked in the whole tile keeps no reference
+            // (its weights are 0 here); where some rows of a warp have one
+            // and others not, the others' sums come out infinite or NaN and
+            // the redo below sets their reference from the tile's maximum.
             transform_cols<SCORE, 64>(v0, 0, tc, 0.0f, partial);
             tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(v1));
             tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(v1 + 32));
             transform_cols<SCORE, 64>(v1, 64, tc, 0.0f, partial);
             const float mt = fmaxf(row_max<64>(v0), row_max<64>(v1));
-            m_ref = mt == -INFINITY ? 0.0f : mt;
-            const float2 sh = make_float2(-m_ref, -m_ref);
+            m_ref = mt;
+            const float m_use = mt == -INFINITY ? 0.0f : mt;
+            const float2 sh = make_float2(-m_use, -m_use);
 #pragma unroll
             for (int c = 0; c < 64; c += 2) {
               const float2 e0 = fadd2(make_float2(v0[c], v0[c + 1]), sh);
@@ -1023,7 +1129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 64-byte row segments instead of one 16-byte piece of 32 rows.
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
       uint4* stg = reinterpret_cast<uint4*>(sarea + warp * C::kWarpArea);
-      const int row0 = U.qt * kTile + (warp & 3) * 32;  // the warp's first row
+      const int row0 = U.qtile(x) * kTile + (warp & 3) * 32;  // the warp's first row
       __nv_bfloat16* Oh = static_cast<__nv_bfloat16*>(p.o) + (size_t)(U.b * p.Hq + h) * p.Sq * D;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
@@ -1103,7 +1209,7 @@ cudaError_t launch_typed(const FwdProblem& p, cudaStream_t stream) {
   if (regs < 0 || 2LL * kSoftmaxThreads * kRegsSoftmax + 128LL * kRegsOther >
                       (long long)regs * kThreads)
     return cudaErrorInvalidConfiguration;
-  const int units = p.B * ((p.Sq + kTile - 1) / kTile) * ((p.Hq + 1) / 2);
+  const int units = count_units<D>(p);
   const int grid = units < sm_count() ? units : sm_count();
   if (grid == 0) return cudaSuccess;
   fwd_tc_kernel<D, SCORE, PAGED><<<grid, kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, p);

@@ -101,6 +101,11 @@ BF16_CASES = {
     "odd_heads_gqa_d128": dict(B=1, Hq=3, Hkv=1, S=512, D=128, causal=True),
     "cross_lengths_d64": dict(B=1, Hq=2, Hkv=2, Sq=256, Skv=768, D=64, causal=True,
                               prefix=True, prefix_lo=300, prefix_hi=500),
+    # Soft-caps small against the scores: |s / cap| > 1 in many or most
+    # 32-row groups of a tile, so the tanh.approx form runs beside (cap 3) or
+    # instead of (cap 1) the polynomial one.
+    "softcap1_causal_d128": dict(B=1, Hq=2, Hkv=2, S=512, D=128, causal=True, softcap=1.0),
+    "softcap3_gqa_d64": dict(B=1, Hq=4, Hkv=2, S=640, D=64, causal=True, softcap=3.0),
 }
 
 
