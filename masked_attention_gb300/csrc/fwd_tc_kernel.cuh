@@ -99,10 +99,21 @@ struct Unit {
   // Row slot x (softmax warpgroup x) is query tile qt[x] of query head h[x];
   // h[1] < 0: a single-row unit.
   int b, qt[2], h[2];
-  // Row slot x's fields by selection, not by indexing: an index that is not a
-  // compile-time constant would put the whole unit in local memory.
-  __device__ __forceinline__ int head(int x) const { return x ? h[1] : h[0]; }
-  __device__ __forceinline__ int qtile(int x) const { return x ? qt[1] : qt[0]; }
+  // Row slot x's fields. kRegs: by selection, which keeps the unit in
+  // registers; otherwise by indexing with x, which is not a compile-time
+  // constant and so puts the unit in local memory, read from there where a
+  // field is used. Which is faster depends on the instantiation's register
+  // pressure (measured; see kUnitRegs in the kernel).
+  template <bool kRegs>
+  __device__ __forceinline__ int head(int x) const {
+    if constexpr (kRegs) return x ? h[1] : h[0];
+    else return h[x];
+  }
+  template <bool kRegs>
+  __device__ __forceinline__ int qtile(int x) const {
+    if constexpr (kRegs) return x ? qt[1] : qt[0];
+    else return qt[x];
+  }
   int n_full, n_part;
   const int* lf;
   const int* lp;
@@ -169,7 +180,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u) {
     U.qt[1] = 2 * qp + 1;
     U.h[0] = h;
     U.h[1] = U.qt[1] < nq ? h : -1;
-    const int rows_end = min((U.qtile(U.h[1] >= 0) + 1) * kTile, p.Sq);
+    const int rows_end = min((U.qtile<true>(U.h[1] >= 0) + 1) * kTile, p.Sq);
     const int last = causal_bound ? causal_tiles(p.mask, rows_end - 1, nkv) : nkv;
     const bool masked = (p.variant & ATTN_MASK_BITS) != 0;
     U.n_full = masked ? 0 : last;
@@ -605,6 +616,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_base_smem;
 
   const int num_units = count_units<D>(p);
+  // Unit fields in registers or local memory (Unit::head), as measured per
+  // instantiation: registers gained 2-5 % on the contiguous kernels without
+  // the bias; local memory was faster for the paged kernel without soft-cap
+  // (causal B8 H16 S4096, 16-token pages: 0.71 against 0.80 ms) and for soft-
+  // cap + bias (GQA prefix B2 Hq32 S8192: 1.61 against 1.82 ms), registers
+  // for the paged soft-cap and the ALiBi + bias kernels (1-2 %).
+  constexpr bool kUnitRegs = PAGED ? (SCORE & 2) != 0 : (SCORE & 6) != 6;
   const int group = p.Hq / p.Hkv;
 
   if (warp >= 8) {
@@ -627,15 +645,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool two = U.h[1] >= 0;
       const int hk0 = U.h[0] / group, hk1 = two ? U.h[1] / group : hk0;
       const bool shared = !two || hk0 == hk1;
+      const int hks[2] = {hk0, hk1};
+      auto hk_of = [&](int x) {
+        if constexpr (kUnitRegs) return x ? hk1 : hk0;
+        else return hks[x];
+      };
       ok = __all_sync(0xffffffffu, wait_bounded(q_empty, (q_it & 1) ^ 1, wd));
       if (!ok) break;
       if (leader) {
         mbar_arrive_expect_tx(q_full, (two ? 2 : 1) * C::kTileBytes);
         for (int x = 0; x < (two ? 2 : 1); ++x) {
-          const int slice = U.b * p.Hq + U.head(x);
+          const int slice = U.b * p.Hq + U.head<kUnitRegs>(x);
           for (int bx = 0; bx < C::kBoxes; ++bx)
             tma_load_3d(sQ + x * C::kTileBytes + bx * C::kBoxBytes, &tm_q, q_full, bx * 64,
-                        U.qtile(x) * kTile, slice);
+                        U.qtile<kUnitRegs>(x) * kTile, slice);
         }
       }
       __syncwarp();
@@ -656,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           load_kv_tile<C::kBoxes, C::kBoxBytes, PAGED>(sSlots + slot * C::kTileBytes,
                                                 is_v ? &tm_v : &tm_k, slot_full + slot,
                                                 p.page_table, p.page_size, p.pages_per_seq,
-                                                p.Skv, p.Hkv, U.b, x ? hk1 : hk0, kt, lane, issue);
+                                                p.Skv, p.Hkv, U.b, hk_of(x), kt, lane, issue);
           __syncwarp();
           ++slot_it;
         }
@@ -901,10 +924,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int u = zigzag_unit(rr);
       if (u >= num_units) continue;
       const Unit U = decode_unit<D>(p, u);
-      const int h = U.head(x);
+      const int h = U.head<kUnitRegs>(x);
       if (h < 0) continue;
       const int n = U.n();
-      const int i = U.qtile(x) * kTile + t;
+      const int i = U.qtile<kUnitRegs>(x) * kTile + t;
       const bool row_in = i < p.Sq;  // a last query tile may run past Sq
       const size_t orow = ((size_t)(U.b * p.Hq + h) * p.Sq + i);
       __nv_bfloat16* O = static_cast<__nv_bfloat16*>(p.o) + orow * D;
@@ -941,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // relative-position bias of this head: windows copied one tile ahead
       const float* rtab =
           (SCORE & 4) ? p.score.rel_bias + (size_t)h * p.score.rb_len : nullptr;
-      const int rb_first = U.qtile(x) * kTile + (warp & 3) * 32 - 127 + p.score.rb_zero;  // minus j0
+      const int rb_first = U.qtile<kUnitRegs>(x) * kTile + (warp & 3) * 32 - 127 + p.score.rb_zero;  // minus j0
       if (rtab) rb_fill<C::kRbWindow>(wrb, rtab, p.score.rb_len, rb_first - kt_cur * kTile);
       int dcur[4] = {0, 0, 0, 0};
       if (docb && elementwise_tile(U, 0, kt_cur, p.Skv)) {
@@ -1129,7 +1152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 64-byte row segments instead of one 16-byte piece of 32 rows.
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
       uint4* stg = reinterpret_cast<uint4*>(sarea + warp * C::kWarpArea);
-      const int row0 = U.qtile(x) * kTile + (warp & 3) * 32;  // the warp's first row
+      const int row0 = U.qtile<kUnitRegs>(x) * kTile + (warp & 3) * 32;  // the warp's first row
       __nv_bfloat16* Oh = static_cast<__nv_bfloat16*>(p.o) + (size_t)(U.b * p.Hq + h) * p.Sq * D;
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
