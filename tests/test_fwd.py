@@ -238,3 +238,37 @@ def test_deterministic():
 def test_status_clean_after_runs():
     import masked_attention_gb300 as M
     assert M.attn_check_status() == M.ATTN_OK
+
+
+# Multi-head attention at D = 128 without a block mask runs units of two query
+# tiles of one head (2q, 2q + 1) over the union of their key tiles. Odd tile
+# counts leave a last unit with one row; with a query offset (new tokens after
+# a cached prefix) the two rows' causal ranges differ by a tile, and the
+# earlier row's first visited tile is wholly masked for it.
+PAIR_CASES = {
+    "causal_odd_tiles_q300": dict(B=2, Hq=3, Hkv=3, Sq=300, Skv=300, D=128, causal=True),
+    "causal_offset_q333_k700": dict(B=1, Hq=2, Hkv=2, Sq=333, Skv=700, D=128, causal=True,
+                                    alibi=True),
+    "window_offset_q384_k900": dict(B=1, Hq=2, Hkv=2, Sq=384, Skv=900, D=128, causal=True,
+                                    window=200),
+    "full_q200_k129": dict(B=1, Hq=1, Hkv=1, Sq=200, Skv=129, D=128),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PAIR_CASES))
+def test_bf16_query_tile_pairs(name):
+    import dataclasses
+    import torch
+    import masked_attention_gb300 as M
+    from tests.helpers import guarded_empty, check_canaries, variant_bits
+    w = make_workload(0, seed=560 + sorted(PAIR_CASES).index(name), **PAIR_CASES[name])
+    q_off = max(0, w.Skv - w.Sq)
+    q, k, v = (t.cuda().contiguous() for t in (w.q, w.k, w.v))
+    o = guarded_empty((w.B, w.Hq, w.Sq, w.D), torch.bfloat16)
+    lse = guarded_empty((w.B, w.Hq, w.Sq), torch.float32)
+    M.attn_fwd(q, k, v, o, lse, variant_bits(w), window=w.window or 0, q_offset=q_off)
+    check_canaries()
+    assert M.attn_check_status() == M.ATTN_OK
+    spec = dataclasses.replace(oracle_spec(w), q_offset=q_off)
+    O_ref, L_ref = attention_forward(w.q, w.k, w.v, spec)
+    check(w, o, lse, O_ref, L_ref)
