@@ -272,3 +272,34 @@ def test_bf16_query_tile_pairs(name):
     spec = dataclasses.replace(oracle_spec(w), q_offset=q_off)
     O_ref, L_ref = attention_forward(w.q, w.k, w.v, spec)
     check(w, o, lse, O_ref, L_ref)
+
+
+# Scores that jump far above a row's running reference: the keys of the first
+# key tile (visited last: tiles go from the largest index down) and every query
+# share a large component, so their scores exceed the reference taken from the
+# later tiles by far more than 64 (log2 units). The tile's weights overflow the
+# 2^64 bound, and the kernel redoes it with its true maximum, rescaling l and O.
+# With the soft-cap the shared component also pushes |s / cap| past 1, which
+# sends the polynomial form's columns back to tanh.approx.
+REDO_CASES = {
+    "causal_d128": dict(B=1, Hq=2, Hkv=2, S=768, D=128, causal=True),
+    "gqa_softcap_d128": dict(B=1, Hq=4, Hkv=2, S=640, D=128, causal=True, softcap=50.0),
+    "alibi_d64": dict(B=1, Hq=2, Hkv=2, S=512, D=64, causal=True, alibi=True),
+    "prefix_gqa_d128": dict(B=1, Hq=2, Hkv=1, S=600, D=128, causal=True, prefix=True,
+                            prefix_lo=100, prefix_hi=300),
+}
+
+
+@pytest.mark.parametrize("use_block_mask", [True, False])
+@pytest.mark.parametrize("name", sorted(REDO_CASES))
+def test_bf16_redo_after_large_scores(name, use_block_mask):
+    import torch
+    w = make_workload(0, seed=600 + sorted(REDO_CASES).index(name), **REDO_CASES[name])
+    g = torch.Generator().manual_seed(601)
+    u = torch.randn(w.D, generator=g)
+    u = u / u.norm() * 30.0
+    w.q = (w.q.float() + u).to(w.q.dtype)
+    k = w.k.float()
+    k[:, :, :128] += u
+    w.k = k.to(w.k.dtype)
+    run_and_check(w, use_block_mask=use_block_mask)
