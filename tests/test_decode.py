@@ -153,3 +153,25 @@ def test_decode_argument_checks():
     with pytest.raises(M.AttnError) as e:  # 32 query heads per key/value head > 16 rows
         M.attn_decode(q, k, v, o, lse, 0)
     assert e.value.status == M.ATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_decode_scores_far_above_the_running_max(split):
+    """Keys of one early block score far above the rest (a large component
+    shared with the queries): each split's running maximum jumps by far more
+    than the exponent range when that block arrives, and the merged result
+    still equals the oracle's."""
+    w = make_workload(0, seed=896, B=2, Hq=8, Hkv=2, Sq=1, Skv=3000, D=128, causal=True)
+    g = torch.Generator().manual_seed(897)
+    u = torch.randn(w.D, generator=g)
+    u = u / u.norm() * 30.0
+    w.q = (w.q.float() + u).to(w.q.dtype)
+    k = w.k.float()
+    k[:, :, 64:192] += u
+    w.k = k.to(w.k.dtype)
+    q_off = w.Skv - w.Sq
+    o, lse, _ = run_decode(w, q_off, 0, split)
+    spec = dataclasses.replace(oracle_spec(w), q_offset=q_off)
+    O_ref, L_ref = attention_forward(w.q, w.k, w.v, spec)
+    check_bf16(o.float().cpu().numpy(), O_ref, f"decode large scores split={split}")
+    assert max_abs(lse.cpu().numpy(), L_ref) <= lse_tol(w, L_ref)
