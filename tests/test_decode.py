@@ -157,9 +157,9 @@ def test_decode_argument_checks():
 
 @pytest.mark.parametrize("split", [False, True])
 def test_decode_scores_far_above_the_running_max(split):
-    """Keys of one early block score far above the rest (a large component
-    shared with the queries): each split's running maximum jumps by far more
-    than the exponent range when that block arrives, and the merged result
+    """Keys of one late block score far above the rest (a large component
+    shared with the queries): the running maximum of the split that reaches
+    it jumps by far more than the exponent range there, and the merged result
     still equals the oracle's."""
     w = make_workload(0, seed=896, B=2, Hq=8, Hkv=2, Sq=1, Skv=3000, D=128, causal=True)
     g = torch.Generator().manual_seed(897)
@@ -167,7 +167,7 @@ def test_decode_scores_far_above_the_running_max(split):
     u = u / u.norm() * 30.0
     w.q = (w.q.float() + u).to(w.q.dtype)
     k = w.k.float()
-    k[:, :, 64:192] += u
+    k[:, :, 2500:2628] += u
     w.k = k.to(w.k.dtype)
     q_off = w.Skv - w.Sq
     o, lse, _ = run_decode(w, q_off, 0, split)
