@@ -314,12 +314,14 @@ namespace {
 
 constexpr int kDecodeMaxRows = 16;  // query heads per key/value head times Sq
 
-// Splits of the keys for decode: enough CTAs for about two per SM, at least
-// 128 keys per split, at most 64 splits; chunk = keys per split (multiple of
-// 16). Returns the split count.
+// Splits of the keys for decode: enough CTAs for about eight per SM (more
+// loads in flight: on 16 sequences x 8 key/value heads x 32768 keys, 10
+// splits ran at 0.87 of the measured HBM bandwidth against 0.82-0.85 with 3),
+// at least 128 keys per split, at most 64 splits; chunk = keys per split
+// (multiple of 16). Returns the split count.
 int decode_splits(int B, int Hkv, int Skv, int& chunk) {
   const long long ctas = (long long)B * Hkv;
-  long long want = ctas > 0 ? (2LL * sm_count() + ctas - 1) / ctas : 1;
+  long long want = ctas > 0 ? (8LL * sm_count() + ctas - 1) / ctas : 1;
   long long cap = (Skv + 127) / 128;
   if (want > cap) want = cap;
   if (want > 64) want = 64;
