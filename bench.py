@@ -618,7 +618,10 @@ def run_ours(args, rank: int, world: int) -> None:
 def run_backward(args) -> None:
     """Diagnostic: the backward of the bf16 causal training workload (B=8,
     Hq=Hkv=16, S=4096, D=128) after one forward, timed with CUDA events per
-    launch, in TFLOPS of 2.5 x the forward's unmasked FLOPs."""
+    launch, in TFLOPS of 2.5 x the forward's unmasked FLOPs; one line per
+    path: bf16 operands with their rounding remainders (the minimal
+    workspace), and fp16 operands (a workspace with room for the fp16 copies
+    of Q, K, V, dO; their conversion is inside the timed call)."""
     import torch
 
     import masked_attention_gb300 as M
@@ -632,27 +635,33 @@ def run_backward(args) -> None:
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(M.attn_bwd_workspace_bytes(w.B, w.Hq, w.Sq), dtype=torch.uint8, device=dev)
     bm = M.build_block_mask(variant & 0xF, w.B, w.Sq, w.Skv, transposed=True)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     M.attn_fwd(q, k, v, o, lse, variant, block_mask=bm)
-    for _ in range(max(args.warmup, 3)):
-        M.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, variant, block_mask=bm)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for s_ in range(args.steps):
-        flush.fill_(s_ & 0xFF)
-        ev[s_][0].record()
-        M.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, variant, block_mask=bm)
-        ev[s_][1].record()
-    torch.cuda.synchronize()
-    if M.attn_check_status() != M.ATTN_OK:
-        raise RuntimeError("device status error during the backward")
-    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
-    print(json.dumps({"diagnostic": "backward", "workload": config_dict(w)["workload"],
-                      "ms_per_launch": ms, "flops_per_launch": flops,
-                      "tflops": flops / ms / 1e9, "source_digest": source_digest()}), flush=True)
+    for path, nbytes in (("bf16", M.attn_bwd_workspace_bytes(w.B, w.Hq, w.Sq)),
+                         ("f16", M.attn_bwd_workspace_bytes_f16(w.B, w.Hq, w.Hkv, w.Sq, w.Skv,
+                                                                w.D))):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        for _ in range(max(args.warmup, 3)):
+            M.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, variant, block_mask=bm)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for s_ in range(args.steps):
+            flush.fill_(s_ & 0xFF)
+            ev[s_][0].record()
+            M.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, variant, block_mask=bm)
+            ev[s_][1].record()
+        torch.cuda.synchronize()
+        if M.attn_check_status() != M.ATTN_OK:
+            raise RuntimeError("device status error during the backward")
+        ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+        print(json.dumps({"diagnostic": "backward", "path": path,
+                          "workload": config_dict(w)["workload"],
+                          "workspace_bytes": nbytes, "ms_per_launch": ms,
+                          "flops_per_launch": flops, "tflops": flops / ms / 1e9,
+                          "source_digest": source_digest()}), flush=True)
+        del ws
 
 
 def run_combine(args) -> None:

@@ -261,12 +261,25 @@ attn_status build_block_mask(unsigned variant, const attn_params* p, int B, int 
  * Delta_i = <dO_i, O_i>). */
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq);
 
+/* Bytes of workspace for attn_bwd()'s fp16 path: the row terms, then fp16
+ * copies of q, k, v and dO (about 2 (B Hq Sq + B Hkv Skv) D * 2 bytes more).
+ * A call given at least this much, with Sq and Skv multiples of 128, no
+ * position offsets and no relative-position bias, converts its inputs to fp16
+ * (recording their largest |x|) and, where every |x| <= 60000 and
+ * 2 D max|dO| max|V| <= 60000, computes the gradients from fp16 operands: each
+ * product of a probability or dS term with an input is then one tensor-core
+ * product instead of the bf16 path's two (the bf16 value and its rounding
+ * remainder). Otherwise, and with a smaller workspace, the bf16 path runs.
+ * Both meet the same bound. */
+size_t attn_bwd_workspace_bytes_f16(int B, int Hq, int Hkv, int Sq, int Skv, int D);
+
 /* Backward of the forward above (FlexAttention page, "Performance": a
  * deterministic backward that recomputes intermediates instead of storing
  * them): from q, k, v, o, lse and dO computes
  *   dq [B,Hq,Sq,D], dk and dv [B,Hkv,Skv,D] (dtype p->dtype; with GQA, dk and
  *   dv sum over the query heads of their group).
- * `workspace` is device memory of attn_bwd_workspace_bytes() bytes. No
+ * `workspace` is device memory of attn_bwd_workspace_bytes() bytes, or of
+ * attn_bwd_workspace_bytes_f16() bytes for the fp16 path (see there). No
  * atomics: results are bitwise reproducible. Supported: ATTN_BF16, D = 128 and
  * 64, any Sq, Skv >= 1 (a last tile that runs past Sq or Skv reads zero rows,
  * its padding keys are masked and its padding rows are not stored); a block

@@ -98,6 +98,8 @@ def lib() -> ctypes.CDLL:
         L.build_block_mask.restype = i
         L.attn_bwd_workspace_bytes.argtypes = [i, i, i]
         L.attn_bwd_workspace_bytes.restype = sz
+        L.attn_bwd_workspace_bytes_f16.argtypes = [i, i, i, i, i, i]
+        L.attn_bwd_workspace_bytes_f16.restype = sz
         L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, u, P,
                                vp]
         L.attn_bwd.restype = i
@@ -265,6 +267,11 @@ def attn_block_mask_bytes(B: int, Sq: int, Skv: int, transposed: bool = False) -
 
 def attn_bwd_workspace_bytes(B: int, Hq: int, Sq: int) -> int:
     return int(lib().attn_bwd_workspace_bytes(B, Hq, Sq))
+
+
+def attn_bwd_workspace_bytes_f16(B: int, Hq: int, Hkv: int, Sq: int, Skv: int, D: int) -> int:
+    """Workspace bytes for attn_bwd's fp16 path (fp16 copies of q, k, v, dO)."""
+    return int(lib().attn_bwd_workspace_bytes_f16(B, Hq, Hkv, Sq, Skv, D))
 
 
 def build_block_mask(variant: int, B: int, Sq: int, Skv: int, *, window: int = 0, doc_id=None,

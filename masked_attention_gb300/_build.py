@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libmattn.so")
 LIB_DEBUG_PATH = os.path.join(HERE, "libmattn_debug.so")
 SOURCES = ["api.cu", "mask_build.cu", "fwd_f32.cu", "fwd_tc.cu", "fwd_tc_rb.cu",
-           "fwd_tc_paged.cu", "bwd_tc.cu", "bwd_tc_ragged.cu",
+           "fwd_tc_paged.cu", "bwd_tc.cu", "bwd_tc_ragged.cu", "bwd_tc_f16.cu",
            "bwd_noalloc.cu", "varlen.cu", "combine.cu", "decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",

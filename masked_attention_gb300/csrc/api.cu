@@ -425,6 +425,36 @@ MATTN_API size_t attn_bwd_workspace_bytes(int B, int Hq, int Sq) {
 }
 
 namespace mattn {
+namespace {
+
+// Byte offsets in the workspace of the backward's fp16 path: the Delta row
+// terms, the range record, then the fp16 copies of Q, K, V, dO, each 256-byte
+// aligned. Returns the total.
+struct BwdF16Layout {
+  size_t rec, q16, k16, v16, do16, total;
+};
+
+BwdF16Layout bwd_f16_layout(int B, int Hq, int Hkv, int Sq, int Skv, int D) {
+  BwdF16Layout l;
+  l.rec = align256(sizeof(float) * (size_t)B * Hq * Sq);
+  l.q16 = l.rec + 256;
+  const size_t nq = align256((size_t)B * Hq * Sq * D * 2), nk = align256((size_t)B * Hkv * Skv * D * 2);
+  l.k16 = l.q16 + nq;
+  l.v16 = l.k16 + nk;
+  l.do16 = l.v16 + nk;
+  l.total = l.do16 + nq;
+  return l;
+}
+
+}  // namespace
+}  // namespace mattn
+
+MATTN_API size_t attn_bwd_workspace_bytes_f16(int B, int Hq, int Hkv, int Sq, int Skv, int D) {
+  if (B < 0 || Hq < 0 || Hkv < 0 || Sq < 0 || Skv < 0 || D < 0) return 0;
+  return mattn::bwd_f16_layout(B, Hq, Hkv, Sq, Skv, D).total;
+}
+
+namespace mattn {
 
 // Every check of attn_bwd's arguments except those on the workspace; makes no
 // CUDA call. Fills bp.f on success.
@@ -467,6 +497,18 @@ MATTN_API attn_status attn_bwd(const void* q, const void* k, const void* v, cons
   bp.dk = dk;
   bp.dv = dv;
   bp.delta = static_cast<float*>(workspace);
+  // fp16 path: whole tiles at offset 0 without the bias table, and room for
+  // the copies
+  const BwdF16Layout fl = bwd_f16_layout(B, Hq, Hkv, Sq, Skv, D);
+  if (workspace_bytes >= fl.total && Sq % 128 == 0 && Skv % 128 == 0 && p->q_offset == 0 &&
+      p->kv_offset == 0 && !(variant & ATTN_SCORE_RELBIAS)) {
+    char* w = static_cast<char*>(workspace);
+    bp.f16_max = reinterpret_cast<unsigned*>(w + fl.rec);
+    bp.q16 = w + fl.q16;
+    bp.k16 = w + fl.k16;
+    bp.v16 = w + fl.v16;
+    bp.do16 = w + fl.do16;
+  }
   if (p->block_mask) {
     const attn_block_mask* bm = p->block_mask;
     bp.t_lists = BlockLists{bm->t_full_cnt, bm->t_part_cnt, bm->t_full_idx, bm->t_part_idx,
@@ -532,6 +574,7 @@ const DebugTu kDebugTus[] = {
     {debug_fetch_fwd_tc_paged, debug_clear_fwd_tc_paged},
     {debug_fetch_bwd_tc, debug_clear_bwd_tc},
     {debug_fetch_bwd_tc_ragged, debug_clear_bwd_tc_ragged},
+    {debug_fetch_bwd_tc_f16, debug_clear_bwd_tc_f16},
     {debug_fetch_decode, debug_clear_decode},
     {debug_fetch_combine, debug_clear_combine},
     {debug_fetch_mask_build, debug_clear_mask_build},

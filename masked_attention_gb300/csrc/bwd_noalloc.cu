@@ -62,6 +62,8 @@ MATTN_API attn_status attn_bwd_noalloc(const void* q, const void* k, const void*
   if ((size_t)B * (size_t)Hq * (size_t)Sq > mattn::kMaxRows) return ATTN_ERR_WORKSPACE_TOO_SMALL;
   float* ws = mattn::workspace_address();
   if (!ws) return ATTN_ERR_CUDA;
-  return attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, ws, sizeof(float) * mattn::kMaxRows, B, Hq, Hkv,
-                  Sq, Skv, D, variant, p, stream);
+  // the array holds the row terms only (the exact size: never the fp16 path,
+  // whose copies it has no room for)
+  return attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, ws, attn_bwd_workspace_bytes(B, Hq, Sq), B,
+                  Hq, Hkv, Sq, Skv, D, variant, p, stream);
 }

@@ -54,6 +54,7 @@
 #pragma once
 
 #include <cmath>
+#include <cuda_fp16.h>
 #include <mutex>
 
 #include "host_util.h"
@@ -109,6 +110,11 @@ struct BwdArgs {
   const float* delta;  // Delta, read by the dKV kernel
   float* delta_out;    // Delta, written by the dQ kernel (same buffer)
   BlockLists lists;    // forward lists (dQ) or transposed lists (dKV)
+  // fp16 path: the largest |x| of Q, K, V, dO (float bits; written by the
+  // conversion to fp16) decides between the fp16 kernels and the bf16 ones,
+  // which are both launched and of which one returns at once; nullptr: no
+  // fp16 copies, the bf16 kernels run
+  const unsigned* f16_max;
 };
 
 // One unit of work and its iteration list.
@@ -238,6 +244,17 @@ __device__ __forceinline__ void tanh16(float (&y)[16]) {
   }
 }
 
+// tcgen05 instruction descriptor with fp16 A and B (format fields 0; the
+// bf16 one sets them to 1).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
+  return idesc_bf16(M, N, b_mn_major) & ~((1u << 7) | (1u << 10));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);  // .x = lo (low half), .y = hi
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
 // The bf16 pair of (a, b) and the bf16 pair of their rounding remainders:
 // hi + lo represents a and b to about 2^-17 of their magnitude.
 __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -285,6 +302,18 @@ __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint64_t a_desc, uint6
   mma_ss_warp<K>(d_tmem, a, b, idesc, 0u);
 }
 
+// Whether the fp16 copies of Q, K, V and dO hold the inputs exactly enough
+// and the fp16 operands of the TS products stay in range: every |x| at most
+// 60000 (fp16's largest finite value is 65504), and |dS| <= 2 D max|dO|
+// max|V| at most 60000 (|dP| <= D max|dO| max|V|, and |Delta| too; P and the
+// soft-cap's derivative are at most 1). A NaN fails every test.
+__device__ __forceinline__ bool f16_in_range(const unsigned* mx, int D) {
+  const float q = __uint_as_float(mx[0]), k = __uint_as_float(mx[1]),
+              v = __uint_as_float(mx[2]), d = __uint_as_float(mx[3]);
+  const float lim = 60000.0f;
+  return q <= lim && k <= lim && v <= lim && d <= lim && 2.0f * float(D) * d * v <= lim;
+}
+
 // GENERAL: Sq or Skv is not a multiple of 128, or the call's queries and
 // keys sit at position offsets (a separate instantiation, so the kernel for
 // whole tiles at offset 0 keeps its code unchanged). 3-D tensor maps read
@@ -293,13 +322,19 @@ __device__ __forceinline__ void issue_ss(uint32_t d_tmem, uint64_t a_desc, uint6
 // query rows get LSE +inf in dK/dV (their P is 0), rows past the sequence are
 // not stored; every mask term, ALiBi and the document ids use the absolute
 // positions q_offset + i and kv_offset + j.
-template <int D, int SCORE, int MODE, bool GENERAL>
+// F16: Q, K, V, dO come from fp16 copies and every product takes fp16
+// operands: P, P g and dS rounded once to fp16 (2^-11 relative, against bf16's
+// 2^-8) meet the flat bound without a second, lo part, so each TS product is
+// one product instead of two (dQ: 4 per tile pair, dK/dV: 4, against 5 and 6).
+template <int D, int SCORE, int MODE, bool GENERAL, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const BwdArgs a) {
   using C = BwdCfg<D, MODE>;
   const FwdProblem& p = a.f;
+  // the fp16 and bf16 kernels of an fp16-path call: one of them returns here
+  if (a.f16_max != nullptr && f16_in_range(a.f16_max, D) != F16) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -552,8 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop (waits stay converged) and issues each
     // product as one block (issue_ss, issue_ts); lane 0 issues.
-    constexpr uint32_t kIdescSS = idesc_bf16(128, 128, false);
-    constexpr uint32_t kIdescTS = idesc_bf16(128, D, true);
+    constexpr uint32_t kIdescSS = F16 ? idesc_f16(128, 128, false) : idesc_bf16(128, 128, false);
+    constexpr uint32_t kIdescTS = F16 ? idesc_f16(128, D, true) : idesc_bf16(128, D, true);
     // shared-memory descriptors: K-major (SS operands) and MN-major (B of the
     // TS products) views of the fixed tiles and of ring slot 0; other slots
     // and tiles add their byte offset >> 4
@@ -613,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++p_it;
           tc_fence_after();
           issue_ts(acc0, colS, 0, s1, kIdescTS, acc);
-          issue_ts(acc0, colS, 32, s1, kIdescTS, true);
+          if constexpr (!F16) issue_ts(acc0, colS, 32, s1, kIdescTS, true);
           mma_commit_warp(slot_empty1 + seq % C::kSlots);  // dO read
         } else {
           // B += (P g) K and A += lo K (operands over S)
@@ -622,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++ds_it;
           tc_fence_after();
           issue_ts(acc1, colS, 0, s0, kIdescTS, acc);
-          issue_ts(acc0, colS, 32, s0, kIdescTS, acc);
+          if constexpr (!F16) issue_ts(acc0, colS, 32, s0, kIdescTS, acc);
         }
         __syncwarp();
         if (it + 1 < n) {  // S of the next tile (its P/lo operands over S are consumed)
@@ -640,10 +675,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++ds_it;
           tc_fence_after();
           issue_ts(acc1, colP, 0, s0, kIdescTS, acc);
-          issue_ts(acc1, colP, 32, s0, kIdescTS, true);
+          if constexpr (!F16) issue_ts(acc1, colP, 32, s0, kIdescTS, true);
         } else {
-          // A += hi K (operand over dP)
-          issue_ts(acc0, colP, 0, s0, kIdescTS, true);
+          // A += hi K (operand over dP); with fp16 operands the only part,
+          // so it starts the accumulator
+          issue_ts(acc0, colP, 0, s0, kIdescTS, F16 ? acc : true);
         }
         mma_commit_warp(slot_empty0 + seq % C::kSlots);  // Q or K read
         __syncwarp();
@@ -896,14 +932,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               v[c] = vg.x;
               v[c + 1] = vg.y;
               if constexpr (kKeepP) pf[c] = p0, pf[c + 1] = p1;
-              if constexpr (MODE == kDKV)  // P^T, split, for dV += P^T dO
+              if constexpr (F16) {  // P^T for dV += P^T dO, or P g for B += (P g) K
+                hi16[8 * q2 + e] = MODE == kDKV ? pack_f16x2(p0, p1) : pack_f16x2(vg.x, vg.y);
+              } else if constexpr (MODE == kDKV) {  // P^T, split, for dV += P^T dO
                 split_bf16x2(p0, p1, hi16[8 * q2 + e], lo16[8 * q2 + e]);
-              else  // P g in bf16, for B += (P g) K
+              } else {  // P g in bf16, for B += (P g) K
                 hi16[8 * q2 + e] = pack_bf16x2(vg.x, vg.y);
+              }
             }
           }
           tmem_st16(colS + 16 * h2, hi16);
-          if constexpr (MODE == kDKV) tmem_st16(colS + 32 + 16 * h2, lo16);
+          if constexpr (MODE == kDKV && !F16) tmem_st16(colS + 32 + 16 * h2, lo16);
         }
         if constexpr (MODE == kDKV) {
           tmem_st_wait();
@@ -947,12 +986,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else  // identity or ALiBi score_mod: P g = P
                   dacc = ffma2(vv, dp, dacc);
               }
-              split_bf16x2(ds.x, ds.y, dh[e / 2 + z], dl[e / 2 + z]);
+              if constexpr (F16) dh[e / 2 + z] = pack_f16x2(ds.x, ds.y);
+              else split_bf16x2(ds.x, ds.y, dh[e / 2 + z], dl[e / 2 + z]);
             }
           }
           if constexpr (MODE == kDQ) row_delta += dacc.x + dacc.y;
           tmem_st16(colP + 16 * hh, dh);
-          if constexpr (MODE == kDKV) {
+          if constexpr (F16) {
+            // no lo parts
+          } else if constexpr (MODE == kDKV) {
             if (hh == 0) {
 #pragma unroll
               for (int e = 0; e < 16; ++e) dl0[e] = dl[e];
@@ -1052,7 +1094,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, int SCORE, int MODE, bool GENERAL>
+template <int D, int SCORE, int MODE, bool GENERAL, bool F16>
 cudaError_t launch_one(const BwdArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, const CUtensorMap& mdo, int units,
                        cudaStream_t stream) {
@@ -1060,7 +1102,7 @@ cudaError_t launch_one(const BwdArgs& a, const CUtensorMap& mq, const CUtensorMa
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(bwd_kernel<D, SCORE, MODE, GENERAL>,
+    attr_err = cudaFuncSetAttribute(bwd_kernel<D, SCORE, MODE, GENERAL, F16>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -1071,25 +1113,36 @@ cudaError_t launch_one(const BwdArgs& a, const CUtensorMap& mq, const CUtensorMa
   static std::once_flag regs_once;
   std::call_once(regs_once, [] {
     cudaFuncAttributes fa{};
-    if (cudaFuncGetAttributes(&fa, bwd_kernel<D, SCORE, MODE, GENERAL>) == cudaSuccess) regs = fa.numRegs;
+    if (cudaFuncGetAttributes(&fa, bwd_kernel<D, SCORE, MODE, GENERAL, F16>) == cudaSuccess)
+      regs = fa.numRegs;
   });
   if (regs < 0 || 256LL * kRegsCompute + 128LL * kRegsOther > (long long)regs * kThreads)
     return cudaErrorInvalidConfiguration;
   const int grid = units < sm_count() ? units : sm_count();
   if (grid == 0) return cudaSuccess;
-  bwd_kernel<D, SCORE, MODE, GENERAL><<<grid, kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, mdo, a);
+  bwd_kernel<D, SCORE, MODE, GENERAL, F16>
+      <<<grid, kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, mdo, a);
   return cudaGetLastError();
 }
 
-template <int D, int SCORE, bool GENERAL>
-cudaError_t launch_typed(const BwdProblem& bp, cudaStream_t stream) {
+// Delta-hat from the bf16 O and dO (both paths).
+inline cudaError_t launch_delta(const BwdProblem& bp, cudaStream_t stream) {
   const FwdProblem& f = bp.f;
   const size_t rows = (size_t)f.B * f.Hq * f.Sq;
   delta_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(f.o), static_cast<const __nv_bfloat16*>(bp.dO),
-      bp.delta, rows, D);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+      bp.delta, rows, f.D);
+  return cudaGetLastError();
+}
+
+// One of the two kernels (MODE) of the backward. F16: over the fp16 copies of
+// Q, K, V, dO (whole tiles only). guard: the fp16 path's range record, or
+// nullptr when the call has no fp16 copies.
+template <int D, int SCORE, bool GENERAL, bool F16>
+cudaError_t launch_mode(const BwdProblem& bp, int mode, const unsigned* guard,
+                        cudaStream_t stream) {
+  static_assert(!(F16 && GENERAL), "fp16 copies serve whole tiles at offset 0 only");
+  const FwdProblem& f = bp.f;
   CUtensorMap mq, mk, mv, mdo;
   if constexpr (GENERAL) {  // 3-D views [B*H][S][D]: a tile past the sequence reads zeros
     if (!make_map_bf16_3d(&mq, f.q, (long long)f.B * f.Hq, f.Sq, D) ||
@@ -1098,18 +1151,30 @@ cudaError_t launch_typed(const BwdProblem& bp, cudaStream_t stream) {
         !make_map_bf16_3d(&mdo, bp.dO, (long long)f.B * f.Hq, f.Sq, D))
       return cudaErrorInvalidValue;
   } else {
-    if (!make_map_bf16(&mq, f.q, (long long)f.B * f.Hq * f.Sq, D) ||
-        !make_map_bf16(&mk, f.k, (long long)f.B * f.Hkv * f.Skv, D) ||
-        !make_map_bf16(&mv, f.v, (long long)f.B * f.Hkv * f.Skv, D) ||
-        !make_map_bf16(&mdo, bp.dO, (long long)f.B * f.Hq * f.Sq, D))
+    const CUtensorMapDataType dt =
+        F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    if (!make_map_bf16(&mq, F16 ? bp.q16 : f.q, (long long)f.B * f.Hq * f.Sq, D, dt) ||
+        !make_map_bf16(&mk, F16 ? bp.k16 : f.k, (long long)f.B * f.Hkv * f.Skv, D, dt) ||
+        !make_map_bf16(&mv, F16 ? bp.v16 : f.v, (long long)f.B * f.Hkv * f.Skv, D, dt) ||
+        !make_map_bf16(&mdo, F16 ? bp.do16 : bp.dO, (long long)f.B * f.Hq * f.Sq, D, dt))
       return cudaErrorInvalidValue;
   }
-  BwdArgs a{f, bp.dO, bp.dq, bp.dk, bp.dv, bp.delta, bp.delta, f.lists};
+  BwdArgs a{f, bp.dO, bp.dq, bp.dk, bp.dv, bp.delta, bp.delta, f.lists, guard};
   const int nq = (f.Sq + kTile - 1) / kTile, nkv = (f.Skv + kTile - 1) / kTile;
-  e = launch_one<D, SCORE, kDQ, GENERAL>(a, mq, mk, mv, mdo, f.B * nq * f.Hq, stream);
-  if (e != cudaSuccess) return e;
+  if (mode == kDQ) return launch_one<D, SCORE, kDQ, GENERAL, F16>(a, mq, mk, mv, mdo,
+                                                                   f.B * nq * f.Hq, stream);
   a.lists = bp.t_lists;
-  return launch_one<D, SCORE, kDKV, GENERAL>(a, mq, mk, mv, mdo, f.B * nkv * f.Hkv, stream);
+  return launch_one<D, SCORE, kDKV, GENERAL, F16>(a, mq, mk, mv, mdo, f.B * nkv * f.Hkv, stream);
+}
+
+// The whole bf16 backward: Delta-hat, then the dQ and dK/dV kernels.
+template <int D, int SCORE, bool GENERAL>
+cudaError_t launch_typed(const BwdProblem& bp, cudaStream_t stream) {
+  cudaError_t e = launch_delta(bp, stream);
+  if (e != cudaSuccess) return e;
+  e = launch_mode<D, SCORE, GENERAL, false>(bp, kDQ, nullptr, stream);
+  if (e != cudaSuccess) return e;
+  return launch_mode<D, SCORE, GENERAL, false>(bp, kDKV, nullptr, stream);
 }
 
 }  // namespace

@@ -29,17 +29,19 @@ inline EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2-D view [rows, D] of a contiguous [B, H, S, D] bf16 tensor; box = 128 rows x
-// 64 columns (128 bytes), 128-byte swizzle: the K-major / MN-major operand
-// layout the tcgen05 shared-memory descriptors expect.
-inline bool make_map_bf16(CUtensorMap* map, const void* base, long long rows, int D) {
+// 2-D view [rows, D] of a contiguous [B, H, S, D] bf16 tensor (or, with
+// dt = FLOAT16, an fp16 one of the same layout); box = 128 rows x 64 columns
+// (128 bytes), 128-byte swizzle: the K-major / MN-major operand layout the
+// tcgen05 shared-memory descriptors expect.
+inline bool make_map_bf16(CUtensorMap* map, const void* base, long long rows, int D,
+                          CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * 2};
   cuuint32_t box[2] = {64, 128};
   cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

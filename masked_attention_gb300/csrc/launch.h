@@ -35,6 +35,14 @@ struct BwdProblem {
   void* dv;
   float* delta;        // workspace [B, Hq, Sq]
   BlockLists t_lists;  // transposed lists (per key tile), or full_cnt == nullptr
+  // fp16 path (whole tiles at offset 0, workspace large enough): fp16 copies
+  // of Q, K, V, dO in the workspace and the record of their largest |x|;
+  // nullptr otherwise
+  void* q16 = nullptr;
+  void* k16 = nullptr;
+  void* v16 = nullptr;
+  void* do16 = nullptr;
+  unsigned* f16_max = nullptr;
 };
 
 // Decode (few query rows against a long cache): one CTA per (batch element,
@@ -65,6 +73,7 @@ MATTN_DECLARE_DEBUG_RECORD(fwd_tc_rb)
 MATTN_DECLARE_DEBUG_RECORD(fwd_tc_paged)
 MATTN_DECLARE_DEBUG_RECORD(bwd_tc)
 MATTN_DECLARE_DEBUG_RECORD(bwd_tc_ragged)
+MATTN_DECLARE_DEBUG_RECORD(bwd_tc_f16)
 MATTN_DECLARE_DEBUG_RECORD(decode)
 MATTN_DECLARE_DEBUG_RECORD(combine)
 MATTN_DECLARE_DEBUG_RECORD(mask_build)
@@ -91,6 +100,10 @@ cudaError_t launch_fwd_tc_paged(const FwdProblem& p, cudaStream_t stream);  // p
 cudaError_t launch_bwd_tc(const BwdProblem& p, cudaStream_t stream);
 // Sq or Skv not a multiple of 128, or position offsets (bwd_tc_ragged.cu).
 cudaError_t launch_bwd_tc_ragged(const BwdProblem& p, cudaStream_t stream);
+// fp16 path of the backward (bwd_tc_f16.cu): zero the range record and
+// convert Q, K, V, dO to the fp16 copies; one fp16 kernel (mode: 0 dQ, 1 dK/dV)
+cudaError_t launch_bwd_f16_prepare(const BwdProblem& p, cudaStream_t stream);
+cudaError_t launch_bwd_f16_mode(const BwdProblem& p, int mode, cudaStream_t stream);
 
 // The checks attn_bwd makes on everything but its workspace (no CUDA call);
 // fills bp.f when they pass.

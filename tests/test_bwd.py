@@ -19,7 +19,9 @@ from tests.helpers import (DeviceRun, check_bf16, check_canaries, guarded_empty,
 pytestmark = pytest.mark.gpu
 
 
-def run_bwd(w, use_block_mask=True):
+def run_bwd(w, use_block_mask=True, f16=False):
+    """f16: a workspace with room for the fp16 path's copies (used where the
+    lengths are whole tiles and the inputs in range; else the bf16 path)."""
     import torch
     import masked_attention_gb300 as M
     g = DeviceRun(w, use_block_mask=use_block_mask, transposed=True)
@@ -27,7 +29,9 @@ def run_bwd(w, use_block_mask=True):
     dq = guarded_like(g.q)
     dk = guarded_like(g.k)
     dv = guarded_like(g.v)
-    ws = guarded_empty((M.attn_bwd_workspace_bytes(w.B, w.Hq, w.Sq),), torch.uint8)
+    nbytes = (M.attn_bwd_workspace_bytes_f16(w.B, w.Hq, w.Hkv, w.Sq, w.Skv, w.D) if f16
+              else M.attn_bwd_workspace_bytes(w.B, w.Hq, w.Sq))
+    ws = guarded_empty((nbytes,), torch.uint8)
     M.attn_bwd(g.q, g.k, g.v, O, L, g.do, dq, dk, dv, ws, g.variant, **g.kwargs())
     torch.cuda.synchronize()
     assert M.attn_check_status() == M.ATTN_OK
@@ -61,9 +65,30 @@ CASES = {
 
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_bwd_reduced(name):
+    """Both paths on whole tiles: bf16 operands with their rounding remainders,
+    and fp16 operands (a workspace with the fp16 copies), against one oracle
+    result."""
     w = make_workload(0, seed=500 + sorted(CASES).index(name), backward=True, **CASES[name])
-    _, dq, dk, dv = run_bwd(w)
-    check_grads(w, dq, dk, dv)
+    dQ, dK, dV, _, _ = attention_backward(w.q, w.k, w.v, w.do, oracle_spec(w))
+    for f16 in (False, True):
+        _, dq, dk, dv = run_bwd(w, f16=f16)
+        for nm, got, ref in (("dq", dq, dQ), ("dk", dk, dK), ("dv", dv, dV)):
+            check_bf16(got.float().cpu().numpy(), ref, f"{nm} {w.name} f16={f16}")
+
+
+def test_bwd_f16_out_of_range_takes_the_bf16_path():
+    """Values whose products would leave fp16's range (2 D max|dO| max|V| >
+    60000) with the fp16 path's workspace: the call converts, finds them out of
+    range and runs the bf16 kernels; the gradients still match the oracle and
+    equal those of the bf16 path bit for bit."""
+    import torch
+    w = make_workload(0, seed=509, backward=True, B=1, Hq=2, Hkv=2, S=256, D=64, causal=True)
+    w.v = (w.v.float() * 8.0).to(w.v.dtype)
+    w.do = (w.do.float() * 4.0).to(w.do.dtype)
+    _, dq1, dk1, dv1 = run_bwd(w, f16=False)
+    _, dq2, dk2, dv2 = run_bwd(w, f16=True)
+    assert torch.equal(dq1, dq2) and torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    check_grads(w, dq2, dk2, dv2)
 
 
 # Lengths that are not multiples of the 128-row tile: the last query and key
@@ -103,20 +128,22 @@ def test_bwd_without_block_mask(name):
     check_grads(w, dq, dk, dv)
 
 
-def test_bwd_full_size_workload5_sampled_heads():
-    """The training-step workload at full size; every gradient of three
-    (b, h) heads is checked (heads are independent under MHA)."""
+@pytest.mark.parametrize("f16", [False, True])
+def test_bwd_full_size_workload5_sampled_heads(f16):
+    """The training-step workload at full size, on both paths; every gradient
+    of three (b, h) heads is checked (heads are independent under MHA)."""
     w = make_workload(5)
-    _, dq, dk, dv = run_bwd(w)
+    _, dq, dk, dv = run_bwd(w, f16=f16)
     check_grads(w, dq, dk, dv, heads=[(0, 0), (3, 7), (7, 15)])
 
 
-def test_bwd_deterministic():
+@pytest.mark.parametrize("f16", [False, True])
+def test_bwd_deterministic(f16):
     import torch
     w = make_workload(0, seed=77, backward=True, **CASES["gqa_prefix_softcap_d128"])
-    _, a, b, c = run_bwd(w)
+    _, a, b, c = run_bwd(w, f16=f16)
     for _ in range(2):
-        _, a2, b2, c2 = run_bwd(w)
+        _, a2, b2, c2 = run_bwd(w, f16=f16)
         assert torch.equal(a, a2) and torch.equal(b, b2) and torch.equal(c, c2)
 
 
