@@ -145,7 +145,8 @@ __device__ __forceinline__ int zigzag_unit(int r) {
   return r * (int)gridDim.x + c;
 }
 
-// Two kinds of unit. Multi-head attention without block-mask lists pairs the
+// Two kinds of unit. Multi-head attention without block-mask lists (or with a
+// causal mask alone, whose lists it does not need) pairs the
 // query tiles 2q and 2q + 1 of one head: both rows read the same K/V tiles,
 // so each tile is loaded into shared memory once for two products, as the
 // heads of a GQA group share theirs. The pair visits the union of its rows'
@@ -155,23 +156,29 @@ __device__ __forceinline__ int zigzag_unit(int r) {
 // see the same key-tile list because the mask does not depend on the head.
 // Pairs only at D = 128: at D = 64 (separate P, one MMA warp per row) they
 // measured slower than head pairs (causal ALiBi B4 H16 S2048: 91 against 81 us).
-template <int D>
+// A causal mask alone needs no lists (a tile is full below the diagonal,
+// partial on it, empty above), so on contiguous K/V pairs serve it with or
+// without them (causal B8 H16 S4096 with lists: 0.535 -> 0.520 ms); the paged
+// kernel keeps head pairs there (0.570 against 0.579 ms with 64-token pages).
+template <int D, bool PAGED>
 __host__ __device__ __forceinline__ bool pair_tiles(const FwdProblem& p) {
-  return D == 128 && p.Hq == p.Hkv && p.lists.full_cnt == nullptr;
+  return D == 128 && p.Hq == p.Hkv &&
+         (p.lists.full_cnt == nullptr ||
+          (!PAGED && (p.variant & ATTN_MASK_BITS) == ATTN_MASK_CAUSAL));
 }
 
-template <int D>
+template <int D, bool PAGED>
 __host__ __device__ __forceinline__ int count_units(const FwdProblem& p) {
   const int nq = (p.Sq + kTile - 1) / kTile;
-  return pair_tiles<D>(p) ? p.B * ((nq + 1) / 2) * p.Hq : p.B * nq * ((p.Hq + 1) / 2);
+  return pair_tiles<D, PAGED>(p) ? p.B * ((nq + 1) / 2) * p.Hq : p.B * nq * ((p.Hq + 1) / 2);
 }
 
-template <int D>
+template <int D, bool PAGED>
 __device__ __forceinline__ Unit decode_unit(const FwdProblem& p, int u) {
   const int nq = (p.Sq + kTile - 1) / kTile, nkv = (p.Skv + kTile - 1) / kTile;
   const bool causal_bound = (p.variant & ATTN_MASK_CAUSAL) && !(p.variant & ATTN_MASK_PREFIX);
   Unit U;
-  if (pair_tiles<D>(p)) {
+  if (pair_tiles<D, PAGED>(p)) {
     const int npair = (nq + 1) / 2;
     const int rank = u / p.Hq, h = u % p.Hq;
     const int qp = causal_bound ? npair - 1 - rank / p.B : rank % npair;  // longest first
@@ -615,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_base_smem;
 
-  const int num_units = count_units<D>(p);
+  const int num_units = count_units<D, PAGED>(p);
   // Unit fields in registers or local memory (Unit::head), as measured per
   // instantiation: registers gained 2-5 % on the contiguous kernels without
   // the bias; local memory was faster for the paged kernel without soft-cap
@@ -639,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
       const int u = zigzag_unit(r);
       if (u >= num_units) continue;
-      const Unit U = decode_unit<D>(p, u);
+      const Unit U = decode_unit<D, PAGED>(p, u);
       const int n = U.n();
       if (n == 0) continue;
       const bool two = U.h[1] >= 0;
@@ -710,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
         const int u = zigzag_unit(r);
         if (u >= num_units) continue;
-        const Unit U = decode_unit<D>(p, u);
+        const Unit U = decode_unit<D, PAGED>(p, u);
         const int n = U.n();
         if (n == 0) continue;
         const int nx = U.h[1] >= 0 ? 2 : 1;
@@ -818,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int r = 0; r * (int)gridDim.x < num_units && ok; ++r) {
         const int u = zigzag_unit(r);
         if (u >= num_units) continue;
-        const Unit U = decode_unit<D>(p, u);
+        const Unit U = decode_unit<D, PAGED>(p, u);
         const int n = U.n();
         if (n == 0) continue;
         const int nx = U.h[1] >= 0 ? 2 : 1;
@@ -923,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int rr = 0; rr * (int)gridDim.x < num_units && ok; ++rr) {
       const int u = zigzag_unit(rr);
       if (u >= num_units) continue;
-      const Unit U = decode_unit<D>(p, u);
+      const Unit U = decode_unit<D, PAGED>(p, u);
       const int h = U.head<kUnitRegs>(x);
       if (h < 0) continue;
       const int n = U.n();
@@ -1232,7 +1239,7 @@ cudaError_t launch_typed(const FwdProblem& p, cudaStream_t stream) {
   if (regs < 0 || 2LL * kSoftmaxThreads * kRegsSoftmax + 128LL * kRegsOther >
                       (long long)regs * kThreads)
     return cudaErrorInvalidConfiguration;
-  const int units = count_units<D>(p);
+  const int units = count_units<D, PAGED>(p);
   const int grid = units < sm_count() ? units : sm_count();
   if (grid == 0) return cudaSuccess;
   fwd_tc_kernel<D, SCORE, PAGED><<<grid, kThreads, C::kSmemAlloc, stream>>>(mq, mk, mv, p);
