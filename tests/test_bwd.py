@@ -202,3 +202,15 @@ def test_bwd_position_offsets(name, use_block_mask):
     dQ, dK, dV, _, _ = attention_backward(q, k, v, do, spec)
     for nm, got, ref in (("dq", dq, dQ), ("dk", dk, dK), ("dv", dv, dV)):
         check_bf16(got.float().cpu().numpy(), ref, f"{nm} shard {name}")
+
+
+def test_bwd_f16_workspace_on_ragged_lengths_takes_the_general_path():
+    """A workspace with room for the fp16 copies on lengths that are not whole
+    tiles: the fp16 path does not apply (whole tiles at offset 0 only) and the
+    general bf16 kernels give the same bits as with the minimal workspace."""
+    import torch
+    w = make_workload(0, seed=610, backward=True, **RAGGED["ragged_causal_alibi_softcap_d128"])
+    _, dq1, dk1, dv1 = run_bwd(w, f16=False)
+    _, dq2, dk2, dv2 = run_bwd(w, f16=True)
+    assert torch.equal(dq1, dq2) and torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    check_grads(w, dq2, dk2, dv2)
