@@ -50,7 +50,9 @@
 //   dKV: dV += P_j^T dO (hi, lo) | S_{j+1} | dK += dS_j^T Q (hi, lo) | dP_{j+1}
 //   dQ:  B += (P g)_j K, A += lo_j K | S_{j+1} | A += hi_j K | dP_{j+1}
 // so the next tile's S is computed while the compute warps still work on the
-// current tile's dS.
+// current tile's dS (dKV). In dQ's bf16 path the lo part of A sits over S, so
+// B waits for dS too; with fp16 operands (no lo part) B follows P g at once:
+//   dQ fp16: B += (P g)_j K | S_{j+1} | A += dS_j K | dP_{j+1}
 #pragma once
 
 #include <cmath>
@@ -650,6 +652,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_ts(acc0, colS, 0, s1, kIdescTS, acc);
           if constexpr (!F16) issue_ts(acc0, colS, 32, s1, kIdescTS, true);
           mma_commit_warp(slot_empty1 + seq % C::kSlots);  // dO read
+        } else if constexpr (F16) {
+          // B += (P g) K as soon as P g is stored (over S): with no lo part of
+          // A beside it, the next tile's S follows at once and is computed
+          // while the compute warps work on dS
+          ok = __all_sync(0xffffffffu, wait_bounded(p_full, p_it & 1, wd));
+          if (!ok) break;
+          ++p_it;
+          tc_fence_after();
+          issue_ts(acc1, colS, 0, s0, kIdescTS, acc);
         } else {
           // B += (P g) K and A += lo K (operands over S)
           ok = __all_sync(0xffffffffu, wait_bounded(ds_full, ds_it & 1, wd));
@@ -657,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++ds_it;
           tc_fence_after();
           issue_ts(acc1, colS, 0, s0, kIdescTS, acc);
-          if constexpr (!F16) issue_ts(acc0, colS, 32, s0, kIdescTS, acc);
+          issue_ts(acc0, colS, 32, s0, kIdescTS, acc);
         }
         __syncwarp();
         if (it + 1 < n) {  // S of the next tile (its P/lo operands over S are consumed)
@@ -678,7 +689,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (!F16) issue_ts(acc1, colP, 32, s0, kIdescTS, true);
         } else {
           // A += hi K (operand over dP); with fp16 operands the only part,
-          // so it starts the accumulator
+          // so it starts the accumulator, once dS is stored
+          if constexpr (F16) {
+            ok = __all_sync(0xffffffffu, wait_bounded(ds_full, ds_it & 1, wd));
+            if (!ok) break;
+            ++ds_it;
+            tc_fence_after();
+          }
           issue_ts(acc0, colP, 0, s0, kIdescTS, F16 ? acc : true);
         }
         mma_commit_warp(slot_empty0 + seq % C::kSlots);  // Q or K read
@@ -944,7 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16(colS + 16 * h2, hi16);
           if constexpr (MODE == kDKV && !F16) tmem_st16(colS + 32 + 16 * h2, lo16);
         }
-        if constexpr (MODE == kDKV) {
+        if constexpr (MODE == kDKV || F16) {  // P (dKV) or P g (dQ, fp16) is stored
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
