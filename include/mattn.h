@@ -96,7 +96,9 @@ enum { ATTN_BF16 = 0, ATTN_F32 = 1 };
  *   order               int32 [B*nq]: b*nq+qt by descending full+part count
  *                       (ties by ascending index): longest work first
  * The t_* members hold the transposed lists (per key tile, its query tiles,
- * [B][nkv] and [B][nkv][nq]) when built with transposed = 1, else NULL. */
+ * [B][nkv] and [B][nkv][nq]) when built with transposed = 1, else NULL;
+ * t_order lists their rows batch element by batch element (ascending b),
+ * within one by descending full+part count (ties by ascending index). */
 typedef struct attn_block_mask {
   int B, Sq, Skv;
   int nq, nkv;

@@ -158,7 +158,7 @@ __device__ __forceinline__ BUnit decode_bwd(const BwdArgs& a, int u) {
     row = a.lists.order[rank];
     if (!MATTN_IN_BOUNDS(kSiteBwdList, row, p.B * n_outer)) row = 0;
   } else if (causal_bound)  // longest first: dQ large query tiles first, dKV small key tiles first
-    row = MODE == kDQ ? (rank % p.B) * nq + (nq - 1 - rank / p.B) : (rank % p.B) * nkv + rank / p.B;
+    row = MODE == kDQ ? (rank % p.B) * nq + (nq - 1 - rank / p.B) : rank;  // dKV by batch element
   else row = rank;
   BUnit U;
   U.b = row / n_outer;

@@ -186,18 +186,24 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(MaskArgs m, 
 // tiles (full + partial), descending, ties by row index. Each thread ranks its
 // rows against all others (costs staged in shared memory); large inputs that
 // do not fit fall back to one thread's counting sort over global memory.
+// by_batch (the transposed lists, which only the dK/dV kernel reads): batch
+// element by batch element, longest first within each, so the kernel streams
+// one batch element's queries and dO at a time and they stay in the L2.
 constexpr int kOrderSmemRows = 12288;
 
-__global__ void order_kernel(const int* cnt_full, const int* cnt_part, int n_rows, int n_inner,
-                             int* order) {
+__global__ void order_kernel(const int* cnt_full, const int* cnt_part, int n_rows, int n_outer,
+                             int n_inner, int by_batch, int* order) {
   extern __shared__ int cost[];
+  // rows ranked among themselves: all rows, or those of one batch element
+  const int group = by_batch ? n_outer : n_rows;
   if (n_rows <= kOrderSmemRows) {
     for (int r = threadIdx.x; r < n_rows; r += blockDim.x) cost[r] = cnt_full[r] + cnt_part[r];
     __syncthreads();
     for (int r = threadIdx.x; r < n_rows; r += blockDim.x) {
       const int c = cost[r];
-      int rank = 0;
-      for (int k = 0; k < n_rows; ++k) {
+      const int first = (r / group) * group;
+      int rank = first;
+      for (int k = first; k < first + group; ++k) {
         const int ck = cost[k];
         rank += (ck > c) || (ck == c && k < r);
       }
@@ -207,22 +213,24 @@ __global__ void order_kernel(const int* cnt_full, const int* cnt_part, int n_row
   }
   if (threadIdx.x != 0) return;
   int* hist = cost;  // n_inner + 2 buckets
-  for (int c = 0; c < n_inner + 2; ++c) hist[c] = 0;
-  for (int r = 0; r < n_rows; ++r) {
-    const int c = cnt_full[r] + cnt_part[r];
-    if (MATTN_IN_BOUNDS(kSiteMaskBuild, c, n_inner + 1)) ++hist[c];
-  }
-  int pos = 0;
-  for (int c = n_inner; c >= 0; --c) {
-    const int n = hist[c];
-    hist[c] = pos;
-    pos += n;
-  }
-  for (int r = 0; r < n_rows; ++r) {
-    const int c = cnt_full[r] + cnt_part[r];
-    if (!MATTN_IN_BOUNDS(kSiteMaskBuild, c, n_inner + 1)) continue;
-    const int at = hist[c]++;
-    if (MATTN_IN_BOUNDS(kSiteMaskBuild, at, n_rows)) order[at] = r;
+  for (int first = 0; first < n_rows; first += group) {
+    for (int c = 0; c < n_inner + 2; ++c) hist[c] = 0;
+    for (int r = first; r < first + group; ++r) {
+      const int c = cnt_full[r] + cnt_part[r];
+      if (MATTN_IN_BOUNDS(kSiteMaskBuild, c, n_inner + 1)) ++hist[c];
+    }
+    int pos = first;
+    for (int c = n_inner; c >= 0; --c) {
+      const int n = hist[c];
+      hist[c] = pos;
+      pos += n;
+    }
+    for (int r = first; r < first + group; ++r) {
+      const int c = cnt_full[r] + cnt_part[r];
+      if (!MATTN_IN_BOUNDS(kSiteMaskBuild, c, n_inner + 1)) continue;
+      const int at = hist[c]++;
+      if (MATTN_IN_BOUNDS(kSiteMaskBuild, at, n_rows)) order[at] = r;
+    }
   }
 }
 
@@ -247,7 +255,8 @@ cudaError_t launch_block_mask(const MaskArgs& m, int B, int Sq, int Skv, int tra
                              (int)smem);
     if (e != cudaSuccess) return e;
   }
-  order_kernel<<<1, 1024, smem, stream>>>(cnt_full, cnt_part, n_rows, n_inner, order);
+  order_kernel<<<1, 1024, smem, stream>>>(cnt_full, cnt_part, n_rows, n_outer, n_inner,
+                                          transposed, order);
   return cudaGetLastError();
 }
 

@@ -45,7 +45,8 @@ def compare(w, transposed=True):
                 assert list(got["t_part_idx"][b, kt, :np_]) == list(ref.t_part_idx[b][kt])
         tcost = (ref.t_full_cnt + ref.t_part_cnt).reshape(-1)
         assert sorted(got["t_order"]) == list(range(w.B * bm.nkv))
-        tkeys = [(-tcost[r], r) for r in got["t_order"]]
+        # t_order: batch element by batch element, longest first within each
+        tkeys = [(r // bm.nkv, -tcost[r], r) for r in got["t_order"]]
         assert tkeys == sorted(tkeys)
     return ref
 
