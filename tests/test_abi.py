@@ -198,6 +198,15 @@ def test_block_mask_buffer_checks(M):
                             ctypes.byref(out), None)
     assert st == M.ATTN_ERR_MISALIGNED
     assert M.attn_bwd_workspace_bytes(8, 16, 4096) == 4 * 8 * 16 * 4096
+    # the fp16 path: the row terms, a 256-byte range record, then fp16 copies
+    # of q, k, v, dO, each 256-byte aligned
+    a256 = lambda x: (x + 255) // 256 * 256
+    for B, Hq, Hkv, Sq, Skv, D in ((8, 16, 16, 4096, 4096, 128), (2, 32, 8, 640, 384, 64)):
+        rows = a256(4 * B * Hq * Sq)
+        q = a256(2 * B * Hq * Sq * D)
+        k = a256(2 * B * Hkv * Skv * D)
+        assert M.attn_bwd_workspace_bytes_f16(B, Hq, Hkv, Sq, Skv, D) == rows + 256 + 2 * q + 2 * k
+    assert M.attn_bwd_workspace_bytes_f16(-1, 1, 1, 1, 1, 64) == 0
 
 
 def test_combine_binding_refuses_strided_views(M):
